@@ -1,0 +1,91 @@
+"""The invariant that pins the verify step end to end.
+
+"Efficient LLM Challenge Results", section 3: under greedy verification
+speculative decoding leaves the output unchanged, whatever the drafts; drafts
+padded with -1 sentinels stay lossless.  On a toy W4A16 target with an int8
+lm_head (oracle/toy_model.py), speculative decoding with random, perfect,
+perfect-then-wrong, all-sentinel, K=0, K=15 and K=20 drafters must emit the
+same tokens as plain greedy decoding, token for token.
+"""
+import numpy as np
+import pytest
+
+from oracle.toy_model import ToyWeights, greedy_decode, spec_decode
+from speculative_decoding_verify_w4a16_gb300 import inputs
+
+
+def _weights(seed, V):
+    E, layers, W8, s8 = inputs.toy_model_arrays(seed, V=V, H=256, layers=2)
+    return ToyWeights(E, layers, W8, s8)
+
+
+def _drafters(w, seed):
+    rng = np.random.default_rng(seed)
+    V = w.V
+
+    def random(ctx, K):
+        return [int(x) for x in rng.integers(0, V, K)]
+
+    def perfect(ctx, K):
+        return greedy_decode(w, ctx, K)
+
+    def perfect_then_wrong(ctx, K):
+        good = greedy_decode(w, ctx, K)
+        j = int(rng.integers(0, K + 1))
+        tail = [(g + 1 + int(rng.integers(0, V - 1))) % V for g in good[j:]]
+        return good[:j] + tail
+
+    def sentinel(ctx, K):
+        return [-1] * K
+
+    def padded(ctx, K):
+        L = int(rng.integers(0, K + 1))
+        return greedy_decode(w, ctx, L) + [-1] * (K - L)
+
+    return dict(random=random, perfect=perfect, perfect_then_wrong=perfect_then_wrong,
+                sentinel=sentinel, padded=padded)
+
+
+CASES = (("random", 15), ("perfect", 15), ("perfect_then_wrong", 15),
+         ("sentinel", 20), ("padded", 20), ("random", 0), ("perfect", 4))
+
+
+@pytest.mark.parametrize("V", [64, 1024])
+def test_spec_decode_equals_greedy(V):
+    w = _weights(11, V)
+    n_prompts = 6 if V == 64 else 3
+    n_new = 24
+    for p in range(n_prompts):
+        prompt = inputs.random_tokens(100 + p, 1 + p % 5, V)
+        want = greedy_decode(w, prompt, n_new)
+        drafters = _drafters(w, 1000 + p)
+        for name, K in CASES:
+            stats = {}
+            got = spec_decode(w, prompt, n_new, K, drafters[name], stats)
+            assert got == want, (V, p, name, K)
+            if name == "perfect" and K > 0:
+                # a perfect drafter is fully accepted: K+1 tokens per verify step
+                assert stats["steps"] == -(-n_new // (K + 1))
+            if name == "sentinel":
+                assert stats["accepted"] == 0
+
+
+@pytest.mark.slow
+def test_spec_decode_equals_greedy_many_prompts():
+    w = _weights(12, 64)
+    for p in range(100):
+        prompt = inputs.random_tokens(500 + p, 1 + p % 7, 64)
+        want = greedy_decode(w, prompt, 20)
+        drafters = _drafters(w, 2000 + p)
+        for name, K in (("random", 15), ("perfect_then_wrong", 15), ("padded", 20)):
+            assert spec_decode(w, prompt, 20, K, drafters[name]) == want, (p, name)
+
+
+def test_toy_model_is_context_dependent():
+    """Guards the invariant test against a degenerate model whose greedy output
+    ignores the context (which would make it pass trivially)."""
+    w = _weights(11, 64)
+    outs = {tuple(greedy_decode(w, inputs.random_tokens(300 + i, 3, 64), 12)) for i in range(8)}
+    assert len(outs) >= 4
+    seq = greedy_decode(w, [1, 2, 3], 24)
+    assert len(set(seq)) >= 3
