@@ -1,0 +1,153 @@
+/*
+ * w4v.h -- C ABI of libw4v, the GB300 (sm_103a) speculative-decoding verify
+ * step for a W4A16 target with an int8 lm_head.
+ *
+ * The operations follow the statement of the problem in "Efficient LLM
+ * Challenge Results" (AdaptFM @ ICML 2026):
+ *   - section 3 "Speculative decoding did the heavy lifting": a drafter
+ *     proposes K tokens, the target runs all K+1 positions in one forward
+ *     pass, and greedy verification keeps the longest draft prefix equal to
+ *     the target's own tokens; drafts may be padded to a constant K with -1
+ *     sentinels, which are never accepted (runner-up paragraph);
+ *   - sections 3 and 5 "Quantization was common, but not the deciding lever":
+ *     the target's projections are 4-bit W4A16 GPTQ with group size 128 and
+ *     fp16 activations, and its untied lm_head is quantized to 8 bits;
+ *   - section 2 "Where the time goes": decode is bound by reading the weights
+ *     from HBM, so the K+1 positions share one weight read.
+ * The pages give no interface; this one is the plainest that carries those
+ * operations.
+ *
+ * Conventions (all entry points):
+ *   - fp16 data is passed as uint16_t holding IEEE-754 binary16 bit patterns.
+ *   - Matrices are dense row-major with the leading dimension equal to the
+ *     row length given.  Device pointers must be 16-byte aligned.
+ *   - The caller owns every buffer, including the workspace; no entry point
+ *     allocates device memory.  A workspace must be zero-filled once before
+ *     its first use; every call that returns W4V_OK leaves it zero-filled
+ *     again, so it can be reused by the next call on the same stream.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream).
+ *     Argument, shape and alignment errors are returned before anything is
+ *     launched.  A launch failure returns W4V_ERR_CUDA.  A kernel that gives
+ *     up on an internal wait (bounded at about two seconds) records
+ *     W4V_ERR_TIMEOUT in a device status word read by w4v_get_status(); after
+ *     that the workspace must be zero-filled again.
+ *   - Nothing here is thread-safe against concurrent use of the same
+ *     workspace; distinct workspaces may be used concurrently.
+ */
+#ifndef W4V_H
+#define W4V_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* A cudaStream_t. */
+typedef struct CUstream_st *w4v_stream_t;
+
+typedef enum {
+    W4V_OK = 0,
+    W4V_ERR_ARG = 1,        /* null pointer or invalid enum/flag            */
+    W4V_ERR_SHAPE = 2,      /* unsupported sizes (see each entry point)     */
+    W4V_ERR_ALIGN = 3,      /* pointer not 16-byte aligned                  */
+    W4V_ERR_WORKSPACE = 4,  /* workspace missing or smaller than required   */
+    W4V_ERR_ARCH = 5,       /* current device is not sm_103 (GB300)         */
+    W4V_ERR_CUDA = 6,       /* CUDA runtime / launch error                  */
+    W4V_ERR_TIMEOUT = 7     /* a kernel abandoned a bounded wait            */
+} w4v_status;
+
+/* Short English text for a status code (static storage, never NULL). */
+const char *w4v_status_string(w4v_status status);
+
+/* Checks that the current device is compute capability 10.3 and runs one
+ * tiny kernel, so that a library built for another architecture fails here
+ * rather than at the first real launch ("DFlash K=15 for Qwen3.5-4B on a
+ * single A10G", section "What transfers": build for the card you run on).
+ * Idempotent per device; every entry point calls it implicitly. */
+w4v_status w4v_init(void);
+
+/* Synchronizes `stream`, then returns and clears the device status word of
+ * the current device: W4V_OK, or W4V_ERR_TIMEOUT if a kernel gave up a wait
+ * since the last call. */
+w4v_status w4v_get_status(w4v_stream_t stream);
+
+/* ------------------------------------------------------- int4 weight packing
+ * The logical W4A16 weight is q[N][K], one 4-bit code (0..15) per byte, with
+ * w[n][k] = s[k/G][n] * (q[n][k] - z) (z = 8, or a per-group zero table).
+ * The device format is this library's own tile layout: N is split into tiles
+ * of 128 rows (the last one zero-padded), K into groups of 128; every
+ * (tile, group) block is 8192 contiguous bytes, blocks ordered tile-major.
+ * Inside a block, 16-byte chunk j (j = 0..3, k = 32j..32j+31 of the group)
+ * of row r sits at byte (j*128 + r)*16 and holds four little-endian 32-bit
+ * words; word w covers k = 32j+8w .. +7 with nibble i holding the code of
+ * k offset {0,2,4,6,1,3,5,7}[i].
+ * Sizes: K % 128 == 0, N % 8 == 0, N, K > 0.  Host memory only. */
+size_t w4v_packed_bytes(int N, int K);
+w4v_status w4v_pack_int4(const uint8_t *q_host, int N, int K, void *packed_host_out);
+/* Inverse of w4v_pack_int4 (rows >= N of the padded tile are dropped). */
+w4v_status w4v_unpack_int4(const void *packed_host, int N, int K, uint8_t *q_host_out);
+
+/* ------------------------------------------------------------- w4a16_gemm
+ * C[M][N] = A[M][K] * W^T, W[n][k] = scales[k/G][n] * (q[n][k] - z[k/G][n]),
+ * z = 8 when zeros == NULL (symmetric GPTQ) else the uint8 table
+ * zeros[K/G][N] (values 0..15, AWQ style).  A, scales, C are fp16; products
+ * are accumulated in fp32 per group, each group's sum is multiplied by its
+ * scale in fp32, and C is rounded to fp16 (round to nearest even).  The
+ * per-element arithmetic does not depend on M for M <= 32.
+ *   A        device, fp16 [M][K]
+ *   Bq       device, packed int4 from w4v_pack_int4 (w4v_packed_bytes(N,K))
+ *   scales   device, fp16 [K/G][N]
+ *   zeros    device, uint8 [K/G][N] or NULL (requires N % 16 == 0)
+ *   group    must be 128
+ *   C        device, fp16 [M][N] (written, never read)
+ * Sizes: 0 <= M <= 32 (M == 0 is a no-op), N % 8 == 0, K % 128 == 0.
+ * Workspace: w4a16_workspace_bytes(M, N, K) bytes, zero-filled before first
+ * use (split-K partial sums and per-tile arrival counters). */
+size_t w4a16_workspace_bytes(int M, int N, int K);
+w4v_status w4a16_gemm(const uint16_t *A, const void *Bq, const uint16_t *scales,
+                      const uint8_t *zeros, int group, uint16_t *C, int M, int N, int K,
+                      void *workspace, size_t workspace_bytes, w4v_stream_t stream);
+
+/* ------------------------------------------------------- w8_lmhead_argmax
+ * Greedy token per row: argmax_out[r] = argmax_v scale[v] * sum_k X[r][k]*W[v][k],
+ * int8 weights, one fp16 scale per vocabulary row, fp32 accumulation with
+ * the scale applied to the finished sum.  Ties go to the lowest v; a NaN
+ * logit counts as -inf; -0 equals +0.  Full logits are never written unless
+ * logits_debug is given.
+ *   X              device, fp16 [M][K]
+ *   W              device, int8 [V][K]
+ *   scale          device, fp16 [V]
+ *   argmax_out     device, int32 [M]
+ *   maxlogit       device, float [M] or NULL: the winning logit
+ *   logits_debug   device, float [M][V] or NULL: every logit (testing aid)
+ * Sizes: 0 <= M <= 128, K % 128 == 0, V % 8 == 0, V > 0.
+ * Workspace: w8_lmhead_argmax_workspace_bytes(M, V) bytes, zero-filled
+ * before first use (per-CTA best keys and an arrival counter). */
+size_t w8_lmhead_argmax_workspace_bytes(int M, int V);
+w4v_status w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uint16_t *scale,
+                            int M, int K, int V, int32_t *argmax_out, float *maxlogit,
+                            float *logits_debug, void *workspace, size_t workspace_bytes,
+                            w4v_stream_t stream);
+
+/* ----------------------------------------------------------- spec_accept
+ * Longest-prefix greedy acceptance for B sequences:
+ *   n[b] = the largest j <= K with draft[b][i] == target[b][i] for all i < j,
+ * where a negative draft (the -1 padding sentinel) never matches.  The
+ * emitted tokens are target[b][0..n[b]] (= drafts 0..n-1 then the target's
+ * own next token); out_tokens[b][j] = target[b][j] for j <= n[b], else -1.
+ *   target      device, int32 [B][K+1]: the target's greedy token after
+ *               each verify position (row b*(K+1)+j of the verify block)
+ *   draft       device, int32 [B][K] (may be NULL when K == 0)
+ *   n_accepted  device, int32 [B]
+ *   out_tokens  device, int32 [B][K+1] or NULL
+ * Sizes: B >= 0 (0 is a no-op), 0 <= K <= 1024. */
+w4v_status spec_accept(const int32_t *target, const int32_t *draft, int B, int K,
+                       int32_t *n_accepted, int32_t *out_tokens, w4v_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* W4V_H */

@@ -1,0 +1,148 @@
+// api.cpp -- the C ABI: argument validation (before anything touches the
+// GPU), workspace sizing, the host int4 packer, and dispatch to launchers.
+#include <cstring>
+
+#include "runtime.h"
+
+namespace {
+
+constexpr int kGroup = 128;
+constexpr int kTile = 128;
+constexpr int kBlockBytes = kTile * kGroup / 2;
+// Nibble i of a packed word holds the code of k offset kNibbleK[i].
+constexpr int kNibbleK[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+
+inline size_t packed_offset(int t, int g, int n_groups, int r, int j) {
+    return (size_t(t) * n_groups + g) * kBlockBytes + (size_t(j) * kTile + r) * 16;
+}
+
+bool pack_shape_ok(int N, int K) { return N > 0 && K > 0 && K % kGroup == 0 && N % 8 == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char *w4v_status_string(w4v_status s) {
+    switch (s) {
+        case W4V_OK: return "ok";
+        case W4V_ERR_ARG: return "invalid argument (null pointer or bad flag)";
+        case W4V_ERR_SHAPE: return "unsupported shape";
+        case W4V_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case W4V_ERR_WORKSPACE: return "workspace missing or too small";
+        case W4V_ERR_ARCH: return "current device is not sm_103 (GB300) or the library was built for another GPU";
+        case W4V_ERR_CUDA: return "CUDA runtime or launch error";
+        case W4V_ERR_TIMEOUT: return "a kernel abandoned a bounded wait";
+    }
+    return "unknown status";
+}
+
+size_t w4v_packed_bytes(int N, int K) {
+    if (!pack_shape_ok(N, K)) return 0;
+    const size_t tiles = (size_t(N) + kTile - 1) / kTile;
+    return tiles * size_t(K / kGroup) * kBlockBytes;
+}
+
+w4v_status w4v_pack_int4(const uint8_t *q, int N, int K, void *out) {
+    if (q == nullptr || out == nullptr) return W4V_ERR_ARG;
+    if (!pack_shape_ok(N, K)) return W4V_ERR_SHAPE;
+    const int n_groups = K / kGroup;
+    const int n_tiles = (N + kTile - 1) / kTile;
+    uint8_t *o = static_cast<uint8_t *>(out);
+    for (int t = 0; t < n_tiles; ++t)
+        for (int g = 0; g < n_groups; ++g)
+            for (int r = 0; r < kTile; ++r) {
+                const int n = t * kTile + r;
+                for (int j = 0; j < 4; ++j) {
+                    uint8_t *chunk = o + packed_offset(t, g, n_groups, r, j);
+                    for (int w = 0; w < 4; ++w) {
+                        const int k0 = g * kGroup + 32 * j + 8 * w;
+                        uint32_t word = 0;
+                        for (int i = 0; i < 8; ++i) {
+                            const uint32_t code = n < N ? (q[size_t(n) * K + k0 + kNibbleK[i]] & 15u) : 8u;
+                            word |= code << (4 * i);
+                        }
+                        for (int b = 0; b < 4; ++b) chunk[4 * w + b] = uint8_t(word >> (8 * b));
+                    }
+                }
+            }
+    return W4V_OK;
+}
+
+w4v_status w4v_unpack_int4(const void *packed, int N, int K, uint8_t *q) {
+    if (q == nullptr || packed == nullptr) return W4V_ERR_ARG;
+    if (!pack_shape_ok(N, K)) return W4V_ERR_SHAPE;
+    const int n_groups = K / kGroup;
+    const uint8_t *p = static_cast<const uint8_t *>(packed);
+    for (int n = 0; n < N; ++n) {
+        const int t = n / kTile, r = n % kTile;
+        for (int g = 0; g < n_groups; ++g)
+            for (int j = 0; j < 4; ++j) {
+                const uint8_t *chunk = p + packed_offset(t, g, n_groups, r, j);
+                for (int w = 0; w < 4; ++w) {
+                    uint32_t word = 0;
+                    for (int b = 0; b < 4; ++b) word |= uint32_t(chunk[4 * w + b]) << (8 * b);
+                    const int k0 = g * kGroup + 32 * j + 8 * w;
+                    for (int i = 0; i < 8; ++i) q[size_t(n) * K + k0 + kNibbleK[i]] = uint8_t((word >> (4 * i)) & 15u);
+                }
+            }
+    }
+    return W4V_OK;
+}
+
+size_t w4a16_workspace_bytes(int M, int N, int K) {
+    if (M < 0 || M > 32 || !pack_shape_ok(N, K)) return 0;
+    return w4v::w4a16_decode_ws_bytes(M, N, K);
+}
+
+w4v_status w4a16_gemm(const uint16_t *A, const void *Bq, const uint16_t *scales, const uint8_t *zeros,
+                      int group, uint16_t *C, int M, int N, int K, void *ws, size_t ws_bytes,
+                      w4v_stream_t stream) {
+    if (M < 0 || N <= 0 || K <= 0) return W4V_ERR_SHAPE;
+    if (group != kGroup) return W4V_ERR_SHAPE;
+    if (K % kGroup != 0 || N % 8 != 0 || M > 32) return W4V_ERR_SHAPE;
+    if (zeros != nullptr && N % 16 != 0) return W4V_ERR_SHAPE;
+    if (M == 0) return W4V_OK;
+    if (A == nullptr || Bq == nullptr || scales == nullptr || C == nullptr) return W4V_ERR_ARG;
+    if (!w4v::aligned16(A) || !w4v::aligned16(Bq) || !w4v::aligned16(scales) ||
+        (zeros != nullptr && !w4v::aligned16(zeros)))
+        return W4V_ERR_ALIGN;
+    if (ws == nullptr || ws_bytes < w4v::w4a16_decode_ws_bytes(M, N, K)) return W4V_ERR_WORKSPACE;
+    if (!w4v::aligned16(ws)) return W4V_ERR_ALIGN;
+    return w4v::launch_w4a16_decode(A, Bq, scales, zeros, C, M, N, K, ws,
+                                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t w8_lmhead_argmax_workspace_bytes(int M, int V) {
+    if (M < 0 || M > 128 || V <= 0) return 0;
+    return w4v::w8_lmhead_ws_bytes(M, V);
+}
+
+w4v_status w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uint16_t *scale, int M, int K,
+                            int V, int32_t *argmax_out, float *maxlogit, float *logits_debug,
+                            void *ws, size_t ws_bytes, w4v_stream_t stream) {
+    if (M < 0 || M > 128 || K <= 0 || V <= 0 || K % 128 != 0 || V % 8 != 0) return W4V_ERR_SHAPE;
+    if (M == 0) return W4V_OK;
+    if (X == nullptr || W == nullptr || scale == nullptr || argmax_out == nullptr) return W4V_ERR_ARG;
+    if (!w4v::aligned16(X) || !w4v::aligned16(W) || !w4v::aligned16(scale)) return W4V_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(argmax_out) & 3u) || (reinterpret_cast<uintptr_t>(maxlogit) & 3u) ||
+        (reinterpret_cast<uintptr_t>(logits_debug) & 3u))
+        return W4V_ERR_ALIGN;
+    if (ws == nullptr || ws_bytes < w4v::w8_lmhead_ws_bytes(M, V)) return W4V_ERR_WORKSPACE;
+    if (!w4v::aligned16(ws)) return W4V_ERR_ALIGN;
+    return w4v::launch_w8_lmhead_argmax(X, W, scale, M, K, V, argmax_out, maxlogit, logits_debug, ws,
+                                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+w4v_status spec_accept(const int32_t *target, const int32_t *draft, int B, int K, int32_t *n_accepted,
+                       int32_t *out_tokens, w4v_stream_t stream) {
+    if (B < 0 || K < 0 || K > 1024) return W4V_ERR_SHAPE;
+    if (B == 0) return W4V_OK;
+    if (target == nullptr || n_accepted == nullptr || (K > 0 && draft == nullptr)) return W4V_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(target) & 3u) || (reinterpret_cast<uintptr_t>(draft) & 3u) ||
+        (reinterpret_cast<uintptr_t>(n_accepted) & 3u) || (reinterpret_cast<uintptr_t>(out_tokens) & 3u))
+        return W4V_ERR_ALIGN;
+    return w4v::launch_spec_accept(target, draft, B, K, n_accepted, out_tokens,
+                                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

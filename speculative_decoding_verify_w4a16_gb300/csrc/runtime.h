@@ -1,0 +1,60 @@
+// runtime.h -- internal host-side helpers shared by the launchers (not part
+// of the public ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/w4v.h"
+
+namespace w4v {
+
+// Upper bound on the CTAs of one persistent launch; it sizes workspaces
+// without querying a device.
+constexpr int kMaxCtas = 256;
+
+struct DeviceInfo {
+    int sm_count = 0;
+    uint32_t *status = nullptr;   // device status word (bit per w4v_status code)
+};
+
+// Arch check, smoke launch and per-device facts for the current device
+// (cached after the first successful call on that device).
+w4v_status device_info(const DeviceInfo **out);
+
+// Row-major 2-D tensor map: `outer` rows of `inner` elements, rows
+// `row_bytes` apart, boxes of box_inner x box_outer elements, zero fill out
+// of bounds.
+w4v_status encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                          uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                          uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Stream-K style even split of `units` over `ctas`: CTA c owns
+// [c*units/ctas, (c+1)*units/ctas).
+__host__ __device__ inline long long split_begin(long long c, long long units, long long ctas) {
+    return c * units / ctas;
+}
+// The CTA whose range holds unit u.
+__host__ __device__ inline int split_owner(long long u, long long units, long long ctas) {
+    return static_cast<int>(((u + 1) * ctas - 1) / units);
+}
+
+// Launchers (one per kernel family), called after argument validation.
+w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t *scales,
+                               const uint8_t *zeros, uint16_t *C, int M, int N, int K,
+                               void *ws, cudaStream_t stream);
+size_t w4a16_decode_ws_bytes(int M, int N, int K);
+
+w4v_status launch_w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uint16_t *scale,
+                                   int M, int K, int V, int32_t *argmax_out, float *maxlogit,
+                                   float *logits, void *ws, cudaStream_t stream);
+size_t w8_lmhead_ws_bytes(int M, int V);
+
+w4v_status launch_spec_accept(const int32_t *target, const int32_t *draft, int B, int K,
+                              int32_t *n_accepted, int32_t *out_tokens, cudaStream_t stream);
+
+}  // namespace w4v

@@ -1,0 +1,188 @@
+"""Thin ctypes binding of libw4v (include/w4v.h): argument marshalling only.
+
+Every step of the verify path runs in the library's CUDA kernels; this
+module passes device pointers from torch tensors, the current stream, and
+turns status codes into exceptions.  There is no fallback: if the library is
+missing or the GPU is not sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from typing import Optional
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libw4v.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "w4v.h")
+
+OK, ERR_ARG, ERR_SHAPE, ERR_ALIGN, ERR_WORKSPACE, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(8)
+GROUP = 128
+
+_lock = threading.Lock()
+_lib = None
+
+
+class W4VError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s: %s (w4v status %d)" % (where, status_string(code), code))
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libw4v.so (built by ``_build.build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError("libw4v.so not built: run speculative_decoding_verify_w4a16_gb300._build.build()")
+            lib = ctypes.CDLL(path)
+            P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            lib.w4v_status_string.argtypes = [I]
+            lib.w4v_status_string.restype = ctypes.c_char_p
+            lib.w4v_init.restype = I
+            lib.w4v_get_status.argtypes = [P]
+            lib.w4v_get_status.restype = I
+            lib.w4v_packed_bytes.argtypes = [I, I]
+            lib.w4v_packed_bytes.restype = S
+            lib.w4v_pack_int4.argtypes = [P, I, I, P]
+            lib.w4v_pack_int4.restype = I
+            lib.w4v_unpack_int4.argtypes = [P, I, I, P]
+            lib.w4v_unpack_int4.restype = I
+            lib.w4a16_workspace_bytes.argtypes = [I, I, I]
+            lib.w4a16_workspace_bytes.restype = S
+            lib.w4a16_gemm.argtypes = [P, P, P, P, I, P, I, I, I, P, S, P]
+            lib.w4a16_gemm.restype = I
+            lib.w8_lmhead_argmax_workspace_bytes.argtypes = [I, I]
+            lib.w8_lmhead_argmax_workspace_bytes.restype = S
+            lib.w8_lmhead_argmax.argtypes = [P, P, P, I, I, I, P, P, P, P, S, P]
+            lib.w8_lmhead_argmax.restype = I
+            lib.spec_accept.argtypes = [P, P, I, I, P, P, P]
+            lib.spec_accept.restype = I
+            _lib = lib
+    return _lib
+
+
+def header_functions(path: str = HEADER):
+    """Names of the functions declared in include/w4v.h."""
+    with open(path) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    return sorted(set(re.findall(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\(", text)) -
+                  {"if", "defined", "sizeof"})
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().w4v_status_string(int(code)).decode()
+    except Exception:
+        return "status %d" % code
+
+
+def _check(code: int, where: str) -> None:
+    if code != OK:
+        raise W4VError(code, where)
+
+
+def _stream(stream=None) -> Optional[int]:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream if hasattr(s, "cuda_stream") else s
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def init() -> None:
+    _check(load().w4v_init(), "w4v_init")
+
+
+def get_status(stream=None) -> int:
+    return load().w4v_get_status(_stream(stream))
+
+
+# ------------------------------------------------------------------ packing --
+def packed_bytes(N: int, K: int) -> int:
+    return load().w4v_packed_bytes(N, K)
+
+
+def pack_int4(q: np.ndarray) -> np.ndarray:
+    """Logical codes uint8 [N][K] (0..15) -> the library's packed tile layout (host)."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    N, K = q.shape
+    nbytes = packed_bytes(N, K)
+    if nbytes == 0:
+        raise W4VError(ERR_SHAPE, "w4v_pack_int4")
+    out = np.empty(nbytes, np.uint8)
+    _check(load().w4v_pack_int4(q.ctypes.data, N, K, out.ctypes.data), "w4v_pack_int4")
+    return out
+
+
+def unpack_int4(packed: np.ndarray, N: int, K: int) -> np.ndarray:
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    q = np.empty((N, K), np.uint8)
+    _check(load().w4v_unpack_int4(packed.ctypes.data, N, K, q.ctypes.data), "w4v_unpack_int4")
+    return q
+
+
+# --------------------------------------------------------------- workspaces --
+def w4a16_workspace_bytes(M: int, N: int, K: int) -> int:
+    return load().w4a16_workspace_bytes(M, N, K)
+
+
+def w8_lmhead_argmax_workspace_bytes(M: int, V: int) -> int:
+    return load().w8_lmhead_argmax_workspace_bytes(M, V)
+
+
+def workspace(nbytes: int, device="cuda"):
+    """A zero-filled device workspace (the library leaves it zeroed after each call)."""
+    import torch
+    return torch.zeros(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ compute --
+def w4a16_gemm(A, Bq, scales, N: int, zeros=None, out=None, ws=None, stream=None):
+    """C = A @ deq(Bq, scales, zeros)^T on the GPU.  A fp16 [M][K] cuda, Bq packed uint8 cuda."""
+    import torch
+    M, K = A.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    if ws is None:
+        ws = workspace(w4a16_workspace_bytes(M, N, K), A.device)
+    code = load().w4a16_gemm(_ptr(A), _ptr(Bq), _ptr(scales), _ptr(zeros), GROUP, _ptr(out), M, N, K,
+                             _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "w4a16_gemm")
+    return out
+
+
+def w8_lmhead_argmax(X, W, scale, out=None, maxlogit=None, logits=None, ws=None, stream=None):
+    """Greedy token per row of X through the int8 lm_head; returns the int32 [M] token tensor."""
+    import torch
+    M, K = X.shape
+    V = W.shape[0]
+    if out is None:
+        out = torch.empty(M, dtype=torch.int32, device=X.device)
+    if ws is None:
+        ws = workspace(w8_lmhead_argmax_workspace_bytes(M, V), X.device)
+    code = load().w8_lmhead_argmax(_ptr(X), _ptr(W), _ptr(scale), M, K, V, _ptr(out), _ptr(maxlogit),
+                                   _ptr(logits), _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "w8_lmhead_argmax")
+    return out
+
+
+def spec_accept(target, draft, n_out=None, tok_out=None, stream=None):
+    """(n [B], tokens [B][K+1]) for int32 target [B][K+1] and drafts [B][K] on the GPU."""
+    import torch
+    B, K1 = target.shape
+    K = K1 - 1
+    if n_out is None:
+        n_out = torch.empty(B, dtype=torch.int32, device=target.device)
+    if tok_out is None:
+        tok_out = torch.empty((B, K1), dtype=torch.int32, device=target.device)
+    code = load().spec_accept(_ptr(target), _ptr(draft) if K > 0 else None, B, K, _ptr(n_out),
+                              _ptr(tok_out), _stream(stream))
+    _check(code, "spec_accept")
+    return n_out, tok_out

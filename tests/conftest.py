@@ -31,3 +31,21 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def w4v_mod():
+    """The ctypes binding, with libw4v.so built for sm_103a (nvcc cross-compiles without a GPU)."""
+    from speculative_decoding_verify_w4a16_gb300 import _build, w4v
+    _build.build()
+    w4v.load()
+    return w4v
+
+
+@pytest.fixture(scope="session")
+def gpu(w4v_mod):
+    """Skips nothing: a gpu-marked test on a machine without CUDA fails loudly."""
+    import torch
+    assert torch.cuda.is_available(), "gpu test needs a CUDA device"
+    w4v_mod.init()
+    return torch.device("cuda:0")

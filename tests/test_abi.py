@@ -1,0 +1,123 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every function include/w4v.h declares, packs int4 weights in the documented
+layout, sizes workspaces, and rejects bad arguments before launching
+anything.  Every call here with fake pointers fails validation, so nothing
+ever reaches a kernel."""
+import ctypes
+
+import numpy as np
+import pytest
+
+FAKE = 0x10000          # an aligned, never-dereferenced stand-in pointer
+
+
+def test_exports_every_header_function(w4v_mod):
+    names = w4v_mod.header_functions()
+    for required in ("w4v_init", "w4v_get_status", "w4v_pack_int4", "w4a16_gemm",
+                     "w8_lmhead_argmax", "spec_accept"):
+        assert required in names
+    lib = w4v_mod.load()
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(w4v_mod):
+    for code in range(8):
+        s = w4v_mod.status_string(code)
+        assert isinstance(s, str) and s
+    assert w4v_mod.status_string(0) == "ok"
+    assert w4v_mod.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (512, 256), (200, 384), (8, 128), (7680, 2560)])
+def test_pack_roundtrip(w4v_mod, N, K):
+    q = np.random.default_rng(N + K).integers(0, 16, size=(N, K), dtype=np.uint8)
+    packed = w4v_mod.pack_int4(q)
+    assert packed.size == -(-N // 128) * 128 * K // 2
+    assert np.array_equal(w4v_mod.unpack_int4(packed, N, K), q)
+
+
+def test_pack_layout_documented(w4v_mod):
+    """Spot-check the header's description: block (tile, group) is 8192 bytes,
+    chunk j of row r at (j*128 + r)*16, word w covers k = 32j+8w..+7, nibble i
+    holds k offset {0,2,4,6,1,3,5,7}[i]."""
+    N, K = 256, 256
+    q = np.random.default_rng(1).integers(0, 16, size=(N, K), dtype=np.uint8)
+    packed = w4v_mod.pack_int4(q)
+    order = [0, 2, 4, 6, 1, 3, 5, 7]
+    rng = np.random.default_rng(2)
+    for _ in range(200):
+        n, k = int(rng.integers(0, N)), int(rng.integers(0, K))
+        t, r, g = n // 128, n % 128, k // 128
+        kk = k % 128
+        j, w, off = kk // 32, (kk % 32) // 8, kk % 8
+        i = order.index(off)
+        base = (t * (K // 128) + g) * 8192 + (j * 128 + r) * 16 + 4 * w
+        word = int.from_bytes(packed[base:base + 4].tobytes(), "little")
+        assert (word >> (4 * i)) & 15 == q[n, k]
+
+
+def test_pack_pads_tail_rows_with_zero_point(w4v_mod):
+    N, K = 136, 128
+    q = np.zeros((N, K), np.uint8)
+    packed = w4v_mod.pack_int4(q)
+    tail = packed[8192:].reshape(4, 128, 16)[:, 8:, :]     # rows 136.. of the second tile
+    assert np.all(tail == 0x88)
+
+
+def test_workspace_sizes(w4v_mod):
+    assert w4v_mod.w4a16_workspace_bytes(16, 7680, 2560) > 0
+    assert w4v_mod.w4a16_workspace_bytes(33, 512, 256) == 0
+    assert w4v_mod.w4a16_workspace_bytes(16, 100, 256) == 0       # N % 8 != 0
+    assert w4v_mod.w8_lmhead_argmax_workspace_bytes(128, 151936) > 0
+    assert w4v_mod.w8_lmhead_argmax_workspace_bytes(129, 151936) == 0
+    assert w4v_mod.packed_bytes(100, 256) == 0
+
+
+def test_argument_validation_before_launch(w4v_mod):
+    lib = w4v_mod.load()
+    ws_small = 16
+    # w4a16_gemm
+    assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 64, FAKE, 16, 512, 256, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, 33, 512, 256, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 500, 256, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 512, 200, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert lib.w4a16_gemm(FAKE, FAKE, FAKE, FAKE, 128, FAKE, 16, 520, 256, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert lib.w4a16_gemm(None, FAKE, FAKE, None, 128, FAKE, 16, 512, 256, FAKE, 1 << 30, None) == w4v_mod.ERR_ARG
+    assert lib.w4a16_gemm(FAKE + 2, FAKE, FAKE, None, 128, FAKE, 16, 512, 256, FAKE, 1 << 30, None) == w4v_mod.ERR_ALIGN
+    assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 512, 256, FAKE, ws_small, None) == w4v_mod.ERR_WORKSPACE
+    assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 512, 256, None, 1 << 30, None) == w4v_mod.ERR_WORKSPACE
+    assert lib.w4a16_gemm(None, None, None, None, 128, None, 0, 512, 256, None, 0, None) == w4v_mod.OK   # M == 0
+    # w8_lmhead_argmax
+    assert lib.w8_lmhead_argmax(FAKE, FAKE, FAKE, 129, 256, 1024, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert lib.w8_lmhead_argmax(FAKE, FAKE, FAKE, 16, 200, 1024, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert lib.w8_lmhead_argmax(FAKE, FAKE, FAKE, 16, 256, 1020, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert lib.w8_lmhead_argmax(FAKE, FAKE, None, 16, 256, 1024, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_ARG
+    assert lib.w8_lmhead_argmax(FAKE, FAKE + 8, FAKE, 16, 256, 1024, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_ALIGN
+    assert lib.w8_lmhead_argmax(FAKE, FAKE, FAKE, 16, 256, 1024, FAKE, None, None, FAKE, ws_small, None) == w4v_mod.ERR_WORKSPACE
+    assert lib.w8_lmhead_argmax(None, None, None, 0, 256, 1024, None, None, None, None, 0, None) == w4v_mod.OK
+    # spec_accept
+    assert lib.spec_accept(FAKE, FAKE, 4, 1025, FAKE, None, None) == w4v_mod.ERR_SHAPE
+    assert lib.spec_accept(FAKE, FAKE, -1, 4, FAKE, None, None) == w4v_mod.ERR_SHAPE
+    assert lib.spec_accept(None, FAKE, 4, 4, FAKE, None, None) == w4v_mod.ERR_ARG
+    assert lib.spec_accept(FAKE, None, 4, 4, FAKE, None, None) == w4v_mod.ERR_ARG
+    assert lib.spec_accept(FAKE + 1, FAKE, 4, 4, FAKE, None, None) == w4v_mod.ERR_ALIGN
+    assert lib.spec_accept(None, None, 0, 4, None, None, None) == w4v_mod.OK
+    # packer
+    assert lib.w4v_pack_int4(None, 128, 128, FAKE) == w4v_mod.ERR_ARG
+    buf = ctypes.create_string_buffer(16)
+    assert lib.w4v_pack_int4(ctypes.addressof(buf), 100, 128, ctypes.addressof(buf)) == w4v_mod.ERR_SHAPE
+
+
+def test_split_owner_matches_even_split():
+    """Host restatement check of the stream-K ownership formula used by the kernels:
+    owner(u) = ((u+1)P - 1) // U is the CTA whose [cU/P, (c+1)U/P) holds u."""
+    for U in (1, 7, 10, 400, 1200, 1520, 3040):
+        for P in (1, 3, 4, 148, 152):
+            if P > U:
+                continue
+            for c in range(P):
+                lo, hi = c * U // P, (c + 1) * U // P
+                assert hi > lo
+                for u in (lo, hi - 1):
+                    assert ((u + 1) * P - 1) // U == c

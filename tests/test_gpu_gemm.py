@@ -1,0 +1,111 @@
+"""w4a16_gemm on the GPU against the oracle: max relative error <= 2e-3
+(|C - R| / max(|R|, rms R)) against the double-precision definition, on the
+small configuration in full and on the 4B-shaped projections on sampled
+outputs; plus batch invariance and workspace hygiene."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import GEMM_TOL, gemm_rel_err, to_dev
+from speculative_decoding_verify_w4a16_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_gemm(w4v_mod, gpu, A, q, s, zeros=None, ws=None):
+    N = q.shape[0]
+    packed = to_dev(w4v_mod.pack_int4(q), gpu)
+    C = w4v_mod.w4a16_gemm(to_dev(A, gpu), packed, to_dev(s, gpu), N,
+                           zeros=None if zeros is None else to_dev(zeros, gpu), ws=ws)
+    torch.cuda.synchronize()
+    return C.cpu().numpy().astype(np.float64)
+
+
+def test_cfg0_linear(w4v_mod, gpu, oracle_mod):
+    """Tiny verify step: M = 16 rows through one 256 -> 512 W4A16 linear."""
+    A = inputs.activations(0, 16, 256, "cfg0-a")
+    q = inputs.w4_codes(0, 512, 256, "cfg0")
+    s = inputs.w4_scales(0, 512, 256, "cfg0")
+    C = _gpu_gemm(w4v_mod, gpu, A, q, s)
+    assert gemm_rel_err(C, oracle_mod.w4a16_gemm(A, q, s)) <= GEMM_TOL
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 512, 256), (2, 128, 128), (5, 200, 384), (8, 1024, 1024),
+                                   (16, 2560, 2560), (17, 520, 640), (21, 768, 1280), (32, 384, 2560),
+                                   (16, 2560, 9728)])
+def test_shapes(w4v_mod, gpu, oracle_mod, M, N, K):
+    A = inputs.activations(M, M, K, "shape")
+    q = inputs.w4_codes(M, N, K, "shape")
+    s = inputs.w4_scales(M, N, K, "shape")
+    C = _gpu_gemm(w4v_mod, gpu, A, q, s)
+    assert gemm_rel_err(C, oracle_mod.w4a16_gemm(A, q, s)) <= GEMM_TOL
+
+
+def test_zero_points(w4v_mod, gpu, oracle_mod):
+    M, N, K = 16, 512, 512
+    A = inputs.activations(3, M, K)
+    q = inputs.w4_codes(3, N, K)
+    s = inputs.w4_scales(3, N, K)
+    z = inputs.w4_zeros(3, N, K)
+    C = _gpu_gemm(w4v_mod, gpu, A, q, s, zeros=z)
+    assert gemm_rel_err(C, oracle_mod.w4a16_gemm(A, q, s, zeros=z)) <= GEMM_TOL
+
+
+def test_closed_forms_gpu(w4v_mod, gpu):
+    """q == 8 gives exactly 0; a +-1 permutation with unit scales gives +-A[:, pi]."""
+    M, K = 16, 256
+    N = K
+    A = inputs.activations(4, M, K)
+    s = np.ones((K // 128, N), np.float16)
+    C = _gpu_gemm(w4v_mod, gpu, A, np.full((N, K), 8, np.uint8), s)
+    assert np.all(C == 0)
+    pi = np.random.default_rng(4).permutation(K)
+    q = np.full((N, K), 8, np.uint8)
+    q[np.arange(N), pi] = 7
+    C = _gpu_gemm(w4v_mod, gpu, A, q, s)
+    assert np.array_equal(C, -A.astype(np.float64)[:, pi])
+
+
+def test_batch_invariance(w4v_mod, gpu):
+    """For M <= 32 every output element comes from the same arithmetic, so the
+    rows of a small-M call equal the same rows of a larger call bit for bit."""
+    N, K = 2560, 2560
+    A = inputs.activations(6, 32, K)
+    q = inputs.w4_codes(6, N, K)
+    s = inputs.w4_scales(6, N, K)
+    full = _gpu_gemm(w4v_mod, gpu, A, q, s)
+    for m in (1, 7, 16, 21):
+        part = _gpu_gemm(w4v_mod, gpu, A[:m], q, s)
+        assert np.array_equal(part, full[:m]), m
+
+
+def test_workspace_reuse_is_clean(w4v_mod, gpu):
+    M, N, K = 16, 2560, 9728
+    A = inputs.activations(7, M, K)
+    q = inputs.w4_codes(7, N, K)
+    s = inputs.w4_scales(7, N, K)
+    ws = w4v_mod.workspace(w4v_mod.w4a16_workspace_bytes(M, N, K), gpu)
+    a = _gpu_gemm(w4v_mod, gpu, A, q, s, ws=ws)
+    b = _gpu_gemm(w4v_mod, gpu, A, q, s, ws=ws)
+    assert np.array_equal(a, b)
+    n_tiles = -(-N // 128)
+    counters = ws.cpu().numpy()[-(((n_tiles * 4 + 255) // 256) * 256):]
+    assert np.all(counters == 0)
+    assert w4v_mod.get_status() == 0
+
+
+@pytest.mark.parametrize("proj", inputs.LAYER_PROJS, ids=lambda p: p.name)
+def test_layer_projection_sampled(w4v_mod, gpu, oracle_mod, proj):
+    """The 4B-shaped projections at M = 16 (the verify block of K = 15 drafts):
+    4000 sampled outputs plus two full output rows against the oracle."""
+    M = 16
+    A = inputs.activations(1, M, proj.K, 0, proj.name)
+    q, s = inputs.layer_weights(1, 0, proj)
+    C = _gpu_gemm(w4v_mod, gpu, A, q, s)
+    r = np.random.default_rng(1)
+    rows = r.integers(0, M, 4000).astype(np.int32)
+    cols = r.integers(0, proj.N, 4000).astype(np.int32)
+    rows = np.concatenate([rows, np.zeros(proj.N, np.int32), np.full(proj.N, M - 1, np.int32)])
+    cols = np.concatenate([cols, np.arange(proj.N, dtype=np.int32), np.arange(proj.N, dtype=np.int32)])
+    R = oracle_mod.w4a16_gemm_sampled(A, q, s, rows, cols)
+    assert gemm_rel_err(C[rows, cols], R) <= GEMM_TOL
