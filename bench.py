@@ -1,0 +1,475 @@
+#!/usr/bin/env python3
+"""Verify-step benchmark: W4A16 layer set + int8 lm_head argmax + acceptance.
+
+Workload (the 4B-shaped verify step at M = 16, i.e. K = 15 drafts + 1): the
+four W4A16 g128 projections of one decoder layer set (qkv 2560->7680,
+o 2560->2560, gate_up 2560->19456, down 9728->2560), the int8 lm_head
+2560->151936 with fused greedy argmax, and longest-prefix acceptance of 15
+seeded drafts.  One step = all of it once, captured as one CUDA graph.
+
+value      = algorithmic input bytes per step (packed int4 + fp16 group
+             scales + fp16 activations, int8 lm_head + row scales + its
+             activations) / device time per step, in GB/s, summed over ranks.
+e2e        = the same through the public API with host buffers: pinned host
+             -> device copies of the step's activations and drafts, the
+             kernels, and the device -> host read of the accepted tokens.
+roofline   = the dominant kernel (the lm_head at M = 16), its duration timed
+             live with CUDA events inside the graph, against the measured HBM
+             copy bandwidth; per-kernel rooflines sit in "kernels", and the
+             W4A16 GEMM alone across a 36-layer stack in "sweep".
+cpu_baseline = the CPU oracle on one full step of the same workload.
+
+--impl reference times the oracle alone (the only reference this method has
+here) on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_verify_w4a16_gb300 import inputs  # noqa: E402
+
+METRIC = "verify W4A16 GEMM GB/s & % HBM peak at M=16; prefill TFLOP/s at M=8192"
+M_VERIFY = 16
+K_DRAFT = 15
+SEED = 1
+COPIES = 3          # projection weight sets rotated per step
+
+
+def step_bytes(M=M_VERIFY):
+    proj = sum(p.N * p.K // 2 + (p.K // 128) * p.N * 2 + M * p.K * 2 for p in inputs.LAYER_PROJS)
+    lm = inputs.V_4B * inputs.H_4B + inputs.V_4B * 2 + M * inputs.H_4B * 2
+    return proj, lm
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.rows = []
+        self._stop = threading.Event()
+        self._thr = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                      "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                                     timeout=5).stdout.strip()
+                if out:
+                    self.rows.append([x.strip() for x in out.split(",")])
+            except Exception:
+                pass
+            self._stop.wait(0.2)
+
+    def __enter__(self):
+        self._thr = threading.Thread(target=self._run, daemon=True)
+        self._thr.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        self._thr.join(timeout=10)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if len(r) > 3 + i and r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# --------------------------------------------------------------------- GPU arm
+class VerifyStep:
+    """Device buffers and the enqueue order of one config-1 verify step."""
+
+    def __init__(self, dev, w4v, torch):
+        self.dev, self.w4v, self.torch = dev, w4v, torch
+        H, V = inputs.H_4B, inputs.V_4B
+        M = M_VERIFY
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        self.host = {}
+        self.projs = []
+        for c in range(COPIES):
+            layer = []
+            for p in inputs.LAYER_PROJS:
+                q, s = inputs.layer_weights(SEED, c, p)
+                if c == 0:
+                    self.host[p.name] = (q, s)
+                layer.append((p, t(w4v.pack_int4(q)), t(s)))
+            self.projs.append(layer)
+        self.acts = {p.name: t(inputs.activations(SEED, M, p.K, "bench", p.name)) for p in inputs.LAYER_PROJS}
+        self.outs = {p.name: torch.empty((M, p.N), dtype=torch.float16, device=dev) for p in inputs.LAYER_PROJS}
+        self.ws = {p.name: w4v.workspace(w4v.w4a16_workspace_bytes(M, p.N, p.K), dev) for p in inputs.LAYER_PROJS}
+        W8, s8 = inputs.lmhead_weights(SEED, V, H, "bench")
+        self.host["lm"] = (W8, s8)
+        self.W8, self.s8 = t(W8), t(s8)
+        self.X = t(inputs.activations(SEED, M, H, "bench", "lm"))
+        self.host["acts"] = {k: v.cpu().numpy() for k, v in self.acts.items()}
+        self.host["X"] = self.X.cpu().numpy()
+        self.tok = torch.empty(M, dtype=torch.int32, device=dev)
+        self.ws_lm = w4v.workspace(w4v.w8_lmhead_argmax_workspace_bytes(M, V), dev)
+        # drafts: fixed from the seed (the synthetic verify rows do not depend on them)
+        d = inputs.rng(SEED, "bench-drafts").integers(0, V, size=(1, K_DRAFT)).astype(np.int32)
+        self.draft = t(d)
+        self.n_acc = torch.empty(1, dtype=torch.int32, device=dev)
+        self.out_tok = torch.empty((1, K_DRAFT + 1), dtype=torch.int32, device=dev)
+        self.launches_per_step = len(inputs.LAYER_PROJS) + 2
+
+    def enqueue(self, copy, events=None):
+        w4v = self.w4v
+        for i, (p, packed, s) in enumerate(self.projs[copy]):
+            if events:
+                events[i].record()
+            w4v.w4a16_gemm(self.acts[p.name], packed, s, p.N, out=self.outs[p.name], ws=self.ws[p.name])
+        if events:
+            events[4].record()
+        w4v.w8_lmhead_argmax(self.X, self.W8, self.s8, out=self.tok, ws=self.ws_lm)
+        if events:
+            events[5].record()
+        w4v.spec_accept(self.tok.view(1, M_VERIFY), self.draft, n_out=self.n_acc, tok_out=self.out_tok)
+        if events:
+            events[6].record()
+
+
+def capture(torch, fn):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def run_gpu(args, rank, world):
+    import torch
+    from speculative_decoding_verify_w4a16_gb300 import _build, w4v
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0 or not os.path.exists(_build.LIB):
+        _build.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    w4v.load()
+    w4v.init()
+    peaks = load_peaks()
+    step = VerifyStep(dev, w4v, torch)
+    proj_bytes, lm_bytes = step_bytes()
+    total_bytes = proj_bytes + lm_bytes
+
+    # warm-up eagerly (first launches configure kernels), then capture graphs
+    for i in range(max(args.warmup, 3)):
+        step.enqueue(i % COPIES)
+    torch.cuda.synchronize()
+    n_ev = 7
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(COPIES)]
+    graphs = [capture(torch, lambda c=c: step.enqueue(c, evs[c])) for c in range(COPIES)]
+    for i in range(max(args.warmup, 3)):
+        graphs[i % COPIES].replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays, no host synchronisation inside ---------
+    # Each graph carries CUDA event records around every kernel; after the
+    # region the events hold the last replay of each graph (all inside it).
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        start.record()
+        for i in range(args.steps):
+            graphs[i % COPIES].replay()
+        end.record()
+        torch.cuda.synchronize()
+    ms_total = start.elapsed_time(end)
+    per_kernel = [[evs[c][k].elapsed_time(evs[c][k + 1]) for c in range(min(COPIES, args.steps))]
+                  for k in range(n_ev - 1)]
+    ms_step_local = ms_total / args.steps
+    ms_step = ms_step_local
+    if world > 1:
+        t = torch.tensor([ms_step_local], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * total_bytes / (ms_step * 1e-3) / 1e9
+
+    names = [p.name for p in inputs.LAYER_PROJS] + ["lm_head", "spec_accept"]
+    kern = {}
+    for k, nm in enumerate(names):
+        d_ms = statistics.median(per_kernel[k]) if per_kernel[k] else None
+        if nm == "spec_accept":
+            kern[nm] = {"ms": d_ms}
+            continue
+        if nm == "lm_head":
+            b = lm_bytes
+        else:
+            p = inputs.LAYER_PROJS[k]
+            b = p.N * p.K // 2 + (p.K // 128) * p.N * 2 + M_VERIFY * p.K * 2
+        gbs = b / (d_ms * 1e-3) / 1e9 if d_ms else None
+        kern[nm] = {"ms": d_ms, "bytes": b, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"] if gbs else None}
+    lm = kern["lm_head"]
+    gemm_ms = sum(kern[p.name]["ms"] for p in inputs.LAYER_PROJS)
+    gemm_gbs = proj_bytes / (gemm_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers -----------------
+    e2e = run_e2e(args, step, torch, total_bytes, world)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": "cfg1 verify step: 4B-shaped W4A16 g128 layer set (qkv, o, gate_up, down) "
+                               "+ int8 lm_head 2560->151936 argmax + accept, M=16 (K=15)",
+                   "M": M_VERIFY, "K_draft": K_DRAFT, "bytes_per_step": total_bytes,
+                   "l2": "inputs larger than L2: 442 MB read per step, projection weights rotate over "
+                         "%d copies" % COPIES,
+                   "graph": "one CUDA graph per step", "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "kernel": "w8_lmhead_argmax (M=16, V=151936, K=2560)",
+                     "achieved": round(lm["GB/s"], 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(lm["frac"], 4), "traffic": None,
+                     "peak_source": peaks["source"] + " (hbm copy, burst)"},
+        "gemm_m16": {"GB/s": round(gemm_gbs, 1), "frac": round(gemm_gbs / peaks["hbm_gbs"], 4),
+                     "ms": round(gemm_ms, 5), "bytes": proj_bytes},
+        "kernels": {k: {kk: (round(vv, 5) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                    for k, v in kern.items()},
+        "e2e": e2e,
+        "gpu_launches": step.launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if args.sweep:
+        result["sweep"] = run_sweep(args, dev, w4v, torch, peaks)
+    if rank == 0 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(step)
+    return result
+
+
+def run_e2e(args, step, torch, total_bytes, world):
+    """Host buffers in, accepted tokens out, through the same calls, one graph per step."""
+    names = [p.name for p in inputs.LAYER_PROJS]
+    h_acts = {n: torch.from_numpy(step.host["acts"][n]).pin_memory() for n in names}
+    h_X = torch.from_numpy(step.host["X"]).pin_memory()
+    h_d = step.draft.cpu().pin_memory()
+    h_n = torch.empty(1, dtype=torch.int32).pin_memory()
+    h_tok = torch.empty((1, K_DRAFT + 1), dtype=torch.int32).pin_memory()
+
+    def body(c):
+        for n in names:
+            step.acts[n].copy_(h_acts[n], non_blocking=True)
+        step.X.copy_(h_X, non_blocking=True)
+        step.draft.copy_(h_d, non_blocking=True)
+        step.enqueue(c)
+        h_n.copy_(step.n_acc, non_blocking=True)
+        h_tok.copy_(step.out_tok, non_blocking=True)
+
+    for c in range(COPIES):
+        body(c)
+    torch.cuda.synchronize()
+    graphs = [capture(torch, lambda c=c: body(c)) for c in range(COPIES)]
+    for c in range(COPIES):
+        graphs[c].replay()
+    torch.cuda.synchronize()
+    steps = args.steps
+    t0 = time.perf_counter()
+    for i in range(steps):
+        graphs[i % COPIES].replay()
+        torch.cuda.current_stream().synchronize()     # the host reads the accepted tokens every step
+        _ = int(h_n[0])
+    dt = (time.perf_counter() - t0) / steps
+    h2d = sum(v.numel() * v.element_size() for v in h_acts.values()) + h_X.numel() * 2 + h_d.numel() * 4
+    d2h = h_n.numel() * 4 + h_tok.numel() * 4
+    return {"value": round(world * total_bytes / dt / 1e9, 1), "unit": "GB/s", "ms_per_step": round(dt * 1e3, 5),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "how": "pinned host -> device activations and drafts, one CUDA graph of the step, "
+                   "device -> host accepted tokens, host synchronize each step (wall clock)"}
+
+
+def run_sweep(args, dev, w4v, torch, peaks):
+    """36-layer stack of the projections at M in {1,2,4,8,16,21}: the W4A16 GEMMs
+    alone, each launch reading a different layer's weights (1.87 GB >> L2)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(SEED)
+    layers = []
+    for l in range(36):
+        lay = []
+        for p in inputs.LAYER_PROJS:
+            packed = torch.randint(0, 256, (w4v.packed_bytes(p.N, p.K),), generator=g, device=dev,
+                                   dtype=torch.uint8)
+            sc = (torch.rand(((p.K // 128), p.N), generator=g, device=dev) * 0.015 + 0.005).half()
+            lay.append((p, packed, sc))
+        layers.append(lay)
+    out = {}
+    for M in (1, 2, 4, 8, 16, 21):
+        acts = {p.name: torch.randn((M, p.K), generator=g, device=dev).half() for p in inputs.LAYER_PROJS}
+        outs = {p.name: torch.empty((M, p.N), device=dev, dtype=torch.float16) for p in inputs.LAYER_PROJS}
+        wss = {p.name: w4v.workspace(w4v.w4a16_workspace_bytes(M, p.N, p.K), dev) for p in inputs.LAYER_PROJS}
+
+        def stack():
+            for lay in layers:
+                for (p, packed, sc) in lay:
+                    w4v.w4a16_gemm(acts[p.name], packed, sc, p.N, out=outs[p.name], ws=wss[p.name])
+
+        stack()
+        torch.cuda.synchronize()
+        gr = capture(torch, stack)
+        gr.replay()
+        torch.cuda.synchronize()
+        reps = 5
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            gr.replay()
+        e.record()
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(e) / reps
+        b = 36 * sum(p.N * p.K // 2 + (p.K // 128) * p.N * 2 + M * p.K * 2 for p in inputs.LAYER_PROJS)
+        gbs = b / (ms * 1e-3) / 1e9
+        out["M=%d" % M] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
+                           "launches": 144}
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
+# --------------------------------------------------------------------- CPU arm
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_step(host, frac=1.0):
+    """The oracle on the config-1 step; frac < 1 keeps that fraction of every
+    weight matrix's output rows (all 16 activation rows, full K).  Returns the
+    algorithmic bytes it processed."""
+    import oracle
+    nbytes = 0
+    for p in inputs.LAYER_PROJS:
+        q, s = host[p.name]
+        n = max(8, int(p.N * frac) // 8 * 8)
+        A = host["acts"][p.name]
+        oracle.w4a16_gemm(A, q[:n], np.ascontiguousarray(s[:, :n]))
+        nbytes += n * p.K // 2 + (p.K // 128) * n * 2 + M_VERIFY * p.K * 2
+    W8, s8 = host["lm"]
+    v = max(8, int(W8.shape[0] * frac))
+    L = oracle.lmhead_logits(host["X"], W8[:v], s8[:v])
+    t = oracle.argmax(L)
+    d = np.zeros((1, K_DRAFT), np.int32)
+    oracle.spec_accept(t.reshape(1, -1), d)
+    nbytes += v * inputs.H_4B + v * 2 + M_VERIFY * inputs.H_4B * 2
+    return nbytes
+
+
+def cpu_baseline(step):
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    nbytes = oracle_step(step.host, 1.0)
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": "one full cfg1 verify step (4 projections + lm_head + argmax + accept), M=16, "
+                      "double precision, OpenMP over output rows"}
+
+
+def host_inputs():
+    host = {}
+    for p in inputs.LAYER_PROJS:
+        host[p.name] = inputs.layer_weights(SEED, 0, p)
+    host["acts"] = {p.name: inputs.activations(SEED, M_VERIFY, p.K, "bench", p.name) for p in inputs.LAYER_PROJS}
+    host["lm"] = inputs.lmhead_weights(SEED, inputs.V_4B, inputs.H_4B, "bench")
+    host["X"] = inputs.activations(SEED, M_VERIFY, inputs.H_4B, "bench", "lm")
+    return host
+
+
+def run_reference(args, rank, world):
+    import oracle
+    oracle.build()
+    host = host_inputs()
+    frac = args.ref_frac
+    for _ in range(args.warmup):
+        oracle_step(host, frac)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes = oracle_step(host, frac)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = nbytes / dt / 1e9
+    cb = {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+          "sample": "per step: %.4g of every weight matrix's output rows of the cfg1 verify step "
+                    "(all 16 rows, full K), double precision" % frac}
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "cfg1 verify step (CPU oracle sample)", "M": M_VERIFY,
+                       "bytes_per_step": nbytes, "parallelism": "host cores"},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--ref-frac", type=float, default=1.0 / 16)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    res = run_gpu(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
