@@ -14,7 +14,7 @@ e2e        = the same through the public API with host buffers: pinned host
              -> device copies of the step's activations and drafts, the
              kernels, and the device -> host read of the accepted tokens.
 roofline   = the dominant kernel (the lm_head at M = 16), its duration timed
-             live with CUDA events inside the graph, against the measured HBM
+             live with CUDA events around a graph of repeated launches, against the measured HBM
              copy bandwidth; per-kernel rooflines sit in "kernels", and the
              W4A16 GEMM alone across a 36-layer stack in "sweep".
 cpu_baseline = the CPU oracle on one full step of the same workload.
@@ -148,20 +148,15 @@ class VerifyStep:
         self.out_tok = torch.empty((1, K_DRAFT + 1), dtype=torch.int32, device=dev)
         self.launches_per_step = len(inputs.LAYER_PROJS) + 2
 
-    def enqueue(self, copy, events=None):
+    def enqueue(self, copy):
         w4v = self.w4v
-        for i, (p, packed, s) in enumerate(self.projs[copy]):
-            if events:
-                events[i].record()
+        for p, packed, s in self.projs[copy]:
             w4v.w4a16_gemm(self.acts[p.name], packed, s, p.N, out=self.outs[p.name], ws=self.ws[p.name])
-        if events:
-            events[4].record()
-        w4v.w8_lmhead_argmax(self.X, self.W8, self.s8, out=self.tok, ws=self.ws_lm)
-        if events:
-            events[5].record()
+        self.lm_head()
         w4v.spec_accept(self.tok.view(1, M_VERIFY), self.draft, n_out=self.n_acc, tok_out=self.out_tok)
-        if events:
-            events[6].record()
+
+    def lm_head(self):
+        self.w4v.w8_lmhead_argmax(self.X, self.W8, self.s8, out=self.tok, ws=self.ws_lm)
 
 
 def capture(torch, fn):
@@ -193,16 +188,12 @@ def run_gpu(args, rank, world):
     for i in range(max(args.warmup, 3)):
         step.enqueue(i % COPIES)
     torch.cuda.synchronize()
-    n_ev = 7
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(COPIES)]
-    graphs = [capture(torch, lambda c=c: step.enqueue(c, evs[c])) for c in range(COPIES)]
+    graphs = [capture(torch, lambda c=c: step.enqueue(c)) for c in range(COPIES)]
     for i in range(max(args.warmup, 3)):
         graphs[i % COPIES].replay()
     torch.cuda.synchronize()
 
     # ---- timed region: K graph replays, no host synchronisation inside ---------
-    # Each graph carries CUDA event records around every kernel; after the
-    # region the events hold the last replay of each graph (all inside it).
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         if world > 1:
@@ -214,8 +205,6 @@ def run_gpu(args, rank, world):
         end.record()
         torch.cuda.synchronize()
     ms_total = start.elapsed_time(end)
-    per_kernel = [[evs[c][k].elapsed_time(evs[c][k + 1]) for c in range(min(COPIES, args.steps))]
-                  for k in range(n_ev - 1)]
     ms_step_local = ms_total / args.steps
     ms_step = ms_step_local
     if world > 1:
@@ -224,20 +213,18 @@ def run_gpu(args, rank, world):
         ms_step = float(t.item())
     value = world * total_bytes / (ms_step * 1e-3) / 1e9
 
-    names = [p.name for p in inputs.LAYER_PROJS] + ["lm_head", "spec_accept"]
+    # ---- per-kernel durations: each kernel alone in a graph of repeated launches
     kern = {}
-    for k, nm in enumerate(names):
-        d_ms = statistics.median(per_kernel[k]) if per_kernel[k] else None
-        if nm == "spec_accept":
-            kern[nm] = {"ms": d_ms}
-            continue
-        if nm == "lm_head":
-            b = lm_bytes
-        else:
-            p = inputs.LAYER_PROJS[k]
-            b = p.N * p.K // 2 + (p.K // 128) * p.N * 2 + M_VERIFY * p.K * 2
-        gbs = b / (d_ms * 1e-3) / 1e9 if d_ms else None
-        kern[nm] = {"ms": d_ms, "bytes": b, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"] if gbs else None}
+    reps = 20
+    lm_ms = time_graph(torch, lambda: [step.lm_head() for _ in range(reps)]) / reps
+    lm_gbs = lm_bytes / (lm_ms * 1e-3) / 1e9
+    kern["lm_head"] = {"ms": lm_ms, "bytes": lm_bytes, "GB/s": lm_gbs, "frac": lm_gbs / peaks["hbm_gbs"]}
+    stack = Stack(dev, w4v, torch)
+    for p in inputs.LAYER_PROJS:
+        ms = stack.time_projection(p, M_VERIFY)
+        b = p.N * p.K // 2 + (p.K // 128) * p.N * 2 + M_VERIFY * p.K * 2
+        gbs = b / (ms * 1e-3) / 1e9
+        kern[p.name] = {"ms": ms, "bytes": b, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"]}
     lm = kern["lm_head"]
     gemm_ms = sum(kern[p.name]["ms"] for p in inputs.LAYER_PROJS)
     gemm_gbs = proj_bytes / (gemm_ms * 1e-3) / 1e9
@@ -256,7 +243,8 @@ def run_gpu(args, rank, world):
                    "l2": "inputs larger than L2: 442 MB read per step, projection weights rotate over "
                          "%d copies" % COPIES,
                    "graph": "one CUDA graph per step", "parallelism": "replicas" if world > 1 else "1 GPU"},
-        "roofline": {"bound": "hbm", "kernel": "w8_lmhead_argmax (M=16, V=151936, K=2560)",
+        "roofline": {"bound": "hbm", "kernel": "w8_lmhead_argmax (M=16, V=151936, K=2560), %d launches "
+                               "in one graph, CUDA events on the launching stream" % reps,
                      "achieved": round(lm["GB/s"], 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(lm["frac"], 4), "traffic": None,
                      "peak_source": peaks["source"] + " (hbm copy, burst)"},
@@ -269,7 +257,8 @@ def run_gpu(args, rank, world):
         "clocks": clk.summary(),
     }
     if args.sweep:
-        result["sweep"] = run_sweep(args, dev, w4v, torch, peaks)
+        result["sweep"] = stack.sweep(peaks)
+    del stack
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(step)
     return result
@@ -315,51 +304,84 @@ def run_e2e(args, step, torch, total_bytes, world):
                    "device -> host accepted tokens, host synchronize each step (wall clock)"}
 
 
-def run_sweep(args, dev, w4v, torch, peaks):
-    """36-layer stack of the projections at M in {1,2,4,8,16,21}: the W4A16 GEMMs
-    alone, each launch reading a different layer's weights (1.87 GB >> L2)."""
-    g = torch.Generator(device=dev)
-    g.manual_seed(SEED)
-    layers = []
-    for l in range(36):
-        lay = []
-        for p in inputs.LAYER_PROJS:
-            packed = torch.randint(0, 256, (w4v.packed_bytes(p.N, p.K),), generator=g, device=dev,
-                                   dtype=torch.uint8)
-            sc = (torch.rand(((p.K // 128), p.N), generator=g, device=dev) * 0.015 + 0.005).half()
-            lay.append((p, packed, sc))
-        layers.append(lay)
-    out = {}
-    for M in (1, 2, 4, 8, 16, 21):
-        acts = {p.name: torch.randn((M, p.K), generator=g, device=dev).half() for p in inputs.LAYER_PROJS}
-        outs = {p.name: torch.empty((M, p.N), device=dev, dtype=torch.float16) for p in inputs.LAYER_PROJS}
-        wss = {p.name: w4v.workspace(w4v.w4a16_workspace_bytes(M, p.N, p.K), dev) for p in inputs.LAYER_PROJS}
-
-        def stack():
-            for lay in layers:
-                for (p, packed, sc) in lay:
-                    w4v.w4a16_gemm(acts[p.name], packed, sc, p.N, out=outs[p.name], ws=wss[p.name])
-
-        stack()
-        torch.cuda.synchronize()
-        gr = capture(torch, stack)
-        gr.replay()
-        torch.cuda.synchronize()
-        reps = 5
+def time_graph(torch, fn, reps=3):
+    """Device ms of one replay of a graph of fn, median of reps timed replays."""
+    fn()
+    torch.cuda.synchronize()
+    g = capture(torch, fn)
+    g.replay()
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(reps):
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record()
-        for _ in range(reps):
-            gr.replay()
+        g.replay()
         e.record()
         torch.cuda.synchronize()
-        ms = s.elapsed_time(e) / reps
-        b = 36 * sum(p.N * p.K // 2 + (p.K // 128) * p.N * 2 + M * p.K * 2 for p in inputs.LAYER_PROJS)
-        gbs = b / (ms * 1e-3) / 1e9
-        out["M=%d" % M] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
-                           "launches": 144}
-    del layers
-    torch.cuda.empty_cache()
-    return out
+        out.append(s.elapsed_time(e))
+    del g
+    return statistics.median(out)
+
+
+class Stack:
+    """36-layer stack of the projections (config 2), weights drawn on the device
+    directly in packed form (uniform random bytes = uniform iid 4-bit codes in
+    any nibble order), fp16 scales U[0.005, 0.02]: 1.87 GB, far above L2, so
+    every launch streams its weights from HBM."""
+
+    LAYERS = 36
+
+    def __init__(self, dev, w4v, torch):
+        self.dev, self.w4v, self.torch = dev, w4v, torch
+        g = torch.Generator(device=dev)
+        g.manual_seed(SEED)
+        self.g = g
+        self.layers = []
+        for _ in range(self.LAYERS):
+            lay = []
+            for p in inputs.LAYER_PROJS:
+                packed = torch.randint(0, 256, (w4v.packed_bytes(p.N, p.K),), generator=g, device=dev,
+                                       dtype=torch.uint8)
+                sc = (torch.rand(((p.K // 128), p.N), generator=g, device=dev) * 0.015 + 0.005).half()
+                lay.append((p, packed, sc))
+            self.layers.append(lay)
+
+    def _buffers(self, M):
+        torch = self.torch
+        acts = {p.name: torch.randn((M, p.K), generator=self.g, device=self.dev).half() for p in inputs.LAYER_PROJS}
+        outs = {p.name: torch.empty((M, p.N), device=self.dev, dtype=torch.float16) for p in inputs.LAYER_PROJS}
+        wss = {p.name: self.w4v.workspace(self.w4v.w4a16_workspace_bytes(M, p.N, p.K), self.dev)
+               for p in inputs.LAYER_PROJS}
+        return acts, outs, wss
+
+    def time_projection(self, proj, M):
+        """ms per launch of one projection, launched once per layer (36 launches)."""
+        acts, outs, wss = self._buffers(M)
+        k = [i for i, p in enumerate(inputs.LAYER_PROJS) if p.name == proj.name][0]
+
+        def run():
+            for lay in self.layers:
+                p, packed, sc = lay[k]
+                self.w4v.w4a16_gemm(acts[p.name], packed, sc, p.N, out=outs[p.name], ws=wss[p.name])
+
+        return time_graph(self.torch, run) / self.LAYERS
+
+    def sweep(self, peaks):
+        out = {}
+        for M in (1, 2, 4, 8, 16, 21):
+            acts, outs, wss = self._buffers(M)
+
+            def run():
+                for lay in self.layers:
+                    for (p, packed, sc) in lay:
+                        self.w4v.w4a16_gemm(acts[p.name], packed, sc, p.N, out=outs[p.name], ws=wss[p.name])
+
+            ms = time_graph(self.torch, run)
+            b = self.LAYERS * sum(p.N * p.K // 2 + (p.K // 128) * p.N * 2 + M * p.K * 2 for p in inputs.LAYER_PROJS)
+            gbs = b / (ms * 1e-3) / 1e9
+            out["M=%d" % M] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
+                               "launches": 4 * self.LAYERS}
+        return out
 
 
 # --------------------------------------------------------------------- CPU arm

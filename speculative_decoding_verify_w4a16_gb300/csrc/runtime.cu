@@ -110,6 +110,20 @@ w4v_status encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const voi
     return r == CUDA_SUCCESS ? W4V_OK : W4V_ERR_ARG;
 }
 
+w4v_status encode_tmap_kblocks(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t elem_bytes, const void *base,
+                               uint64_t inner, uint64_t rows, uint32_t inner_box, uint32_t box_rows,
+                               uint32_t box_blocks, CUtensorMapSwizzle swizzle) {
+    if (g_encode == nullptr || inner % inner_box != 0) return W4V_ERR_CUDA;
+    cuuint64_t dims[3] = {inner_box, rows, inner / inner_box};
+    cuuint64_t strides[2] = {inner * elem_bytes, uint64_t(inner_box) * elem_bytes};
+    cuuint32_t box[3] = {inner_box, box_rows, box_blocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? W4V_OK : W4V_ERR_ARG;
+}
+
 }  // namespace w4v
 
 extern "C" w4v_status w4v_init(void) {

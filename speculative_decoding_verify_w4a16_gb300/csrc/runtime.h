@@ -31,6 +31,15 @@ w4v_status encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const voi
                           uint64_t inner, uint64_t outer, uint64_t row_bytes,
                           uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
+// 3-D map over a row-major [outer][inner] matrix viewed as
+// (inner_box elements, rows, inner / inner_box blocks): the block dimension
+// steps inner_box elements along a row, so one box of {inner_box, box_rows,
+// box_blocks} lands in shared memory as box_blocks consecutive
+// [box_rows][inner_box] tiles -- the K-major layout the MMA descriptors use.
+w4v_status encode_tmap_kblocks(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t elem_bytes, const void *base,
+                               uint64_t inner, uint64_t rows, uint32_t inner_box, uint32_t box_rows,
+                               uint32_t box_blocks, CUtensorMapSwizzle swizzle);
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Stream-K style even split of `units` over `ctas`: CTA c owns

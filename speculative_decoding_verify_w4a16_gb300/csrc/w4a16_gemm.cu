@@ -7,55 +7,80 @@
 //
 // Why it looks like this (section 2 of the same page: decode reads the whole
 // weight set from HBM per step, so the K+1 verify rows must share one weight
-// read):
-//   * The weights are the wide operand.  A 128-row weight tile is the MMA's
-//     M side; the (<= 32) activation rows are its N side in blocks of 16, so
+// read; at M = 16 the kernel must move ~45 int4 weights per SM cycle):
+//   * The weights are the wide operand: a 128-row weight tile is the MMA's
+//     M side, the (<= 32) activation rows its N side in blocks of 16, so
 //     every output element comes from the same instruction shape whatever M
 //     is (batch invariance for M <= 32).
-//   * Packed int4 blocks stream from HBM with 1-D bulk copies (8 KB per
-//     128x128 block, evict-first), the group scales / zeros ride along, and
-//     the activation slice arrives by 2-D TMA with 128-byte swizzle.
-//   * Eight math warps turn nibbles into exact fp16 integers (q - z) with a
-//     LOP3 + HFMA2 bit trick and store them straight into tensor memory with
-//     tcgen05.st: the dequantized operand never touches shared memory, which
-//     keeps shared-memory bandwidth for the copies.
-//   * One thread issues tcgen05.mma (A from TMEM, B from shared memory, D in
-//     TMEM) per group; the math warps drain each group's fp32 result with
-//     tcgen05.ld and apply the group scale in fp32 (0.125 FMA per weight).
-//   * Work is the flat list of (tile, group) units split evenly over one CTA
-//     per SM; a tile shared by several CTAs is finished by the last one to
-//     arrive, which sums the fp32 partial tiles in CTA order (deterministic,
-//     no waiting between CTAs).
+//   * Units are (128-row tile, 128-k group).  An SM completes about one TMA
+//     or bulk copy per ~650 cycles whatever its size, so copies are large:
+//     a stage is up to 4 consecutive groups of one tile, fetched as one 32 KB
+//     bulk copy of packed int4 (the library's tile layout, evict-first) and
+//     one 3-D TMA of the 4 groups' activation slices (128-byte swizzle).
+//     Two producer threads issue them.
+//   * Eight dequant warps (one per TMEM lane quarter and k half) turn
+//     nibbles into exact fp16 (q - z) with LOP3 + HFMA2 and store them into
+//     tensor memory with 32-column tcgen05.st; the store of one unit overlaps
+//     the dequant of the next.  The dequantized operand never touches shared
+//     memory.
+//   * tcgen05.mma (A from TMEM, B = activations from shared memory, D in
+//     TMEM) is issued by four threads in four warps: one thread alone issues
+//     at most one MMA per ~55 cycles, four reach the rate HBM needs.  Each
+//     issuer owns fixed (accumulator, column-block) slices; a group's 8
+//     k-steps go round-robin into 4 accumulators, so the result does not
+//     depend on timing.
+//   * Four drain warps read each group's 4 accumulators (32-column
+//     tcgen05.ld), add them in a fixed order and apply the group scale in
+//     fp32, with the scales prefetched from global memory four groups ahead.
+//   * Work is the flat list of units split evenly over one CTA per SM; a
+//     tile shared by several CTAs is finished by the last one to arrive
+//     (release/acquire counter, no waiting between CTAs), which sums the fp32
+//     partial tiles in CTA order, so the result is deterministic.
 #include "runtime.h"
 #include "sm103_ptx.cuh"
 
 namespace w4v {
 namespace {
 
-constexpr int kTileN = 128;                     // weight rows per tile (MMA M)
-constexpr int kGroup = 128;                     // k per unit = one quant group
-constexpr int kBlockBytes = kTileN * kGroup / 2; // packed bytes per unit
-constexpr int kMathWarps = 8;
-constexpr int kThreads = 32 * (4 + kMathWarps);
-constexpr int kStages = 8;
-constexpr int kASlots = 3;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kTileN = 128;                       // weight rows per tile (MMA M)
+constexpr int kGroup = 128;                       // k per unit = one quant group
+constexpr int kBlockBytes = kTileN * kGroup / 2;  // packed bytes per unit
+constexpr int kAcc = 4;                           // accumulators per group
+constexpr int kIssuers = 4;
+constexpr int kDqWarps = 8;
+constexpr int kDrWarps = 4;
+constexpr int kWarpProdW = 0;                     // weights producer
+constexpr int kWarpProdA = 1;                     // activations producer
+constexpr int kWarpIss0 = 2;                      // 2..5 MMA issuers (2 also owns TMEM)
+constexpr int kWarpDr0 = 6;                       // 6..9 drain
+constexpr int kWarpDq0 = 10;                      // 10..17 dequant
+constexpr int kWarps = kWarpDq0 + kDqWarps;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kASlots = 4;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAcol0 = 0;
 constexpr uint32_t kDcol0 = kASlots * 64;
+constexpr int kScaleAhead = 4;                    // drain-side scale prefetch distance
+constexpr int kStageGroups = 4;                   // groups fetched per stage
 
 template <int NBLK>
 struct Layout {
     static constexpr int kRows = 16 * NBLK;             // activation rows per box
-    static constexpr int kActBox = kRows * 128;         // one 64-k box, swizzled
-    static constexpr int kAct = 2 * kActBox;
+    static constexpr int kActBox = kRows * 128;         // one 64-k block, swizzled
+    static constexpr int kAct = 2 * kStageGroups * kActBox;
     static constexpr int kW = kAct;
-    static constexpr int kS = kW + kBlockBytes;
-    static constexpr int kZ = kS + 256;
-    static constexpr int kStage = ((kZ + 128 + 1023) / 1024) * 1024;
+    static constexpr int kStage = kW + kStageGroups * kBlockBytes;
+    static constexpr int kStages = (192 * 1024) / kStage;
+    static constexpr int kDSets = NBLK == 1 ? 4 : 2;    // ring of accumulator sets
+    static constexpr uint32_t kDSet = kAcc * 16 * NBLK; // columns per set, laid out [block][acc][16]
     static constexpr int kBar = kStages * kStage;
-    static constexpr int kNumBars = 2 * kStages + 2 * kASlots + 4 + 2;
+    // full, empty per stage; afull, aempty per A slot; dfull, dempty per set; done; drain sync
+    static constexpr int kNumBars = 2 * kStages + 2 * kASlots + 2 * kDSets + 2;
     static constexpr int kMisc = kBar + 8 * kNumBars;
     static constexpr int kBytes = kMisc + 64 + 1024;     // + alignment slack
+    static_assert(kStage % 1024 == 0, "stage alignment");
+    static_assert(kDcol0 + kDSets * kDSet <= kTmemCols, "tensor memory plan");
+    static_assert(kBytes <= 227 * 1024, "shared memory plan");
 };
 
 struct Args {
@@ -72,10 +97,40 @@ struct Args {
     long long U;
 };
 
+// Stages: runs of at most kStageGroups consecutive groups of one tile.
+struct StageWalk {
+    int t, g, G, left;
+    __device__ StageWalk(long long u, int n_groups, int units)
+        : t(static_cast<int>(u / n_groups)), g(static_cast<int>(u % n_groups)), G(n_groups), left(units) {}
+    __device__ int size() const { return min(min(kStageGroups, G - g), left); }
+    __device__ void next(int ng) {
+        g += ng;
+        left -= ng;
+        if (g == G) {
+            g = 0;
+            ++t;
+        }
+    }
+};
+
+// Walks (tile, group) in unit order without dividing per unit.
+struct UnitWalk {
+    int t, g, G;
+    __device__ UnitWalk(long long u, int n_groups)
+        : t(static_cast<int>(u / n_groups)), g(static_cast<int>(u % n_groups)), G(n_groups) {}
+    __device__ void next() {
+        if (++g == G) {
+            g = 0;
+            ++t;
+        }
+    }
+};
+
 template <int NBLK>
 __global__ void __launch_bounds__(kThreads, 1)
 w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     using L = Layout<NBLK>;
+    constexpr int S = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -83,14 +138,15 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
 
     const uint32_t bar0 = base_s + L::kBar;
     auto full = [&](int s) { return bar0 + 8u * s; };
-    auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
-    auto afull = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
-    auto aempty = [&](int a) { return bar0 + 8u * (2 * kStages + kASlots + a); };
-    auto dfull = [&](int b) { return bar0 + 8u * (2 * kStages + 2 * kASlots + b); };
-    auto dempty = [&](int b) { return bar0 + 8u * (2 * kStages + 2 * kASlots + 2 + b); };
-    const uint32_t done_bar = bar0 + 8u * (2 * kStages + 2 * kASlots + 4);
-    const uint32_t math_bar = bar0 + 8u * (2 * kStages + 2 * kASlots + 5);
-    uint32_t *misc = reinterpret_cast<uint32_t *>(base + L::kMisc);  // [0] tmem, [1] abort, [2] fixer
+    auto empty = [&](int s) { return bar0 + 8u * (S + s); };
+    auto afull = [&](int a) { return bar0 + 8u * (2 * S + a); };
+    auto aempty = [&](int a) { return bar0 + 8u * (2 * S + kASlots + a); };
+    auto dfull = [&](int b) { return bar0 + 8u * (2 * S + 2 * kASlots + b); };
+    auto dempty = [&](int b) { return bar0 + 8u * (2 * S + 2 * kASlots + L::kDSets + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * S + 2 * kASlots + 2 * L::kDSets);
+    const uint32_t drain_bar = done_bar + 8u;
+    // [0] tmem base, [1] abort flag, [2..3] pending tile + 1 per slot, [4..5] last-arriver flags
+    uint32_t *misc = reinterpret_cast<uint32_t *>(base + L::kMisc);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -101,25 +157,24 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     AbortState ab{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.status};
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(full(s), 1);
-            mbar_init(empty(s), kMathWarps + 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full(s), 2);
+            mbar_init(empty(s), kDqWarps + kIssuers);
         }
         for (int a = 0; a < kASlots; ++a) {
-            mbar_init(afull(a), kMathWarps);
-            mbar_init(aempty(a), 1);
+            mbar_init(afull(a), kDqWarps);
+            mbar_init(aempty(a), kIssuers);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(dfull(b), 1);
-            mbar_init(dempty(b), kMathWarps);
+        for (int b = 0; b < L::kDSets; ++b) {
+            mbar_init(dfull(b), kIssuers);
+            mbar_init(dempty(b), kDrWarps);
         }
-        mbar_init(done_bar, 1);
-        mbar_init(math_bar, kMathWarps);
-        misc[1] = 0;
-        misc[2] = 0;
+        mbar_init(done_bar, kIssuers);
+        mbar_init(drain_bar, kDrWarps);
+        for (int k = 1; k < 16; ++k) misc[k] = 0;
         fence_barrier_init();
     }
-    if (warp == 2) {
+    if (warp == kWarpIss0) {
         tmem_alloc(smem_u32(&misc[0]), kTmemCols);
         tmem_relinquish();
     }
@@ -128,117 +183,114 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     tc_fence_after();
     const uint32_t tmem = misc[0];
 
-    if (warp == 0) {
-        // ------------------------------------------------------- producer
+    if (warp == kWarpProdW || warp == kWarpProdA) {
+        // --------------------------------------------------------- producers
         if (lane == 0) {
-            prefetch_tensormap(&xmap);
-            const uint64_t pol_w = l2_policy_evict_first();
-            const uint64_t pol_x = l2_policy_evict_last();
+            const bool weights = warp == kWarpProdW;
+            if (!weights) prefetch_tensormap(&xmap);
+            const uint64_t pol = weights ? l2_policy_evict_first() : l2_policy_evict_last();
+            StageWalk sw(ub, p.n_groups, nunits);
             int issued = 0;
-            for (int i = 0; i < nunits; ++i) {
-                const int s = i % kStages;
-                if (i >= kStages && !mbar_wait(empty(s), ((i / kStages) - 1) & 1, ab)) break;
-                const long long u = ub + i;
-                const int t = static_cast<int>(u / p.n_groups);
-                const int g = static_cast<int>(u % p.n_groups);
-                const int rows = min(kTileN, p.N - t * kTileN);
-                const uint32_t sbytes = 2u * rows;
-                const uint32_t zbytes = p.zeros ? uint32_t(rows) : 0u;
-                const uint32_t st = base_s + s * L::kStage;
-                mbar_arrive_expect_tx(full(s), kBlockBytes + sbytes + zbytes + L::kAct);
-                bulk_load(st + L::kW, p.wq + (size_t(t) * p.n_groups + g) * kBlockBytes, kBlockBytes,
-                          full(s), pol_w);
-                bulk_load(st + L::kS, p.scales + size_t(g) * p.N + size_t(t) * kTileN, sbytes, full(s),
-                          pol_w);
-                if (p.zeros)
-                    bulk_load(st + L::kZ, p.zeros + size_t(g) * p.N + size_t(t) * kTileN, zbytes,
-                              full(s), pol_w);
-                tma_load_2d(st, &xmap, g * kGroup, 0, full(s), pol_x);
-                tma_load_2d(st + L::kActBox, &xmap, g * kGroup + 64, 0, full(s), pol_x);
+            for (int st = 0; sw.left > 0; ++st) {
+                const int ng = sw.size();
+                const int s = st % S;
+                if (st >= S && !mbar_wait(empty(s), ((st / S) - 1) & 1, ab)) break;
+                const uint32_t sa = base_s + s * L::kStage;
+                if (weights) {
+                    mbar_arrive_expect_tx(full(s), ng * kBlockBytes);
+                    bulk_load(sa + L::kW, p.wq + (size_t(sw.t) * p.n_groups + sw.g) * kBlockBytes,
+                              ng * kBlockBytes, full(s), pol);
+                } else {
+                    mbar_arrive_expect_tx(full(s), L::kAct);
+                    tma_load_3d(sa, &xmap, 0, 0, 2 * sw.g, full(s), pol);
+                }
                 ++issued;
+                sw.next(ng);
             }
             if (*ab.flag) {
                 // Let every copy still in flight land before the CTA exits.
-                for (int i = max(0, issued - kStages); i < issued; ++i)
-                    mbar_wait_bounded(full(i % kStages), (i / kStages) & 1);
+                for (int i = max(0, issued - S); i < issued; ++i)
+                    mbar_wait_bounded(full(i % S), (i / S) & 1);
             }
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------- MMA issuer
+    } else if (warp >= kWarpIss0 && warp < kWarpIss0 + kIssuers) {
+        // ------------------------------------------------------ MMA issuers
         if (lane == 0) {
+            const int me = warp - kWarpIss0;
             constexpr uint32_t idesc = idesc_f16_f32(128, 16);
-            for (int i = 0; i < nunits; ++i) {
-                const int s = i % kStages;
-                const int slot = i % kASlots;
-                const int buf = i & 1;
-                if (!mbar_wait(full(s), (i / kStages) & 1, ab)) break;
-                if (!mbar_wait(afull(slot), (i / kASlots) & 1, ab)) break;
-                if (i >= 2 && !mbar_wait(dempty(buf), ((i >> 1) - 1) & 1, ab)) break;
-                tc_fence_after();
-                const uint32_t act = base_s + s * L::kStage;
-#pragma unroll
-                for (int j = 0; j < kGroup / 16; ++j) {
-#pragma unroll
-                    for (int b = 0; b < NBLK; ++b) {
-                        const uint32_t baddr = act + (j >> 2) * L::kActBox + b * 2048 + (j & 3) * 32;
-                        mma_f16_ts(tmem + kDcol0 + buf * 16 * NBLK + 16 * b,
-                                   tmem + kAcol0 + slot * 64 + 8 * j, sdesc_sw128(baddr), idesc,
-                                   j > 0 ? 1u : 0u);
+            StageWalk sw(ub, p.n_groups, nunits);
+            bool ok = true;
+            int i = 0;
+            for (int st = 0; sw.left > 0 && ok; ++st) {
+                const int ng = sw.size();
+                const int s = st % S;
+                if (!mbar_wait(full(s), (st / S) & 1, ab)) break;
+                for (int jj = 0; jj < ng; ++jj, ++i) {
+                    const int slot = i % kASlots;
+                    const int set = i % L::kDSets;
+                    if (!mbar_wait(afull(slot), (i / kASlots) & 1, ab) ||
+                        (i >= L::kDSets && !mbar_wait(dempty(set), ((i / L::kDSets) - 1) & 1, ab))) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint32_t act = base_s + s * L::kStage + 2 * jj * L::kActBox;
+                    const uint32_t dset = tmem + kDcol0 + set * L::kDSet;
+#pragma unroll
+                    for (int j = 0; j < kGroup / 16; ++j) {
+#pragma unroll
+                        for (int b = 0; b < NBLK; ++b) {
+                            const int a = j % kAcc;
+                            if ((a * NBLK + b) % kIssuers != me) continue;
+                            const uint32_t baddr = act + (j >> 2) * L::kActBox + b * 2048 + (j & 3) * 32;
+                            mma_f16_ts(dset + (b * kAcc + a) * 16, tmem + kAcol0 + slot * 64 + 8 * j,
+                                       sdesc_sw128(baddr), idesc, j >= kAcc ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(aempty(slot));
+                    mma_commit(dfull(set));
+                    if (jj == ng - 1) mma_commit(empty(s));
                 }
-                mma_commit(empty(s));
-                mma_commit(aempty(slot));
-                mma_commit(dfull(buf));
+                sw.next(ng);
             }
-            // Every MMA this thread issued has finished once this arrives.
+            // Every MMA of this issuer has finished once this arrives.
             mma_commit(done_bar);
             mbar_wait_bounded(done_bar, 0);
         }
-    } else if (warp >= 4) {
-        // ------------------------------------------- dequant + epilogue
-        const int mw = warp - 4;
+    } else if (warp >= kWarpDq0) {
+        // --------------------------------------------------------- dequant
+        const int dq = warp - kWarpDq0;
         const int q = warp & 3;                 // TMEM lane quarter
-        const int h = mw >> 2;                  // k half (dequant), column half (drain)
+        const int kh = dq >> 2;                 // k half: chunks 2kh, 2kh+1 of the packed row
         const int r = 32 * q + lane;            // row inside the tile
         const uint32_t lane_base = uint32_t(32 * q) << 16;
-        float acc[NBLK][8];
-#pragma unroll
-        for (int b = 0; b < NBLK; ++b)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[b][j] = 0.f;
-        float scale_q[2] = {0.f, 0.f};
         const __half2 sixteenth = __float2half2_rn(0.0625f);
-        uint32_t math_syncs = 0;
-        // Barrier over the math warps only, bounded like every other wait.
-        auto math_sync = [&]() -> bool {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(math_bar);
-            return warp_wait(math_bar, (math_syncs++) & 1, ab);
-        };
+        StageWalk sw(ub, p.n_groups, nunits);
+        int d_st = 0, d_jj = 0, d_ng = sw.size();
 
-        auto dequant = [&](int i) -> bool {
-            const int s = i % kStages;
-            if (!warp_wait(full(s), (i / kStages) & 1, ab)) return false;
-            const uint8_t *st = base + s * L::kStage;
-            const uint4 w0 = *reinterpret_cast<const uint4 *>(st + L::kW + ((2 * h) * 128 + r) * 16);
-            const uint4 w1 = *reinterpret_cast<const uint4 *>(st + L::kW + ((2 * h + 1) * 128 + r) * 16);
-            const long long u = ub + i;
-            const int t = static_cast<int>(u / p.n_groups);
-            const int n = t * kTileN + r;
-            float sc = 0.f;
+        // Loads the next unit's 64 codes of this row and k half (units are
+        // taken in order), releases its stage after the stage's last unit and
+        // dequantizes into 32 half2 registers.
+        auto load_dequant = [&](uint32_t (&regs)[32]) -> bool {
+            const int s = d_st % S;
+            if (d_jj == 0 && !warp_wait(full(s), (d_st / S) & 1, ab)) return false;
+            const uint8_t *st = base + s * L::kStage + L::kW + d_jj * kBlockBytes;
+            const uint4 va = *reinterpret_cast<const uint4 *>(st + ((2 * kh) * 128 + r) * 16);
+            const uint4 vb = *reinterpret_cast<const uint4 *>(st + ((2 * kh + 1) * 128 + r) * 16);
             uint32_t z = 8;
-            if (n < p.N) {
-                sc = __half2float(reinterpret_cast<const __half *>(st + L::kS)[r]);
-                if (p.zeros) z = st[L::kZ + r];
+            const int n = sw.t * kTileN + r;
+            if (p.zeros != nullptr && n < p.N) z = __ldg(p.zeros + size_t(sw.g + d_jj) * p.N + n);
+            if (++d_jj == d_ng) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty(s));
+                sw.next(d_ng);
+                ++d_st;
+                d_jj = 0;
+                d_ng = sw.size();
             }
-            scale_q[i & 1] = sc;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty(s));
-
             const __half2 zlo = u32_as_h2((0x6400u + z) * 0x10001u);          // 1024 + z
             const __half2 zhi = __float2half2_rn(-(64.f + float(z)));
-            const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-            uint32_t regs[32];
+            const uint32_t words[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
             for (int wi = 0; wi < 8; ++wi) {
                 const uint32_t v = words[wi];
@@ -253,17 +305,62 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 regs[4 * wi + 2] = h2_as_u32(__hsub2(u32_as_h2(lo1), zlo));
                 regs[4 * wi + 3] = h2_as_u32(__hfma2(u32_as_h2(hi1), sixteenth, zhi));
             }
-            const int slot = i % kASlots;
-            if (i >= kASlots && !warp_wait(aempty(slot), ((i / kASlots) - 1) & 1, ab)) return false;
-            tc_fence_after();
-            tmem_st_32x32b_x32(tmem + lane_base + kAcol0 + slot * 64 + 32 * h, regs);
-            tc_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(afull(slot));
             return true;
         };
 
+        uint32_t cur[32], nxt[32];
+        bool ok = nunits > 0 && load_dequant(cur);
+        for (int i = 0; i < nunits && ok; ++i) {
+            const int slot = i % kASlots;
+            if (i >= kASlots && !warp_wait(aempty(slot), ((i / kASlots) - 1) & 1, ab)) break;
+            tc_fence_after();
+            tmem_st_32x32b_x32(tmem + lane_base + kAcol0 + slot * 64 + 32 * kh, cur);
+            if (i + 1 < nunits) ok = load_dequant(nxt);            // overlaps the store
+            tc_wait_st();
+            tc_keep_alive<32>(cur);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(afull(slot));
+#pragma unroll
+            for (int k = 0; k < 32; ++k) cur[k] = nxt[k];
+        }
+    } else if (warp >= kWarpDr0 && warp < kWarpDr0 + kDrWarps) {
+        // ----------------------------------------------------------- drain
+        const int dr = warp - kWarpDr0;
+        const int q = warp & 3;
+        const int r = 32 * q + lane;
+        const uint32_t lane_base = uint32_t(32 * q) << 16;
+        float acc[NBLK][16];
+#pragma unroll
+        for (int b = 0; b < NBLK; ++b)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[b][j] = 0.f;
+        uint32_t pend_prev[2] = {0u, 0u};
+        uint32_t drain_syncs = 0;
+        auto drain_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(drain_bar);
+            return warp_wait(drain_bar, (drain_syncs++) & 1, ab);
+        };
+
+        // Group scales, prefetched kScaleAhead units ahead.
+        UnitWalk ws(ub, p.n_groups);
+        float sp[kScaleAhead];
+        auto load_scale = [&](int i) -> float {
+            float v = 0.f;
+            if (i < nunits) {
+                const int n = ws.t * kTileN + r;
+                if (n < p.N) v = __half2float(__ldg(p.scales + size_t(ws.g) * p.N + n));
+                ws.next();
+            }
+            return v;
+        };
+#pragma unroll
+        for (int k = 0; k < kScaleAhead; ++k) sp[k] = load_scale(k);
+
+        // Tile finished by this CTA alone: write C.  Otherwise publish the fp32
+        // partial tile and count this CTA in; whether it arrived last is read
+        // back after the CTA's last group (see fixup).
         auto flush = [&](int t) -> bool {
             const long long t0u = (long long)t * p.n_groups;
             const long long t1u = t0u + p.n_groups;
@@ -273,8 +370,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
 #pragma unroll
                     for (int b = 0; b < NBLK; ++b)
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int m = 16 * b + 8 * h + j;
+                        for (int j = 0; j < 16; ++j) {
+                            const int m = 16 * b + j;
                             if (m < p.M) p.C[size_t(m) * p.N + n] = __float2half_rn(acc[b][j]);
                         }
                 }
@@ -286,45 +383,83 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
 #pragma unroll
             for (int b = 0; b < NBLK; ++b)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int m = 16 * b + 8 * h + j;
+                for (int j = 0; j < 16; ++j) {
+                    const int m = 16 * b + j;
                     if (m < p.M) __stcg(part + m * kTileN + r, acc[b][j]);
                 }
-            __threadfence();
-            if (!math_sync()) return false;
-            const int cf = split_owner(t0u, p.U, p.P);
-            const int cl = split_owner(t1u - 1, p.U, p.P);
-            if (mw == 0 && lane == 0) {
-                const uint32_t prev = atomicAdd(&p.tile_cnt[t], 1u);
-                const bool last = prev == uint32_t(cl - cf);
-                if (last) atomicExch(&p.tile_cnt[t], 0u);
-                misc[2] = last ? 1u : 0u;
+            if (!drain_sync()) return false;
+            if (dr == 0 && lane == 0) {
+                misc[2 + slot] = uint32_t(t) + 1u;
+                pend_prev[slot] = atom_add_release_gpu(&p.tile_cnt[t], 1u);
             }
-            if (!math_sync()) return false;
-            if (misc[2]) {
-                __threadfence();
-                float sum[NBLK][8];
+            return true;
+        };
+
+        // After the CTA's last group: for each published partial tile, if this
+        // CTA arrived last, sum every contributor's partial in CTA order.
+        auto fixup = [&]() -> bool {
+            if (dr == 0 && lane == 0) {
+                for (int sl = 0; sl < 2; ++sl) {
+                    const uint32_t tp = misc[2 + sl];
+                    uint32_t last = 0u;
+                    if (tp != 0u) {
+                        const long long t0u = (long long)(tp - 1u) * p.n_groups;
+                        const int cf = split_owner(t0u, p.U, p.P);
+                        const int cl = split_owner(t0u + p.n_groups - 1, p.U, p.P);
+                        last = pend_prev[sl] == uint32_t(cl - cf) ? 1u : 0u;
+                        if (last) {
+                            fence_acq_rel_gpu();
+                            p.tile_cnt[tp - 1u] = 0u;
+                        }
+                    }
+                    misc[4 + sl] = last;
+                }
+            }
+            if (!drain_sync()) return false;
+            constexpr int kPart = 16 * NBLK * kTileN;
+            for (int sl = 0; sl < 2; ++sl) {
+                if (!misc[4 + sl]) continue;
+                const int t = int(misc[2 + sl]) - 1;
+                const long long t0u = (long long)t * p.n_groups;
+                const int cf = split_owner(t0u, p.U, p.P);
+                const int cl = split_owner(t0u + p.n_groups - 1, p.U, p.P);
+                const int n = t * kTileN + r;
+                float sum[NBLK][16];
 #pragma unroll
                 for (int b = 0; b < NBLK; ++b)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) sum[b][j] = 0.f;
-                for (int cc = cf; cc <= cl; ++cc) {
-                    const int sl = (split_begin(cc, p.U, p.P) >= t0u) ? 0 : 1;
-                    const float *src = p.partial + (size_t(cc) * 2 + sl) * kPart;
+                    for (int j = 0; j < 16; ++j) sum[b][j] = 0.f;
+                constexpr int kBatch = NBLK == 1 ? 4 : 2;     // independent loads in flight
+                for (int c0 = cf; c0 <= cl; c0 += kBatch) {
+                    float v[kBatch][NBLK][16];
 #pragma unroll
-                    for (int b = 0; b < NBLK; ++b)
+                    for (int u = 0; u < kBatch; ++u) {
+                        const int cc = c0 + u;
+                        const int sl2 = (cc <= cl && split_begin(cc, p.U, p.P) >= t0u) ? 0 : 1;
+                        const float *src = p.partial + (size_t(cc <= cl ? cc : cl) * 2 + sl2) * kPart;
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int m = 16 * b + 8 * h + j;
-                            if (m < p.M) sum[b][j] += __ldcg(src + m * kTileN + r);
+                        for (int b = 0; b < NBLK; ++b)
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int m = 16 * b + j;
+                                v[u][b][j] = (cc <= cl && m < p.M) ? __ldcg(src + m * kTileN + r) : 0.f;
+                            }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u)
+                        if (c0 + u <= cl) {
+#pragma unroll
+                            for (int b = 0; b < NBLK; ++b)
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) sum[b][j] += v[u][b][j];
                         }
                 }
                 if (n < p.N) {
 #pragma unroll
                     for (int b = 0; b < NBLK; ++b)
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int m = 16 * b + 8 * h + j;
+                        for (int j = 0; j < 16; ++j) {
+                            const int m = 16 * b + j;
                             if (m < p.M) p.C[size_t(m) * p.N + n] = __float2half_rn(sum[b][j]);
                         }
                 }
@@ -332,53 +467,69 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             return true;
         };
 
-        auto drain = [&](int i) -> bool {
-            const int buf = i & 1;
-            if (!warp_wait(dfull(buf), (i >> 1) & 1, ab)) return false;
+        UnitWalk wd(ub, p.n_groups);
+        bool ok = true;
+        for (int i = 0; i < nunits && ok; ++i) {
+            const int set = i % L::kDSets;
+            if (!warp_wait(dfull(set), (i / L::kDSets) & 1, ab)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
-            uint32_t d[NBLK][8];
+            const float sc = sp[0];
 #pragma unroll
-            for (int b = 0; b < NBLK; ++b)
-                tmem_ld_32x32b_x8(tmem + lane_base + kDcol0 + buf * 16 * NBLK + 16 * b + 8 * h, d[b]);
-            tc_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(dempty(buf));
-            const float sc = scale_q[i & 1];
+            for (int k = 0; k + 1 < kScaleAhead; ++k) sp[k] = sp[k + 1];
+            sp[kScaleAhead - 1] = load_scale(i + kScaleAhead);
+            const uint32_t dset = tmem + lane_base + kDcol0 + set * L::kDSet;
 #pragma unroll
-            for (int b = 0; b < NBLK; ++b)
+            for (int b = 0; b < NBLK; ++b) {
+                // accumulators 0,1 then 2,3 of block b: ((d0 + d1) + d2) + d3
+                float g[16];
+                uint32_t d[32];
+                tmem_ld_32x32b_x32(dset + (b * kAcc) * 16, d);
+                tc_wait_ld_keep<32>(d);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[b][j] = fmaf(sc, __uint_as_float(d[b][j]), acc[b][j]);
-            const long long u = ub + i;
-            const int t = static_cast<int>(u / p.n_groups);
-            if (u + 1 == (long long)(t + 1) * p.n_groups || u + 1 == ue) {
-                if (!flush(t)) return false;
+                for (int j = 0; j < 16; ++j) g[j] = __uint_as_float(d[j]) + __uint_as_float(d[16 + j]);
+                tmem_ld_32x32b_x32(dset + (b * kAcc + 2) * 16, d);
+                tc_wait_ld_keep<32>(d);
+                if (b == NBLK - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(dempty(set));
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    g[j] = (g[j] + __uint_as_float(d[j])) + __uint_as_float(d[16 + j]);
+                    acc[b][j] = fmaf(sc, g[j], acc[b][j]);
+                }
+            }
+            const int t = wd.t;
+            const bool tile_end = wd.g == p.n_groups - 1;
+            wd.next();
+            if (tile_end || i == nunits - 1) {
+                if (!flush(t)) {
+                    ok = false;
+                    break;
+                }
 #pragma unroll
                 for (int b = 0; b < NBLK; ++b)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[b][j] = 0.f;
+                    for (int j = 0; j < 16; ++j) acc[b][j] = 0.f;
             }
-            return true;
-        };
-
-        bool ok = true;
-        for (int i = 0; i < nunits && ok; ++i) {
-            ok = dequant(i);
-            if (ok && i > 0) ok = drain(i - 1);
         }
-        if (ok && nunits > 0) drain(nunits - 1);
+        if (ok) fixup();
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 2) {
+    if (warp == kWarpIss0) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
 }
 
 template <int NBLK>
-w4v_status launch(const DeviceInfo *info, const CUtensorMap &xmap, const Args &a, cudaStream_t stream) {
+w4v_status launch(const CUtensorMap &xmap, const Args &a, cudaStream_t stream) {
     using L = Layout<NBLK>;
     static int configured_for = -1;
     int dev = 0;
@@ -429,11 +580,11 @@ w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t
                                               size_t(kMaxCtas) * 2 * 16 * nblk * kTileN * sizeof(float));
     a.status = info->status;
     CUtensorMap xmap;
-    st = encode_tmap_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, uint64_t(K), uint64_t(M),
-                        uint64_t(K) * 2, 64, 16 * nblk, CU_TENSOR_MAP_SWIZZLE_128B);
+    st = encode_tmap_kblocks(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, uint64_t(K), uint64_t(M), 64, 16 * nblk,
+                             2 * kStageGroups, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != W4V_OK) return st;
-    if (nblk == 1) return launch<1>(info, xmap, a, stream);
-    return launch<2>(info, xmap, a, stream);
+    if (nblk == 1) return launch<1>(xmap, a, stream);
+    return launch<2>(xmap, a, stream);
 }
 
 }  // namespace w4v

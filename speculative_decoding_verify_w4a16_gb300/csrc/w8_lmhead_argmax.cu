@@ -10,21 +10,27 @@
 // so it is bound by HBM bandwidth for the verify sizes):
 //   * 128-row vocabulary tiles are the MMA's M side, activation rows its N
 //     side in blocks of 16 (M <= 128).  Each CTA owns a contiguous run of
-//     whole tiles.
-//   * The int8 tile (128 x 128 bytes per k-chunk) arrives by 2-D TMA with
-//     128-byte swizzle straight from the row-major [V][K] matrix; the
-//     activation slice arrives the same way (reused from L2 by every CTA).
-//   * Math warps widen int8 to exact fp16 (XOR 0x80, PRMT into the mantissa
-//     of 1024, subtract 1152) and store the tile into tensor memory; one
-//     thread issues tcgen05.mma with A from TMEM, accumulating the whole K in
-//     TMEM.
-//   * At the end of a tile each thread owns one vocabulary row: it scales its
-//     logits, turns each into an order-preserving 32-bit key, and a warp
+//     whole tiles; units are (tile, 128-k chunk).
+//   * An SM completes about one TMA copy per ~650 cycles whatever its size,
+//     so a stage is two k-chunks of a tile: one 3-D TMA of 32 KB of int8
+//     weights (128-byte swizzle, straight from the row-major [V][K] matrix)
+//     and one 3-D TMA of the matching activation slices; two producer
+//     threads issue them.
+//   * Eight dequant warps widen int8 to exact fp16 (XOR 0x80, PRMT into the
+//     mantissa of 1024, subtract 1152) and store it into tensor memory with
+//     32-column stores; the store of one unit overlaps the dequant of the
+//     next.
+//   * Four issuer threads (one MMA per ~55 cycles each) run tcgen05.mma with
+//     A from TMEM, accumulating the whole K of a tile in TMEM; the k-steps go
+//     round-robin into independent accumulators, each owned by one issuer.
+//   * Four drain warps finish a tile: add the accumulators in a fixed order,
+//     scale, turn each logit into an order-preserving 32-bit key, and a warp
 //     max-reduction plus a min-reduction over the winning lanes gives the
-//     lowest-index maximum of the warp; a shared-memory 64-bit atomicMax of
-//     (key, ~index) keeps the CTA's best per row.
-//   * CTAs publish their best keys; the last CTA to arrive (atomic counter,
-//     no waiting) takes the maximum over CTAs and writes the token ids.
+//     lowest-index maximum; a shared-memory 64-bit atomicMax of (key, ~index)
+//     keeps the CTA's best per row.
+//   * Each CTA folds its best keys into one global 64-bit atomicMax per row;
+//     the last CTA to arrive (release/acquire counter, no waiting) reads and
+//     clears them and writes the token ids.
 #include "runtime.h"
 #include "sm103_ptx.cuh"
 
@@ -34,29 +40,58 @@ namespace {
 constexpr int kTileV = 128;
 constexpr int kChunk = 128;                 // k per unit (bytes of int8)
 constexpr int kWBytes = kTileV * kChunk;    // 16 KB per unit
-constexpr int kMathWarps = 8;
-constexpr int kThreads = 32 * (4 + kMathWarps);
 constexpr int kMaxRows = 128;
+constexpr int kIssuers = 4;
+constexpr int kDqWarps = 8;
+constexpr int kDrWarps = 4;
+constexpr int kWarpProdW = 0;
+constexpr int kWarpProdA = 1;
+constexpr int kWarpIss0 = 2;                // 2..5 (2 also owns TMEM)
+constexpr int kWarpDr0 = 6;                 // 6..9
+constexpr int kWarpDq0 = 10;                // 10..17
+constexpr int kWarps = kWarpDq0 + kDqWarps;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kASlots = 4;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAcol0 = 0;
+constexpr uint32_t kDcol0 = kASlots * 64;
+constexpr int kStageChunks = 2;             // k-chunks fetched per stage
 
 template <int NBLK>
 struct Layout {
     static constexpr int kRows = 16 * NBLK;
-    static constexpr int kActBox = kRows * 128;
-    static constexpr int kAct = 2 * kActBox;
+    static constexpr int kActBox = kRows * 128;         // one 64-k block, swizzled
+    static constexpr int kAct = 2 * kStageChunks * kActBox;
     static constexpr int kW = kAct;                     // 1024-aligned
-    static constexpr int kS = kW + kWBytes;
-    static constexpr int kStage = ((kS + 256 + 1023) / 1024) * 1024;
-    static constexpr int kStages = (200 * 1024) / kStage > 8 ? 8 : (200 * 1024) / kStage;
-    static constexpr int kASlots = NBLK <= 2 ? 3 : 4;
-    static constexpr uint32_t kTmemCols = NBLK <= 2 ? 256 : 512;
-    static constexpr uint32_t kAcol0 = 0;
-    static constexpr uint32_t kDcol0 = kASlots * 64;
+    static constexpr int kStage = kW + kStageChunks * kWBytes;
+    static constexpr int kStages = (196 * 1024) / kStage > 6 ? 6 : (196 * 1024) / kStage;
+    // Independent accumulators per tile: the same count for every M <= 32,
+    // so the per-logit arithmetic does not depend on M there.
+    static constexpr int kAcc = NBLK <= 2 ? 4 : 8 / NBLK;
+    static constexpr uint32_t kDSet = kAcc * 16 * NBLK;  // laid out [block][acc][16]
     static constexpr int kBar = kStages * kStage;
     static constexpr int kNumBars = 2 * kStages + 2 * kASlots + 4 + 2;
     static constexpr int kBest = ((kBar + 8 * kNumBars + 7) / 8) * 8;   // u64 [128]
     static constexpr int kMisc = kBest + 8 * kMaxRows;
     static constexpr int kBytes = kMisc + 64 + 1024;
-    static_assert(kDcol0 + 2 * 16 * NBLK <= kTmemCols, "tensor memory plan");
+    static_assert(kStage % 1024 == 0, "stage alignment");
+    static_assert(kDcol0 + 2 * kDSet <= kTmemCols, "tensor memory plan");
+    static_assert(kBytes <= 227 * 1024, "shared memory plan");
+};
+
+// Stages: runs of at most kStageChunks consecutive k-chunks of one tile.
+struct ChunkWalk {
+    int j, c, nch, ntiles;
+    __device__ ChunkWalk(int n_chunks, int tiles) : j(0), c(0), nch(n_chunks), ntiles(tiles) {}
+    __device__ bool more() const { return j < ntiles; }
+    __device__ int size() const { return min(kStageChunks, nch - c); }
+    __device__ void next(int ng) {
+        c += ng;
+        if (c == nch) {
+            c = 0;
+            ++j;
+        }
+    }
 };
 
 struct Args {
@@ -65,7 +100,7 @@ struct Args {
     int32_t *argmax_out;
     float *maxlogit;
     float *logits;
-    unsigned long long *keys;   // [kMaxCtas][128]
+    unsigned long long *keys;   // [128], zero between calls
     uint32_t *counter;
     uint32_t *status;
     int M, K, V;
@@ -91,8 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                         const Args p) {
     using L = Layout<NBLK>;
-    constexpr int kStages = L::kStages;
-    constexpr int kASlots = L::kASlots;
+    constexpr int S = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -100,13 +134,13 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
 
     const uint32_t bar0 = base_s + L::kBar;
     auto full = [&](int s) { return bar0 + 8u * s; };
-    auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
-    auto afull = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
-    auto aempty = [&](int a) { return bar0 + 8u * (2 * kStages + kASlots + a); };
-    auto dfull = [&](int b) { return bar0 + 8u * (2 * kStages + 2 * kASlots + b); };
-    auto dempty = [&](int b) { return bar0 + 8u * (2 * kStages + 2 * kASlots + 2 + b); };
-    const uint32_t done_bar = bar0 + 8u * (2 * kStages + 2 * kASlots + 4);
-    const uint32_t math_bar = bar0 + 8u * (2 * kStages + 2 * kASlots + 5);
+    auto empty = [&](int s) { return bar0 + 8u * (S + s); };
+    auto afull = [&](int a) { return bar0 + 8u * (2 * S + a); };
+    auto aempty = [&](int a) { return bar0 + 8u * (2 * S + kASlots + a); };
+    auto dfull = [&](int b) { return bar0 + 8u * (2 * S + 2 * kASlots + b); };
+    auto dempty = [&](int b) { return bar0 + 8u * (2 * S + 2 * kASlots + 2 + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * S + 2 * kASlots + 4);
+    const uint32_t drain_bar = done_bar + 8u;
     unsigned long long *best = reinterpret_cast<unsigned long long *>(base + L::kBest);
     uint32_t *misc = reinterpret_cast<uint32_t *>(base + L::kMisc);   // [0] tmem, [1] abort, [2] last
 
@@ -115,31 +149,32 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
     const int cta = blockIdx.x;
     const int tb = static_cast<int>(split_begin(cta, p.n_tiles, p.P));
     const int te = static_cast<int>(split_begin(cta + 1, p.n_tiles, p.P));
-    const int nunits = (te - tb) * p.n_chunks;
+    const int ntiles = te - tb;
+    const int nunits = ntiles * p.n_chunks;
     AbortState ab{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.status};
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(full(s), 1);
-            mbar_init(empty(s), kMathWarps + 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full(s), 2);
+            mbar_init(empty(s), kDqWarps + kIssuers);
         }
         for (int a = 0; a < kASlots; ++a) {
-            mbar_init(afull(a), kMathWarps);
-            mbar_init(aempty(a), 1);
+            mbar_init(afull(a), kDqWarps);
+            mbar_init(aempty(a), kIssuers);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(dfull(b), 1);
-            mbar_init(dempty(b), kMathWarps);
+            mbar_init(dfull(b), kIssuers);
+            mbar_init(dempty(b), kDrWarps);
         }
-        mbar_init(done_bar, 1);
-        mbar_init(math_bar, kMathWarps);
+        mbar_init(done_bar, kIssuers);
+        mbar_init(drain_bar, kDrWarps);
         misc[1] = 0;
         misc[2] = 0;
         fence_barrier_init();
     }
     if (threadIdx.x < kMaxRows) best[threadIdx.x] = 0ull;
-    if (warp == 2) {
-        tmem_alloc(smem_u32(&misc[0]), L::kTmemCols);
+    if (warp == kWarpIss0) {
+        tmem_alloc(smem_u32(&misc[0]), kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -147,98 +182,110 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
     tc_fence_after();
     const uint32_t tmem = misc[0];
 
-    if (warp == 0) {
+    if (warp == kWarpProdW || warp == kWarpProdA) {
+        // --------------------------------------------------------- producers
         if (lane == 0) {
-            prefetch_tensormap(&xmap);
-            prefetch_tensormap(&wmap);
-            const uint64_t pol_w = l2_policy_evict_first();
-            const uint64_t pol_x = l2_policy_evict_last();
+            const bool weights = warp == kWarpProdW;
+            prefetch_tensormap(weights ? &wmap : &xmap);
+            const uint64_t pol = weights ? l2_policy_evict_first() : l2_policy_evict_last();
             int issued = 0;
-            for (int i = 0; i < nunits; ++i) {
-                const int s = i % kStages;
-                if (i >= kStages && !mbar_wait(empty(s), ((i / kStages) - 1) & 1, ab)) break;
-                const int t = tb + i / p.n_chunks;
-                const int c = i % p.n_chunks;
-                const uint32_t st = base_s + s * L::kStage;
-                const uint32_t sbytes = c == 0 ? 2u * uint32_t(min(kTileV, p.V - t * kTileV)) : 0u;
-                mbar_arrive_expect_tx(full(s), kWBytes + L::kAct + sbytes);
-                tma_load_2d(st + L::kW, &wmap, c * kChunk, t * kTileV, full(s), pol_w);
-                tma_load_2d(st, &xmap, c * kChunk, 0, full(s), pol_x);
-                tma_load_2d(st + L::kActBox, &xmap, c * kChunk + 64, 0, full(s), pol_x);
-                if (sbytes) bulk_load(st + L::kS, p.scale + size_t(t) * kTileV, sbytes, full(s), pol_w);
+            ChunkWalk cw(p.n_chunks, ntiles);
+            for (int st = 0; cw.more(); ++st) {
+                const int ng = cw.size();
+                const int s = st % S;
+                if (st >= S && !mbar_wait(empty(s), ((st / S) - 1) & 1, ab)) break;
+                const uint32_t sa = base_s + s * L::kStage;
+                if (weights) {
+                    mbar_arrive_expect_tx(full(s), kStageChunks * kWBytes);
+                    tma_load_3d(sa + L::kW, &wmap, 0, (tb + cw.j) * kTileV, cw.c, full(s), pol);
+                } else {
+                    mbar_arrive_expect_tx(full(s), L::kAct);
+                    tma_load_3d(sa, &xmap, 0, 0, 2 * cw.c, full(s), pol);
+                }
                 ++issued;
+                cw.next(ng);
             }
             if (*ab.flag) {
-                for (int i = max(0, issued - kStages); i < issued; ++i)
-                    mbar_wait_bounded(full(i % kStages), (i / kStages) & 1);
+                for (int i = max(0, issued - S); i < issued; ++i)
+                    mbar_wait_bounded(full(i % S), (i / S) & 1);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp >= kWarpIss0 && warp < kWarpIss0 + kIssuers) {
+        // ------------------------------------------------------ MMA issuers
         if (lane == 0) {
+            const int me = warp - kWarpIss0;
             constexpr uint32_t idesc = idesc_f16_f32(128, 16);
-            for (int i = 0; i < nunits; ++i) {
-                const int s = i % kStages;
-                const int slot = i % kASlots;
-                const int j = i / p.n_chunks;
-                const int c = i % p.n_chunks;
-                const int buf = j & 1;
-                if (!mbar_wait(full(s), (i / kStages) & 1, ab)) break;
-                if (!mbar_wait(afull(slot), (i / kASlots) & 1, ab)) break;
-                if (c == 0 && j >= 2 && !mbar_wait(dempty(buf), ((j >> 1) - 1) & 1, ab)) break;
-                tc_fence_after();
-                const uint32_t act = base_s + s * L::kStage;
-#pragma unroll
-                for (int kk = 0; kk < kChunk / 16; ++kk) {
-#pragma unroll
-                    for (int b = 0; b < NBLK; ++b) {
-                        const uint32_t baddr = act + (kk >> 2) * L::kActBox + b * 2048 + (kk & 3) * 32;
-                        mma_f16_ts(tmem + L::kDcol0 + buf * 16 * NBLK + 16 * b,
-                                   tmem + L::kAcol0 + slot * 64 + 8 * kk, sdesc_sw128(baddr), idesc,
-                                   (c > 0 || kk > 0) ? 1u : 0u);
+            ChunkWalk cw(p.n_chunks, ntiles);
+            bool ok = true;
+            int i = 0;
+            for (int st = 0; cw.more() && ok; ++st) {
+                const int ng = cw.size();
+                const int s = st % S;
+                if (!mbar_wait(full(s), (st / S) & 1, ab)) break;
+                for (int jj = 0; jj < ng; ++jj, ++i) {
+                    const int j = cw.j, c = cw.c + jj;
+                    const int slot = i % kASlots;
+                    const int buf = j & 1;
+                    if (!mbar_wait(afull(slot), (i / kASlots) & 1, ab) ||
+                        (c == 0 && j >= 2 && !mbar_wait(dempty(buf), ((j >> 1) - 1) & 1, ab))) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint32_t act = base_s + s * L::kStage + 2 * jj * L::kActBox;
+                    const uint32_t dset = tmem + kDcol0 + buf * L::kDSet;
+#pragma unroll
+                    for (int kk = 0; kk < kChunk / 16; ++kk) {
+#pragma unroll
+                        for (int b = 0; b < NBLK; ++b) {
+                            const int a = kk % L::kAcc;
+                            if ((a * NBLK + b) % kIssuers != me) continue;
+                            const uint32_t baddr = act + (kk >> 2) * L::kActBox + b * 2048 + (kk & 3) * 32;
+                            mma_f16_ts(dset + (b * L::kAcc + a) * 16, tmem + kAcol0 + slot * 64 + 8 * kk,
+                                       sdesc_sw128(baddr), idesc, (c > 0 || kk >= L::kAcc) ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(aempty(slot));
+                    if (c == p.n_chunks - 1) mma_commit(dfull(buf));
+                    if (jj == ng - 1) mma_commit(empty(s));
                 }
-                mma_commit(empty(s));
-                mma_commit(aempty(slot));
-                if (c == p.n_chunks - 1) mma_commit(dfull(buf));
+                cw.next(ng);
             }
             mma_commit(done_bar);
             mbar_wait_bounded(done_bar, 0);
         }
-    } else if (warp >= 4) {
-        const int mw = warp - 4;
+    } else if (warp >= kWarpDq0) {
+        // --------------------------------------------------------- dequant
+        const int dq = warp - kWarpDq0;
         const int q = warp & 3;
-        const int h = mw >> 2;
+        const int kh = dq >> 2;                 // 64-byte half of the 128-byte row
         const int r = 32 * q + lane;
         const uint32_t lane_base = uint32_t(32 * q) << 16;
-        float scale_q[2] = {0.f, 0.f};
         const __half2 bias = u32_as_h2(0x64806480u);    // 1152 = 1024 + 128 in both halves
-        uint32_t math_syncs = 0;
-        auto math_sync = [&]() -> bool {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(math_bar);
-            return warp_wait(math_bar, (math_syncs++) & 1, ab);
-        };
 
-        auto dequant = [&](int i) -> bool {
-            const int s = i % kStages;
-            if (!warp_wait(full(s), (i / kStages) & 1, ab)) return false;
-            const uint8_t *st = base + s * L::kStage;
-            const int j = i / p.n_chunks;
-            const int c = i % p.n_chunks;
+        ChunkWalk cw(p.n_chunks, ntiles);
+        int d_st = 0, d_jj = 0, d_ng = cw.size();
+        // Loads the next unit's 64 bytes of this row (units in order), releases
+        // its stage after the stage's last unit and widens them to 32 half2.
+        auto load_dequant = [&](uint32_t (&regs)[32]) -> bool {
+            const int s = d_st % S;
+            if (d_jj == 0 && !warp_wait(full(s), (d_st / S) & 1, ab)) return false;
+            const uint8_t *st = base + s * L::kStage + L::kW + d_jj * kWBytes;
             uint4 w[4];
 #pragma unroll
             for (int ci = 0; ci < 4; ++ci) {
-                const int chunk = 4 * h + ci;
+                const int chunk = 4 * kh + ci;
                 const int phys = chunk ^ (r & 7);            // 128-byte swizzle of the TMA box
-                w[ci] = *reinterpret_cast<const uint4 *>(st + L::kW + r * 128 + phys * 16);
+                w[ci] = *reinterpret_cast<const uint4 *>(st + r * 128 + phys * 16);
             }
-            if (c == 0) {
-                const int v = (tb + j) * kTileV + r;
-                scale_q[j & 1] = v < p.V ? __half2float(reinterpret_cast<const __half *>(st + L::kS)[r]) : 0.f;
+            if (++d_jj == d_ng) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty(s));
+                cw.next(d_ng);
+                ++d_st;
+                d_jj = 0;
+                d_ng = cw.more() ? cw.size() : 0;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty(s));
-            uint32_t regs[32];
 #pragma unroll
             for (int ci = 0; ci < 4; ++ci) {
                 const uint32_t words[4] = {w[ci].x, w[ci].y, w[ci].z, w[ci].w};
@@ -251,39 +298,88 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
                     regs[8 * ci + 2 * wd + 1] = h2_as_u32(__hsub2(u32_as_h2(p23), bias));
                 }
             }
-            const int slot = i % kASlots;
-            if (i >= kASlots && !warp_wait(aempty(slot), ((i / kASlots) - 1) & 1, ab)) return false;
-            tc_fence_after();
-            tmem_st_32x32b_x32(tmem + lane_base + L::kAcol0 + slot * 64 + 32 * h, regs);
-            tc_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(afull(slot));
             return true;
         };
 
-        auto drain_tile = [&](int j) -> bool {
-            const int buf = j & 1;
-            if (!warp_wait(dfull(buf), (j >> 1) & 1, ab)) return false;
+        uint32_t cur[32], nxt[32];
+        bool ok = nunits > 0 && load_dequant(cur);
+        for (int i = 0; i < nunits && ok; ++i) {
+            const int slot = i % kASlots;
+            if (i >= kASlots && !warp_wait(aempty(slot), ((i / kASlots) - 1) & 1, ab)) break;
             tc_fence_after();
-            uint32_t d[NBLK][8];
-#pragma unroll
-            for (int b = 0; b < NBLK; ++b)
-                tmem_ld_32x32b_x8(tmem + lane_base + L::kDcol0 + buf * 16 * NBLK + 16 * b + 8 * h, d[b]);
-            tc_wait_ld();
+            tmem_st_32x32b_x32(tmem + lane_base + kAcol0 + slot * 64 + 32 * kh, cur);
+            if (i + 1 < nunits) ok = load_dequant(nxt);            // overlaps the store
+            tc_wait_st();
+            tc_keep_alive<32>(cur);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(dempty(buf));
+            if (lane == 0) mbar_arrive(afull(slot));
+#pragma unroll
+            for (int k = 0; k < 32; ++k) cur[k] = nxt[k];
+        }
+    } else if (warp >= kWarpDr0 && warp < kWarpDr0 + kDrWarps) {
+        // ----------------------------------------------------------- drain
+        const int dr = warp - kWarpDr0;
+        const int q = warp & 3;
+        const int r = 32 * q + lane;
+        const uint32_t lane_base = uint32_t(32 * q) << 16;
+        uint32_t drain_syncs = 0;
+        auto drain_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(drain_bar);
+            return warp_wait(drain_bar, (drain_syncs++) & 1, ab);
+        };
+
+        bool ok = true;
+        for (int j = 0; j < ntiles && ok; ++j) {
+            const int buf = j & 1;
             const int t = tb + j;
             const int v = t * kTileV + r;
             const bool valid = v < p.V;
-            const float sc = scale_q[j & 1];
-#pragma unroll
+            const float sc = valid ? __half2float(__ldg(p.scale + v)) : 0.f;
+            if (!warp_wait(dfull(buf), (j >> 1) & 1, ab)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t dset = tmem + lane_base + kDcol0 + buf * L::kDSet;
+#pragma unroll 1
             for (int b = 0; b < NBLK; ++b) {
+                // the block's accumulators, added in a fixed order
+                float g[16];
+                if constexpr (L::kAcc == 4) {
+                    uint32_t d[32];
+                    tmem_ld_32x32b_x32(dset + (b * 4) * 16, d);
+                    tc_wait_ld_keep<32>(d);
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const int m = 16 * b + 8 * h + jj;
-                    const float x = sc * __uint_as_float(d[b][jj]);
+                    for (int jj = 0; jj < 16; ++jj) g[jj] = __uint_as_float(d[jj]) + __uint_as_float(d[16 + jj]);
+                    tmem_ld_32x32b_x32(dset + (b * 4 + 2) * 16, d);
+                    tc_wait_ld_keep<32>(d);
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj)
+                        g[jj] = (g[jj] + __uint_as_float(d[jj])) + __uint_as_float(d[16 + jj]);
+                } else if constexpr (L::kAcc == 2) {
+                    uint32_t d[32];
+                    tmem_ld_32x32b_x32(dset + (b * 2) * 16, d);
+                    tc_wait_ld_keep<32>(d);
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) g[jj] = __uint_as_float(d[jj]) + __uint_as_float(d[16 + jj]);
+                } else {
+                    uint32_t d[16];
+                    tmem_ld_32x32b_x16(dset + b * 16, d);
+                    tc_wait_ld_keep<16>(d);
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) g[jj] = __uint_as_float(d[jj]);
+                }
+                if (b == NBLK - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(dempty(buf));
+                }
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int m = 16 * b + jj;
+                    const float x = sc * g[jj];
                     if (p.logits != nullptr && valid && m < p.M) p.logits[size_t(m) * p.V + v] = x;
                     const uint32_t key = valid ? logit_key(x) : 0u;
                     const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, key);
@@ -295,53 +391,40 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
                     }
                 }
             }
-            return true;
-        };
-
-        bool ok = true;
-        for (int i = 0; i < nunits && ok; ++i) {
-            ok = dequant(i);
-            if (ok && i > 0 && (i % p.n_chunks) == 0) ok = drain_tile(i / p.n_chunks - 1);
         }
-        if (ok && nunits > 0) ok = drain_tile(nunits / p.n_chunks - 1);
 
-        // Publish this CTA's best per row; the last CTA reduces over all CTAs.
-        if (ok) ok = math_sync();
+        // Fold this CTA's best per row into the global keys; the last CTA to
+        // arrive reads and clears them.
+        const int tid = dr * 32 + lane;
+        if (ok) ok = drain_sync();
         if (ok) {
-            const int tid = mw * 32 + lane;
-            if (tid < p.M) __stcg(p.keys + size_t(cta) * kMaxRows + tid, best[tid]);
-            __threadfence();
-            ok = math_sync();
+            if (tid < p.M) atomicMax(p.keys + tid, best[tid]);
+            ok = drain_sync();
         }
         if (ok) {
-            if (mw == 0 && lane == 0) {
-                const uint32_t prev = atomicAdd(p.counter, 1u);
+            if (tid == 0) {
+                const uint32_t prev = atom_add_release_gpu(p.counter, 1u);
                 const bool last = prev == uint32_t(p.P - 1);
-                if (last) atomicExch(p.counter, 0u);
+                if (last) {
+                    fence_acq_rel_gpu();
+                    *p.counter = 0u;
+                }
                 misc[2] = last ? 1u : 0u;
             }
-            ok = math_sync();
+            ok = drain_sync();
         }
-        if (ok && misc[2]) {
-            __threadfence();
-            const int tid = mw * 32 + lane;
-            if (tid < p.M) {
-                unsigned long long k = 0ull;
-                for (int cc = 0; cc < p.P; ++cc) {
-                    const unsigned long long o = __ldcg(p.keys + size_t(cc) * kMaxRows + tid);
-                    k = o > k ? o : k;
-                }
-                p.argmax_out[tid] = static_cast<int32_t>(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFull));
-                if (p.maxlogit != nullptr) p.maxlogit[tid] = key_logit(uint32_t(k >> 32));
-            }
+        if (ok && misc[2] && tid < p.M) {
+            const unsigned long long k = atomicExch(p.keys + tid, 0ull);
+            p.argmax_out[tid] = static_cast<int32_t>(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFull));
+            if (p.maxlogit != nullptr) p.maxlogit[tid] = key_logit(uint32_t(k >> 32));
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 2) {
+    if (warp == kWarpIss0) {
         tc_fence_after();
-        tmem_dealloc(tmem, L::kTmemCols);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -368,7 +451,7 @@ w4v_status launch(const CUtensorMap &xmap, const CUtensorMap &wmap, const Args &
 size_t w8_lmhead_ws_bytes(int M, int V) {
     (void)M;
     (void)V;
-    return size_t(kMaxCtas) * kMaxRows * sizeof(unsigned long long) + 256;
+    return size_t(kMaxRows) * sizeof(unsigned long long) + 256;
 }
 
 w4v_status launch_w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uint16_t *scale,
@@ -386,8 +469,7 @@ w4v_status launch_w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uin
     a.maxlogit = maxlogit;
     a.logits = logits;
     a.keys = static_cast<unsigned long long *>(ws);
-    a.counter = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) +
-                                             size_t(kMaxCtas) * kMaxRows * sizeof(unsigned long long));
+    a.counter = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + size_t(kMaxRows) * sizeof(unsigned long long));
     a.status = info->status;
     a.M = M;
     a.K = K;
@@ -396,11 +478,11 @@ w4v_status launch_w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uin
     a.n_chunks = K / kChunk;
     a.P = std::min(std::min(info->sm_count, kMaxCtas), a.n_tiles);
     CUtensorMap xmap, wmap;
-    st = encode_tmap_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, uint64_t(K), uint64_t(M),
-                        uint64_t(K) * 2, 64, 16 * nblk, CU_TENSOR_MAP_SWIZZLE_128B);
+    st = encode_tmap_kblocks(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, X, uint64_t(K), uint64_t(M), 64, 16 * nblk,
+                             2 * kStageChunks, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != W4V_OK) return st;
-    st = encode_tmap_2d(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, uint64_t(K), uint64_t(V), uint64_t(K),
-                        kChunk, kTileV, CU_TENSOR_MAP_SWIZZLE_128B);
+    st = encode_tmap_kblocks(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, uint64_t(K), uint64_t(V), kChunk, kTileV,
+                             kStageChunks, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != W4V_OK) return st;
     switch (nblk) {
         case 1: return launch<1>(xmap, wmap, a, stream);
