@@ -16,22 +16,21 @@
 //     or bulk copy per ~650 cycles whatever its size, so copies are large:
 //     a stage is up to 4 consecutive groups of one tile, fetched as one 32 KB
 //     bulk copy of packed int4 (the library's tile layout, evict-first) and
-//     one 3-D TMA of the 4 groups' activation slices (128-byte swizzle).
-//     Two producer threads issue them.
+//     one 3-D TMA of the 4 groups' activation slices (128-byte swizzle),
+//     both issued by one producer thread.
 //   * Eight dequant warps (one per TMEM lane quarter and k half) turn
 //     nibbles into exact fp16 (q - z) with LOP3 + HFMA2 and store them into
-//     tensor memory with 32-column tcgen05.st; the store of one unit overlaps
-//     the dequant of the next.  The dequantized operand never touches shared
-//     memory.
+//     tensor memory with 32-column tcgen05.st; two register sets alternate so
+//     the store of one unit overlaps the dequant of the next.  The
+//     dequantized operand never touches shared memory.
 //   * tcgen05.mma (A from TMEM, B = activations from shared memory, D in
-//     TMEM) is issued by four threads in four warps: one thread alone issues
-//     at most one MMA per ~55 cycles, four reach the rate HBM needs.  Each
-//     issuer owns fixed (accumulator, column-block) slices; a group's 8
-//     k-steps go round-robin into 4 accumulators, so the result does not
-//     depend on timing.
-//   * Four drain warps read each group's 4 accumulators (32-column
-//     tcgen05.ld), add them in a fixed order and apply the group scale in
-//     fp32, with the scales prefetched from global memory four groups ahead.
+//     TMEM) is issued by three threads in three warps, unit u by issuer
+//     u % 3: one thread alone issues at most one MMA per ~55 cycles.  A unit
+//     accumulates its 8 k-steps into its own accumulator set, so every
+//     output element is the same chain of MMAs whatever the timing or M.
+//   * Four drain warps read each unit's accumulators (16-column tcgen05.ld)
+//     and apply the group scale in fp32, with the scales prefetched from
+//     global memory four units ahead.
 //   * Work is the flat list of units split evenly over one CTA per SM; a
 //     tile shared by several CTAs is finished by the last one to arrive
 //     (release/acquire counter, no waiting between CTAs), which sums the fp32
@@ -45,15 +44,13 @@ namespace {
 constexpr int kTileN = 128;                       // weight rows per tile (MMA M)
 constexpr int kGroup = 128;                       // k per unit = one quant group
 constexpr int kBlockBytes = kTileN * kGroup / 2;  // packed bytes per unit
-constexpr int kAcc = 4;                           // accumulators per group
-constexpr int kIssuers = 4;
+constexpr int kIssuers = 3;
 constexpr int kDqWarps = 8;
 constexpr int kDrWarps = 4;
-constexpr int kWarpProdW = 0;                     // weights producer
-constexpr int kWarpProdA = 1;                     // activations producer
-constexpr int kWarpIss0 = 2;                      // 2..5 MMA issuers (2 also owns TMEM)
-constexpr int kWarpDr0 = 6;                       // 6..9 drain
-constexpr int kWarpDq0 = 10;                      // 10..17 dequant
+constexpr int kWarpProd = 0;                      // producer
+constexpr int kWarpIss0 = 1;                      // 1..3 MMA issuers (1 also owns TMEM)
+constexpr int kWarpDr0 = 4;                       // 4..7 drain
+constexpr int kWarpDq0 = 8;                       // 8..15 dequant
 constexpr int kWarps = kWarpDq0 + kDqWarps;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kASlots = 4;
@@ -71,8 +68,8 @@ struct Layout {
     static constexpr int kW = kAct;
     static constexpr int kStage = kW + kStageGroups * kBlockBytes;
     static constexpr int kStages = (192 * 1024) / kStage;
-    static constexpr int kDSets = NBLK == 1 ? 4 : 2;    // ring of accumulator sets
-    static constexpr uint32_t kDSet = kAcc * 16 * NBLK; // columns per set, laid out [block][acc][16]
+    static constexpr int kDSets = 8;                    // ring of per-unit accumulator sets
+    static constexpr uint32_t kDSet = 16 * NBLK;        // columns per set
     static constexpr int kBar = kStages * kStage;
     // full, empty per stage; afull, aempty per A slot; dfull, dempty per set; done; drain sync
     static constexpr int kNumBars = 2 * kStages + 2 * kASlots + 2 * kDSets + 2;
@@ -158,15 +155,15 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full(s), 2);
+            mbar_init(full(s), 1);
             mbar_init(empty(s), kDqWarps + kIssuers);
         }
         for (int a = 0; a < kASlots; ++a) {
             mbar_init(afull(a), kDqWarps);
-            mbar_init(aempty(a), kIssuers);
+            mbar_init(aempty(a), 1);
         }
         for (int b = 0; b < L::kDSets; ++b) {
-            mbar_init(dfull(b), kIssuers);
+            mbar_init(dfull(b), 1);
             mbar_init(dempty(b), kDrWarps);
         }
         mbar_init(done_bar, kIssuers);
@@ -183,12 +180,12 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     tc_fence_after();
     const uint32_t tmem = misc[0];
 
-    if (warp == kWarpProdW || warp == kWarpProdA) {
-        // --------------------------------------------------------- producers
+    if (warp == kWarpProd) {
+        // ---------------------------------------------------------- producer
         if (lane == 0) {
-            const bool weights = warp == kWarpProdW;
-            if (!weights) prefetch_tensormap(&xmap);
-            const uint64_t pol = weights ? l2_policy_evict_first() : l2_policy_evict_last();
+            prefetch_tensormap(&xmap);
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_x = l2_policy_evict_last();
             StageWalk sw(ub, p.n_groups, nunits);
             int issued = 0;
             for (int st = 0; sw.left > 0; ++st) {
@@ -196,14 +193,10 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 const int s = st % S;
                 if (st >= S && !mbar_wait(empty(s), ((st / S) - 1) & 1, ab)) break;
                 const uint32_t sa = base_s + s * L::kStage;
-                if (weights) {
-                    mbar_arrive_expect_tx(full(s), ng * kBlockBytes);
-                    bulk_load(sa + L::kW, p.wq + (size_t(sw.t) * p.n_groups + sw.g) * kBlockBytes,
-                              ng * kBlockBytes, full(s), pol);
-                } else {
-                    mbar_arrive_expect_tx(full(s), L::kAct);
-                    tma_load_3d(sa, &xmap, 0, 0, 2 * sw.g, full(s), pol);
-                }
+                mbar_arrive_expect_tx(full(s), ng * kBlockBytes + L::kAct);
+                bulk_load(sa + L::kW, p.wq + (size_t(sw.t) * p.n_groups + sw.g) * kBlockBytes, ng * kBlockBytes,
+                          full(s), pol_w);
+                tma_load_3d(sa, &xmap, 0, 0, 2 * sw.g, full(s), pol_x);
                 ++issued;
                 sw.next(ng);
             }
@@ -220,16 +213,20 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             constexpr uint32_t idesc = idesc_f16_f32(128, 16);
             StageWalk sw(ub, p.n_groups, nunits);
             bool ok = true;
-            int i = 0;
+            int i = 0;                          // first unit of the stage
             for (int st = 0; sw.left > 0 && ok; ++st) {
                 const int ng = sw.size();
                 const int s = st % S;
+                // Every issuer waits for every stage, so its once-per-stage
+                // release below always lands in the phase of this stage.
                 if (!mbar_wait(full(s), (st / S) & 1, ab)) break;
-                for (int jj = 0; jj < ng; ++jj, ++i) {
-                    const int slot = i % kASlots;
-                    const int set = i % L::kDSets;
-                    if (!mbar_wait(afull(slot), (i / kASlots) & 1, ab) ||
-                        (i >= L::kDSets && !mbar_wait(dempty(set), ((i / L::kDSets) - 1) & 1, ab))) {
+                for (int jj = 0; jj < ng; ++jj) {
+                    const int u = i + jj;
+                    if (u % kIssuers != me) continue;
+                    const int slot = u % kASlots;
+                    const int set = u % L::kDSets;
+                    if (!mbar_wait(afull(slot), (u / kASlots) & 1, ab) ||
+                        (u >= L::kDSets && !mbar_wait(dempty(set), ((u / L::kDSets) - 1) & 1, ab))) {
                         ok = false;
                         break;
                     }
@@ -240,17 +237,16 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                     for (int j = 0; j < kGroup / 16; ++j) {
 #pragma unroll
                         for (int b = 0; b < NBLK; ++b) {
-                            const int a = j % kAcc;
-                            if ((a * NBLK + b) % kIssuers != me) continue;
                             const uint32_t baddr = act + (j >> 2) * L::kActBox + b * 2048 + (j & 3) * 32;
-                            mma_f16_ts(dset + (b * kAcc + a) * 16, tmem + kAcol0 + slot * 64 + 8 * j,
-                                       sdesc_sw128(baddr), idesc, j >= kAcc ? 1u : 0u);
+                            mma_f16_ts(dset + 16 * b, tmem + kAcol0 + slot * 64 + 8 * j, sdesc_sw128(baddr), idesc,
+                                       j > 0 ? 1u : 0u);
                         }
                     }
                     mma_commit(aempty(slot));
                     mma_commit(dfull(set));
-                    if (jj == ng - 1) mma_commit(empty(s));
                 }
+                mma_commit(empty(s));
+                i += ng;
                 sw.next(ng);
             }
             // Every MMA of this issuer has finished once this arrives.
@@ -308,21 +304,32 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             return true;
         };
 
-        uint32_t cur[32], nxt[32];
-        bool ok = nunits > 0 && load_dequant(cur);
-        for (int i = 0; i < nunits && ok; ++i) {
+        // Store unit i's registers into its A slot, dequantize the next unit
+        // into the other register set while the store runs, then publish.
+        auto store = [&](int i, const uint32_t (&regs)[32]) -> bool {
             const int slot = i % kASlots;
-            if (i >= kASlots && !warp_wait(aempty(slot), ((i / kASlots) - 1) & 1, ab)) break;
+            if (i >= kASlots && !warp_wait(aempty(slot), ((i / kASlots) - 1) & 1, ab)) return false;
             tc_fence_after();
-            tmem_st_32x32b_x32(tmem + lane_base + kAcol0 + slot * 64 + 32 * kh, cur);
-            if (i + 1 < nunits) ok = load_dequant(nxt);            // overlaps the store
+            tmem_st_32x32b_x32(tmem + lane_base + kAcol0 + slot * 64 + 32 * kh, regs);
+            return true;
+        };
+        auto publish = [&](int i, const uint32_t (&regs)[32]) {
             tc_wait_st();
-            tc_keep_alive<32>(cur);
+            tc_keep_alive<32>(regs);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(afull(slot));
-#pragma unroll
-            for (int k = 0; k < 32; ++k) cur[k] = nxt[k];
+            if (lane == 0) mbar_arrive(afull(i % kASlots));
+        };
+        uint32_t ra[32], rb[32];
+        bool ok = nunits > 0 && load_dequant(ra);
+        for (int i = 0; i < nunits && ok; i += 2) {
+            if (!store(i, ra)) break;
+            if (i + 1 < nunits) ok = load_dequant(rb);
+            publish(i, ra);
+            if (!ok || i + 1 >= nunits) break;
+            if (!store(i + 1, rb)) break;
+            if (i + 2 < nunits) ok = load_dequant(ra);
+            publish(i + 1, rb);
         }
     } else if (warp >= kWarpDr0 && warp < kWarpDr0 + kDrWarps) {
         // ----------------------------------------------------------- drain
@@ -481,28 +488,18 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             for (int k = 0; k + 1 < kScaleAhead; ++k) sp[k] = sp[k + 1];
             sp[kScaleAhead - 1] = load_scale(i + kScaleAhead);
             const uint32_t dset = tmem + lane_base + kDcol0 + set * L::kDSet;
+            uint32_t d[NBLK][16];
 #pragma unroll
-            for (int b = 0; b < NBLK; ++b) {
-                // accumulators 0,1 then 2,3 of block b: ((d0 + d1) + d2) + d3
-                float g[16];
-                uint32_t d[32];
-                tmem_ld_32x32b_x32(dset + (b * kAcc) * 16, d);
-                tc_wait_ld_keep<32>(d);
+            for (int b = 0; b < NBLK; ++b) tmem_ld_32x32b_x16(dset + 16 * b, d[b]);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) g[j] = __uint_as_float(d[j]) + __uint_as_float(d[16 + j]);
-                tmem_ld_32x32b_x32(dset + (b * kAcc + 2) * 16, d);
-                tc_wait_ld_keep<32>(d);
-                if (b == NBLK - 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(dempty(set));
-                }
+            for (int b = 0; b < NBLK; ++b) tc_wait_ld_keep<16>(d[b]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dempty(set));
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    g[j] = (g[j] + __uint_as_float(d[j])) + __uint_as_float(d[16 + j]);
-                    acc[b][j] = fmaf(sc, g[j], acc[b][j]);
-                }
-            }
+            for (int b = 0; b < NBLK; ++b)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[b][j] = fmaf(sc, __uint_as_float(d[b][j]), acc[b][j]);
             const int t = wd.t;
             const bool tile_end = wd.g == p.n_groups - 1;
             wd.next();

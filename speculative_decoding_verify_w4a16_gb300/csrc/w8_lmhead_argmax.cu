@@ -14,15 +14,16 @@
 //   * An SM completes about one TMA copy per ~650 cycles whatever its size,
 //     so a stage is two k-chunks of a tile: one 3-D TMA of 32 KB of int8
 //     weights (128-byte swizzle, straight from the row-major [V][K] matrix)
-//     and one 3-D TMA of the matching activation slices; two producer
-//     threads issue them.
+//     and one 3-D TMA of the matching activation slices, both issued by one
+//     producer thread.
 //   * Eight dequant warps widen int8 to exact fp16 (XOR 0x80, PRMT into the
 //     mantissa of 1024, subtract 1152) and store it into tensor memory with
-//     32-column stores; the store of one unit overlaps the dequant of the
-//     next.
-//   * Four issuer threads (one MMA per ~55 cycles each) run tcgen05.mma with
+//     32-column stores; two register sets alternate so the store of one unit
+//     overlaps the dequant of the next.
+//   * Three issuer threads (one MMA per ~55 cycles each) run tcgen05.mma with
 //     A from TMEM, accumulating the whole K of a tile in TMEM; the k-steps go
-//     round-robin into independent accumulators, each owned by one issuer.
+//     round-robin into independent accumulators, each (accumulator, column
+//     block) slice owned by one issuer, so the order of every sum is fixed.
 //   * Four drain warps finish a tile: add the accumulators in a fixed order,
 //     scale, turn each logit into an order-preserving 32-bit key, and a warp
 //     max-reduction plus a min-reduction over the winning lanes gives the
@@ -41,14 +42,13 @@ constexpr int kTileV = 128;
 constexpr int kChunk = 128;                 // k per unit (bytes of int8)
 constexpr int kWBytes = kTileV * kChunk;    // 16 KB per unit
 constexpr int kMaxRows = 128;
-constexpr int kIssuers = 4;
+constexpr int kIssuers = 3;
 constexpr int kDqWarps = 8;
 constexpr int kDrWarps = 4;
-constexpr int kWarpProdW = 0;
-constexpr int kWarpProdA = 1;
-constexpr int kWarpIss0 = 2;                // 2..5 (2 also owns TMEM)
-constexpr int kWarpDr0 = 6;                 // 6..9
-constexpr int kWarpDq0 = 10;                // 10..17
+constexpr int kWarpProd = 0;
+constexpr int kWarpIss0 = 1;                // 1..3 (1 also owns TMEM)
+constexpr int kWarpDr0 = 4;                 // 4..7
+constexpr int kWarpDq0 = 8;                 // 8..15
 constexpr int kWarps = kWarpDq0 + kDqWarps;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kASlots = 4;
@@ -67,7 +67,7 @@ struct Layout {
     static constexpr int kStages = (196 * 1024) / kStage > 6 ? 6 : (196 * 1024) / kStage;
     // Independent accumulators per tile: the same count for every M <= 32,
     // so the per-logit arithmetic does not depend on M there.
-    static constexpr int kAcc = NBLK <= 2 ? 4 : 8 / NBLK;
+    static constexpr int kAcc = NBLK <= 2 ? 3 : 8 / NBLK;
     static constexpr uint32_t kDSet = kAcc * 16 * NBLK;  // laid out [block][acc][16]
     static constexpr int kBar = kStages * kStage;
     static constexpr int kNumBars = 2 * kStages + 2 * kASlots + 4 + 2;
@@ -155,7 +155,7 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full(s), 2);
+            mbar_init(full(s), 1);
             mbar_init(empty(s), kDqWarps + kIssuers);
         }
         for (int a = 0; a < kASlots; ++a) {
@@ -182,12 +182,13 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
     tc_fence_after();
     const uint32_t tmem = misc[0];
 
-    if (warp == kWarpProdW || warp == kWarpProdA) {
-        // --------------------------------------------------------- producers
+    if (warp == kWarpProd) {
+        // ---------------------------------------------------------- producer
         if (lane == 0) {
-            const bool weights = warp == kWarpProdW;
-            prefetch_tensormap(weights ? &wmap : &xmap);
-            const uint64_t pol = weights ? l2_policy_evict_first() : l2_policy_evict_last();
+            prefetch_tensormap(&wmap);
+            prefetch_tensormap(&xmap);
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_x = l2_policy_evict_last();
             int issued = 0;
             ChunkWalk cw(p.n_chunks, ntiles);
             for (int st = 0; cw.more(); ++st) {
@@ -195,13 +196,9 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
                 const int s = st % S;
                 if (st >= S && !mbar_wait(empty(s), ((st / S) - 1) & 1, ab)) break;
                 const uint32_t sa = base_s + s * L::kStage;
-                if (weights) {
-                    mbar_arrive_expect_tx(full(s), kStageChunks * kWBytes);
-                    tma_load_3d(sa + L::kW, &wmap, 0, (tb + cw.j) * kTileV, cw.c, full(s), pol);
-                } else {
-                    mbar_arrive_expect_tx(full(s), L::kAct);
-                    tma_load_3d(sa, &xmap, 0, 0, 2 * cw.c, full(s), pol);
-                }
+                mbar_arrive_expect_tx(full(s), kStageChunks * kWBytes + L::kAct);
+                tma_load_3d(sa + L::kW, &wmap, 0, (tb + cw.j) * kTileV, cw.c, full(s), pol_w);
+                tma_load_3d(sa, &xmap, 0, 0, 2 * cw.c, full(s), pol_x);
                 ++issued;
                 cw.next(ng);
             }
@@ -301,21 +298,30 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
             return true;
         };
 
-        uint32_t cur[32], nxt[32];
-        bool ok = nunits > 0 && load_dequant(cur);
-        for (int i = 0; i < nunits && ok; ++i) {
+        auto store = [&](int i, const uint32_t (&regs)[32]) -> bool {
             const int slot = i % kASlots;
-            if (i >= kASlots && !warp_wait(aempty(slot), ((i / kASlots) - 1) & 1, ab)) break;
+            if (i >= kASlots && !warp_wait(aempty(slot), ((i / kASlots) - 1) & 1, ab)) return false;
             tc_fence_after();
-            tmem_st_32x32b_x32(tmem + lane_base + kAcol0 + slot * 64 + 32 * kh, cur);
-            if (i + 1 < nunits) ok = load_dequant(nxt);            // overlaps the store
+            tmem_st_32x32b_x32(tmem + lane_base + kAcol0 + slot * 64 + 32 * kh, regs);
+            return true;
+        };
+        auto publish = [&](int i, const uint32_t (&regs)[32]) {
             tc_wait_st();
-            tc_keep_alive<32>(cur);
+            tc_keep_alive<32>(regs);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(afull(slot));
-#pragma unroll
-            for (int k = 0; k < 32; ++k) cur[k] = nxt[k];
+            if (lane == 0) mbar_arrive(afull(i % kASlots));
+        };
+        uint32_t ra[32], rb[32];
+        bool ok = nunits > 0 && load_dequant(ra);
+        for (int i = 0; i < nunits && ok; i += 2) {
+            if (!store(i, ra)) break;
+            if (i + 1 < nunits) ok = load_dequant(rb);
+            publish(i, ra);
+            if (!ok || i + 1 >= nunits) break;
+            if (!store(i + 1, rb)) break;
+            if (i + 2 < nunits) ok = load_dequant(ra);
+            publish(i + 1, rb);
         }
     } else if (warp >= kWarpDr0 && warp < kWarpDr0 + kDrWarps) {
         // ----------------------------------------------------------- drain
@@ -347,17 +353,15 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
             for (int b = 0; b < NBLK; ++b) {
                 // the block's accumulators, added in a fixed order
                 float g[16];
-                if constexpr (L::kAcc == 4) {
-                    uint32_t d[32];
-                    tmem_ld_32x32b_x32(dset + (b * 4) * 16, d);
-                    tc_wait_ld_keep<32>(d);
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) g[jj] = __uint_as_float(d[jj]) + __uint_as_float(d[16 + jj]);
-                    tmem_ld_32x32b_x32(dset + (b * 4 + 2) * 16, d);
-                    tc_wait_ld_keep<32>(d);
+                if constexpr (L::kAcc == 3) {
+                    uint32_t d01[32], d2[16];
+                    tmem_ld_32x32b_x32(dset + (b * 3) * 16, d01);
+                    tmem_ld_32x32b_x16(dset + (b * 3 + 2) * 16, d2);
+                    tc_wait_ld_keep<32>(d01);
+                    tc_wait_ld_keep<16>(d2);
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj)
-                        g[jj] = (g[jj] + __uint_as_float(d[jj])) + __uint_as_float(d[16 + jj]);
+                        g[jj] = (__uint_as_float(d01[jj]) + __uint_as_float(d01[16 + jj])) + __uint_as_float(d2[jj]);
                 } else if constexpr (L::kAcc == 2) {
                     uint32_t d[32];
                     tmem_ld_32x32b_x32(dset + (b * 2) * 16, d);
