@@ -132,6 +132,32 @@ w4v_status w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uint16_t *
                             float *logits_debug, void *workspace, size_t workspace_bytes,
                             w4v_stream_t stream);
 
+/* ---------------------------------------------- w8_lmhead_argmax_noalloc
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory for a workspace -- for example a plugin
+ * running inside another inference engine whose execute step may not
+ * allocate, or a serving loop whose device memory is already handed out by
+ * its own allocator (cudaMalloc would also synchronize the device in the
+ * middle of a decode step).  It computes exactly what w8_lmhead_argmax
+ * computes, with the same arguments minus the workspace: the scratch lives
+ * in a 4 KB device array inside this library, which every GPU that loads the
+ * library keeps until the process exits.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *     call.  It clears the scratch with an asynchronous memset on `stream`
+ *     before each launch.
+ *   - The first call on a device looks up that device's address of the
+ *     array (cudaGetSymbolAddress with the device current); make that first
+ *     call outside any stream capture.
+ *   - Every call on a device shares the one array: calls that overlap on the
+ *     GPU (different streams without ordering between them) race and give
+ *     wrong tokens.  Serialize them, or use w8_lmhead_argmax with a
+ *     workspace per stream.
+ *   - Sizes: 0 <= M <= 128 (the array holds the keys of at most 128 rows);
+ *     larger M returns W4V_ERR_SHAPE.  Other sizes as w8_lmhead_argmax. */
+w4v_status w8_lmhead_argmax_noalloc(const uint16_t *X, const int8_t *W, const uint16_t *scale,
+                                    int M, int K, int V, int32_t *argmax_out, float *maxlogit,
+                                    float *logits_debug, w4v_stream_t stream);
+
 /* ----------------------------------------------------------- spec_accept
  * Longest-prefix greedy acceptance for B sequences:
  *   n[b] = the largest j <= K with draft[b][i] == target[b][i] for all i < j,
