@@ -94,18 +94,21 @@ w4v_status w4v_unpack_int4(const void *packed_host, int N, int K, uint8_t *q_hos
  * C[M][N] = A[M][K] * W^T, W[n][k] = scales[k/G][n] * (q[n][k] - z[k/G][n]),
  * z = 8 when zeros == NULL (symmetric GPTQ) else the uint8 table
  * zeros[K/G][N] (values 0..15, AWQ style).  A, scales, C are fp16; products
- * are accumulated in fp32 per group, each group's sum is multiplied by its
- * scale in fp32, and C is rounded to fp16 (round to nearest even).  The
- * per-element arithmetic does not depend on M for M <= 32.
+ * are accumulated in fp32.  For M <= 32 (verify sizes, HBM-bound) each
+ * group's fp32 sum is multiplied by its scale in fp32, and the per-element
+ * arithmetic does not depend on M; for M > 32 (prefill, tensor-bound) the
+ * dequantized weight s*(q-z) is rounded to fp16 once and the whole K is
+ * accumulated in fp32.  C is rounded to fp16 (round to nearest even).
  *   A        device, fp16 [M][K]
  *   Bq       device, packed int4 from w4v_pack_int4 (w4v_packed_bytes(N,K))
  *   scales   device, fp16 [K/G][N]
  *   zeros    device, uint8 [K/G][N] or NULL (requires N % 16 == 0)
  *   group    must be 128
  *   C        device, fp16 [M][N] (written, never read)
- * Sizes: 0 <= M <= 32 (M == 0 is a no-op), N % 8 == 0, K % 128 == 0.
+ * Sizes: M >= 0 (M == 0 is a no-op), N % 8 == 0, K % 128 == 0.
  * Workspace: w4a16_workspace_bytes(M, N, K) bytes, zero-filled before first
- * use (split-K partial sums and per-tile arrival counters). */
+ * use (split-K partial sums and per-tile arrival counters; M > 32 uses
+ * none and may pass NULL). */
 size_t w4a16_workspace_bytes(int M, int N, int K);
 w4v_status w4a16_gemm(const uint16_t *A, const void *Bq, const uint16_t *scales,
                       const uint8_t *zeros, int group, uint16_t *C, int M, int N, int K,
@@ -125,7 +128,7 @@ w4v_status w4a16_gemm(const uint16_t *A, const void *Bq, const uint16_t *scales,
  *   logits_debug   device, float [M][V] or NULL: every logit (testing aid)
  * Sizes: 0 <= M <= 128, K % 128 == 0, V % 8 == 0, V > 0.
  * Workspace: w8_lmhead_argmax_workspace_bytes(M, V) bytes, zero-filled
- * before first use (per-CTA best keys and an arrival counter). */
+ * before first use (one best key per row and an arrival counter). */
 size_t w8_lmhead_argmax_workspace_bytes(int M, int V);
 w4v_status w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uint16_t *scale,
                             int M, int K, int V, int32_t *argmax_out, float *maxlogit,

@@ -90,22 +90,24 @@ w4v_status w4v_unpack_int4(const void *packed, int N, int K, uint8_t *q) {
 }
 
 size_t w4a16_workspace_bytes(int M, int N, int K) {
-    if (M < 0 || M > 32 || !pack_shape_ok(N, K)) return 0;
+    if (M < 0 || !pack_shape_ok(N, K)) return 0;
+    if (M > w4v::kDecodeMaxRows) return 256;     // the prefill kernel needs no workspace
     return w4v::w4a16_decode_ws_bytes(M, N, K);
 }
 
-w4v_status w4a16_gemm(const uint16_t *A, const void *Bq, const uint16_t *scales, const uint8_t *zeros,
-                      int group, uint16_t *C, int M, int N, int K, void *ws, size_t ws_bytes,
-                      w4v_stream_t stream) {
+w4v_status w4a16_gemm(const uint16_t *A, const void *Bq, const uint16_t *scales, const uint8_t *zeros, int group,
+                      uint16_t *C, int M, int N, int K, void *ws, size_t ws_bytes, w4v_stream_t stream) {
     if (M < 0 || N <= 0 || K <= 0) return W4V_ERR_SHAPE;
     if (group != kGroup) return W4V_ERR_SHAPE;
-    if (K % kGroup != 0 || N % 8 != 0 || M > 32) return W4V_ERR_SHAPE;
+    if (K % kGroup != 0 || N % 8 != 0) return W4V_ERR_SHAPE;
     if (zeros != nullptr && N % 16 != 0) return W4V_ERR_SHAPE;
     if (M == 0) return W4V_OK;
     if (A == nullptr || Bq == nullptr || scales == nullptr || C == nullptr) return W4V_ERR_ARG;
     if (!w4v::aligned16(A) || !w4v::aligned16(Bq) || !w4v::aligned16(scales) ||
         (zeros != nullptr && !w4v::aligned16(zeros)))
         return W4V_ERR_ALIGN;
+    if (M > w4v::kDecodeMaxRows)
+        return w4v::launch_w4a16_prefill(A, Bq, scales, zeros, C, M, N, K, reinterpret_cast<cudaStream_t>(stream));
     if (ws == nullptr || ws_bytes < w4v::w4a16_decode_ws_bytes(M, N, K)) return W4V_ERR_WORKSPACE;
     if (!w4v::aligned16(ws)) return W4V_ERR_ALIGN;
     return w4v::launch_w4a16_decode(A, Bq, scales, zeros, C, M, N, K, ws,

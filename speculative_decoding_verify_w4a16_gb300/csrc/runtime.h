@@ -57,6 +57,10 @@ w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t
                                const uint8_t *zeros, uint16_t *C, int M, int N, int K,
                                void *ws, cudaStream_t stream);
 size_t w4a16_decode_ws_bytes(int M, int N, int K);
+w4v_status launch_w4a16_prefill(const uint16_t *A, const void *Bq, const uint16_t *scales, const uint8_t *zeros,
+                                uint16_t *C, int M, int N, int K, cudaStream_t stream);
+// Rows up to which the verify-sized (HBM-bound) kernel is used.
+constexpr int kDecodeMaxRows = 32;
 
 w4v_status launch_w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uint16_t *scale,
                                    int M, int K, int V, int32_t *argmax_out, float *maxlogit,

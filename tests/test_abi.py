@@ -67,7 +67,8 @@ def test_pack_pads_tail_rows_with_zero_point(w4v_mod):
 
 def test_workspace_sizes(w4v_mod):
     assert w4v_mod.w4a16_workspace_bytes(16, 7680, 2560) > 0
-    assert w4v_mod.w4a16_workspace_bytes(33, 512, 256) == 0
+    assert w4v_mod.w4a16_workspace_bytes(33, 512, 256) == 256       # prefill path: no workspace
+    assert w4v_mod.w4a16_workspace_bytes(-1, 512, 256) == 0
     assert w4v_mod.w4a16_workspace_bytes(16, 100, 256) == 0       # N % 8 != 0
     assert w4v_mod.w8_lmhead_argmax_workspace_bytes(128, 151936) > 0
     assert w4v_mod.w8_lmhead_argmax_workspace_bytes(129, 151936) == 0
@@ -79,7 +80,7 @@ def test_argument_validation_before_launch(w4v_mod):
     ws_small = 16
     # w4a16_gemm
     assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 64, FAKE, 16, 512, 256, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
-    assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, 33, 512, 256, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, -1, 512, 256, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
     assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 500, 256, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
     assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 512, 200, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
     assert lib.w4a16_gemm(FAKE, FAKE, FAKE, FAKE, 128, FAKE, 16, 520, 256, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE

@@ -109,3 +109,42 @@ def test_layer_projection_sampled(w4v_mod, gpu, oracle_mod, proj):
     cols = np.concatenate([cols, np.arange(proj.N, dtype=np.int32), np.arange(proj.N, dtype=np.int32)])
     R = oracle_mod.w4a16_gemm_sampled(A, q, s, rows, cols)
     assert gemm_rel_err(C[rows, cols], R) <= GEMM_TOL
+
+
+# ---------------------------------------------------------------- prefill (M > 32)
+@pytest.mark.parametrize("M,N,K", [(33, 512, 256), (64, 128, 128), (128, 2560, 2560), (200, 520, 640),
+                                   (256, 1024, 1280), (300, 384, 9728)])
+def test_prefill_shapes(w4v_mod, gpu, oracle_mod, M, N, K):
+    A = inputs.activations(M, M, K, "prefill")
+    q = inputs.w4_codes(M, N, K, "prefill")
+    s = inputs.w4_scales(M, N, K, "prefill")
+    C = _gpu_gemm(w4v_mod, gpu, A, q, s)
+    assert gemm_rel_err(C, oracle_mod.w4a16_gemm(A, q, s)) <= GEMM_TOL
+
+
+def test_prefill_zero_points(w4v_mod, gpu, oracle_mod):
+    M, N, K = 96, 256, 512
+    A = inputs.activations(8, M, K)
+    q = inputs.w4_codes(8, N, K)
+    s = inputs.w4_scales(8, N, K)
+    z = inputs.w4_zeros(8, N, K)
+    C = _gpu_gemm(w4v_mod, gpu, A, q, s, zeros=z)
+    assert gemm_rel_err(C, oracle_mod.w4a16_gemm(A, q, s, zeros=z)) <= GEMM_TOL
+
+
+@pytest.mark.parametrize("M", [2048, 8192])
+@pytest.mark.parametrize("proj", inputs.LAYER_PROJS, ids=lambda p: p.name)
+def test_prefill_layer_projection_sampled(w4v_mod, gpu, oracle_mod, proj, M):
+    """The 4B-shaped projections at prefill sizes (2048 and 8192 rows): 3000
+    sampled outputs plus one full output row and one full column."""
+    A = inputs.activations(2, M, proj.K, 0, proj.name, "prefill")
+    q, s = inputs.layer_weights(2, 0, proj)
+    C = _gpu_gemm(w4v_mod, gpu, A, q, s)
+    r = np.random.default_rng(M)
+    rows = r.integers(0, M, 3000).astype(np.int32)
+    cols = r.integers(0, proj.N, 3000).astype(np.int32)
+    rows = np.concatenate([rows, np.full(proj.N, M - 1, np.int32), np.arange(0, M, max(1, M // 256), dtype=np.int32)])
+    cols = np.concatenate([cols, np.arange(proj.N, dtype=np.int32),
+                           np.full(len(range(0, M, max(1, M // 256))), proj.N - 1, np.int32)])
+    R = oracle_mod.w4a16_gemm_sampled(A, q, s, rows, cols)
+    assert gemm_rel_err(C[rows, cols], R) <= GEMM_TOL
