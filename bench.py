@@ -259,6 +259,10 @@ def run_gpu(args, rank, world):
     if args.sweep:
         result["sweep"] = stack.sweep(peaks)
     del stack
+    torch.cuda.empty_cache()
+    if args.prefill:
+        result["prefill"] = run_prefill(dev, w4v, torch, peaks)
+        result["lmhead_batched"] = run_lmhead_batched(dev, w4v, torch, peaks)
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(step)
     return result
@@ -384,6 +388,70 @@ class Stack:
         return out
 
 
+def run_prefill(dev, w4v, torch, peaks):
+    """The layer set at prefill sizes (M = 2048 and 8192): tensor-bound."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(SEED + 7)
+    out = {}
+    for M in (8192, 2048):
+        projs = []
+        for p in inputs.LAYER_PROJS:
+            packed = torch.randint(0, 256, (w4v.packed_bytes(p.N, p.K),), generator=g, device=dev, dtype=torch.uint8)
+            sc = (torch.rand(((p.K // 128), p.N), generator=g, device=dev) * 0.015 + 0.005).half()
+            A = torch.randn((M, p.K), generator=g, device=dev).half()
+            C = torch.empty((M, p.N), device=dev, dtype=torch.float16)
+            projs.append((p, packed, sc, A, C))
+
+        def run():
+            for (p, packed, sc, A, C) in projs:
+                w4v.w4a16_gemm(A, packed, sc, p.N, out=C)
+
+        per = {}
+        for (p, packed, sc, A, C) in projs:
+            ms = time_graph(torch, lambda p=p, packed=packed, sc=sc, A=A, C=C: w4v.w4a16_gemm(A, packed, sc, p.N, out=C))
+            per[p.name] = round(2.0 * M * p.N * p.K / (ms * 1e-3) / 1e12, 1)
+        ms = time_graph(torch, run)
+        flop = sum(2.0 * M * p.N * p.K for p in inputs.LAYER_PROJS)
+        tf = flop / (ms * 1e-3) / 1e12
+        out["M=%d" % M] = {"bound": "tensor", "ms": round(ms, 4), "achieved": round(tf, 1), "unit": "TFLOP/s",
+                           "peak": peaks["bf16_tflops"], "frac": round(tf / peaks["bf16_tflops"], 4),
+                           "peak_source": peaks["source"] + " (dense bf16 = fp16 rate, burst)",
+                           "per_projection_TFLOP/s": per}
+        del projs
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_lmhead_batched(dev, w4v, torch, peaks):
+    """Batched verify of 8 sequences x 16 positions (M = 128) through the int8
+    lm_head with per-sequence acceptance, and the prefill's last-row lm_head."""
+    H, V = inputs.H_4B, inputs.V_4B
+    W8, s8 = inputs.lmhead_weights(SEED, V, H, "bench")
+    Wd = torch.from_numpy(W8).to(dev)
+    sd = torch.from_numpy(s8).to(dev)
+    out = {}
+    for (B, K1) in ((8, 16), (1, 1)):
+        M = B * K1
+        X = torch.from_numpy(inputs.activations(SEED, M, H, "lmb")).to(dev)
+        tok = torch.empty(M, dtype=torch.int32, device=dev)
+        ws = w4v.workspace(w4v.w8_lmhead_argmax_workspace_bytes(M, V), dev)
+        d = torch.from_numpy(inputs.rng(SEED, "lmb-d").integers(0, V, size=(B, K1 - 1)).astype(np.int32)).to(dev)
+        n = torch.empty(B, dtype=torch.int32, device=dev)
+        o = torch.empty((B, K1), dtype=torch.int32, device=dev)
+
+        def step():
+            w4v.w8_lmhead_argmax(X, Wd, sd, out=tok, ws=ws)
+            w4v.spec_accept(tok.view(B, K1), d, n_out=n, tok_out=o)
+
+        ms = time_graph(torch, lambda: [step() for _ in range(10)]) / 10
+        b = V * H + 2 * V + 2 * M * H
+        gbs = b / (ms * 1e-3) / 1e9
+        out["M=%d" % M] = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                           "TFLOP/s": round(2.0 * M * V * H / (ms * 1e-3) / 1e12, 1),
+                           "workload": "%d sequences x %d positions + acceptance" % (B, K1)}
+    return out
+
+
 # --------------------------------------------------------------------- CPU arm
 def _cores():
     try:
@@ -470,6 +538,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-prefill", dest="prefill", action="store_false")
+    ap.add_argument("--prefill-only", action="store_true", help="run only the prefill leg (profiling aid)")
     ap.add_argument("--ref-frac", type=float, default=1.0 / 16)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -484,6 +554,15 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
+    if args.prefill_only:
+        import torch
+        from speculative_decoding_verify_w4a16_gb300 import _build, w4v
+        _build.build()
+        w4v.load()
+        w4v.init()
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+        print(json.dumps({"prefill": run_prefill(dev, w4v, torch, load_peaks())}), flush=True)
+        return
     res = run_gpu(args, rank, world)
     if rank == 0:
         print(json.dumps(res), flush=True)
