@@ -40,6 +40,25 @@ w4v_status encode_tmap_kblocks(CUtensorMap *map, CUtensorMapDataType dtype, uint
                                uint64_t inner, uint64_t rows, uint32_t inner_box, uint32_t box_rows,
                                uint32_t box_blocks, CUtensorMapSwizzle swizzle);
 
+// Launches `kernel` with programmatic stream serialization, so its grid can
+// be scheduled while the previous kernel of the stream drains; the kernel
+// itself orders its memory accesses after that kernel (grid_dep_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Stream-K style even split of `units` over `ctas`: CTA c owns

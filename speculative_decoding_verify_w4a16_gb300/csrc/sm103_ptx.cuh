@@ -150,6 +150,47 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Warms L2 with `bytes` (multiple of 16) of global memory from a 16-byte
+// aligned address; nothing lands in shared memory.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Warms L2 with the box of a 3-D tiled tensor copy (same coordinates as
+// tma_load_3d); nothing lands in shared memory.
+__device__ __forceinline__ void prefetch_l2_3d(const CUtensorMap *map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+// Per-thread asynchronous global -> shared copy of `bytes` (4, 8 or 16)
+// bytes; the last bytes - src_bytes bytes are zero-filled (src_bytes = 0
+// reads nothing).  Completion is tracked by commit groups of the issuing
+// thread.
+template <int bytes>
+__device__ __forceinline__ void cp_async(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(dst), "l"(src), "n"(bytes), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Waits until at most n of this thread's most recent commit groups are pending.
+template <int n>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
+}
+
+// ------------------------------------------------ programmatic dependent launch
+// Kernels are launched with programmatic stream serialization: a kernel may
+// start while the previous kernel of the stream is finishing, and must not
+// read or write global memory that kernel can touch before grid_dep_wait()
+// returns (it returns once the previous grid has completed and its writes
+// are visible).  grid_dep_launch() lets the next kernel of the stream be
+// scheduled; it has no effect on the memory order.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -296,6 +337,14 @@ __device__ __forceinline__ void tc_wait_ld_keep(uint32_t (&r)[n]) {
 __device__ __forceinline__ uint32_t atom_add_release_gpu(uint32_t *p, uint32_t v) {
     uint32_t old;
     asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Increment with both release (publishes this CTA's earlier writes) and
+// acquire (the caller then sees every write published by earlier releases).
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
 

@@ -6,6 +6,7 @@
 // lane compares one position, a warp ballot marks the mismatches and the
 // first set bit is the accepted length.
 #include "runtime.h"
+#include "sm103_ptx.cuh"
 
 namespace w4v {
 namespace {
@@ -15,6 +16,8 @@ constexpr int kWarps = 8;
 __global__ void __launch_bounds__(32 * kWarps)
 spec_accept_kernel(const int32_t *__restrict__ target, const int32_t *__restrict__ draft, int B, int K,
                    int32_t *__restrict__ n_out, int32_t *__restrict__ tok_out) {
+    grid_dep_wait();       // target tokens come from the previous kernel
+    grid_dep_launch();
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (b >= B) return;
@@ -49,8 +52,12 @@ w4v_status launch_spec_accept(const int32_t *target, const int32_t *draft, int B
     w4v_status st = device_info(&info);
     if (st != W4V_OK) return st;
     const int grid = (B + kWarps - 1) / kWarps;
-    spec_accept_kernel<<<grid, 32 * kWarps, 0, stream>>>(target, draft, B, K, n_accepted, out_tokens);
-    return cudaGetLastError() == cudaSuccess ? W4V_OK : W4V_ERR_CUDA;
+    if (launch_pdl(spec_accept_kernel, dim3(grid), dim3(32 * kWarps), 0, stream, target, draft, B, K, n_accepted,
+                   out_tokens) != cudaSuccess) {
+        cudaGetLastError();
+        return W4V_ERR_CUDA;
+    }
+    return W4V_OK;
 }
 
 }  // namespace w4v

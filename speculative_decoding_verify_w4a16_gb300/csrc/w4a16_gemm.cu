@@ -12,71 +12,93 @@
 //     M side, the (<= 32) activation rows its N side in blocks of 16, so
 //     every output element comes from the same instruction shape whatever M
 //     is (batch invariance for M <= 32).
-//   * Units are (128-row tile, 128-k group).  An SM completes about one TMA
-//     or bulk copy per ~650 cycles whatever its size, so copies are large:
-//     a stage is up to 4 consecutive groups of one tile, fetched as one 32 KB
-//     bulk copy of packed int4 (the library's tile layout, evict-first) and
-//     one 3-D TMA of the 4 groups' activation slices (128-byte swizzle),
-//     both issued by one producer thread.
-//   * Eight dequant warps (one per TMEM lane quarter and k half) turn
-//     nibbles into exact fp16 (q - z) with LOP3 + HFMA2 and store them into
-//     tensor memory with 32-column tcgen05.st; two register sets alternate so
-//     the store of one unit overlaps the dequant of the next.  The
-//     dequantized operand never touches shared memory.
+//   * A unit is a 128-row tile times two quantization groups (256 k).  Every
+//     hand-off between roles costs a few hundred cycles of latency whatever
+//     it carries, so units are made as large as tensor memory allows: three
+//     A slots of 128 columns plus the accumulators fill the 512 columns.
+//   * An SM completes about one TMA or bulk copy per ~650 cycles whatever its
+//     size, so a stage is two units (four groups) of one tile: one 32 KB bulk
+//     copy of packed int4 (the library's tile layout, evict-first) and one
+//     3-D TMA of the four groups' activation slices (128-byte swizzle), both
+//     issued by one producer thread.
+//   * Eight dequant warps turn nibbles into exact fp16 (q - z) with LOP3 +
+//     HFMA2 and store them into tensor memory with 32-column tcgen05.st.
+//     Warp (quarter, parity) owns its 32 tile rows of every other unit and
+//     does that unit's whole k in four 64-k steps, alternating two register
+//     sets so each store overlaps the next step's arithmetic; the two warps
+//     sharing a scheduler work on different units and so fall naturally out
+//     of phase.  The dequantized operand never touches shared memory.
 //   * tcgen05.mma (A from TMEM, B = activations from shared memory, D in
-//     TMEM) is issued by three threads in three warps, unit u by issuer
-//     u % 3: one thread alone issues at most one MMA per ~55 cycles.  A unit
-//     accumulates its 8 k-steps into its own accumulator set, so every
-//     output element is the same chain of MMAs whatever the timing or M.
-//   * Four drain warps read each unit's accumulators (16-column tcgen05.ld)
-//     and apply the group scale in fp32, with the scales prefetched from
-//     global memory four units ahead.
+//     TMEM) is issued by three threads in three warps; one thread alone
+//     issues at most one MMA per ~90 cycles, so the two groups of a unit go
+//     to two different issuers (group g of unit f to issuer (2f + g) % 3) and
+//     run side by side.  Each group accumulates its 8 k-steps into its own
+//     accumulator block, so every output element is the same chain of MMAs
+//     whatever the timing or M.
+//   * Four drain warps read a unit's accumulators (one tcgen05.ld for both
+//     groups) and apply the group scales in fp32, groups in ascending order.
+//     Scales (and zero points) are tiny but each group needs a fresh row of
+//     them, and a global load takes over a microsecond when HBM is busy:
+//     each warp keeps the next 16 groups' values in flight with cp.async
+//     into a shared-memory ring.
 //   * Work is the flat list of units split evenly over one CTA per SM; a
 //     tile shared by several CTAs is finished by the last one to arrive
-//     (release/acquire counter, no waiting between CTAs), which sums the fp32
-//     partial tiles in CTA order, so the result is deterministic.
+//     (acquire-release counter, no waiting between CTAs), which sums the fp32
+//     partial tiles in CTA order, so the result is deterministic.  All 512
+//     threads of that CTA share the sum, each loading every contributor's
+//     float4 at once: on this two-die part an L2 round trip can take well
+//     over a microsecond, so the fix-up is one round of loads, not several.
+//   * The kernel is launched with programmatic stream serialization: barrier
+//     set-up, tensor-memory allocation and an L2 prefetch of the first
+//     weight stages overlap the end of the previous kernel in the stream.
 #include "runtime.h"
 #include "sm103_ptx.cuh"
 
 namespace w4v {
 namespace {
 
-constexpr int kTileN = 128;                       // weight rows per tile (MMA M)
-constexpr int kGroup = 128;                       // k per unit = one quant group
-constexpr int kBlockBytes = kTileN * kGroup / 2;  // packed bytes per unit
+constexpr int kTileN = 128;                        // weight rows per tile (MMA M)
+constexpr int kGroup = 128;                        // k per quantization group
+constexpr int kGroupBytes = kTileN * kGroup / 2;   // packed bytes per (tile, group)
+constexpr int kUnitGroups = 2;                     // groups per unit
+constexpr int kStageUnits = 2;                     // units per stage
+constexpr int kStageGroups = kUnitGroups * kStageUnits;
 constexpr int kIssuers = 3;
 constexpr int kDqWarps = 8;
 constexpr int kDrWarps = 4;
-constexpr int kWarpProd = 0;                      // producer
-constexpr int kWarpIss0 = 1;                      // 1..3 MMA issuers (1 also owns TMEM)
-constexpr int kWarpDr0 = 4;                       // 4..7 drain
-constexpr int kWarpDq0 = 8;                       // 8..15 dequant
+constexpr int kWarpProd = 0;                       // producer
+constexpr int kWarpIss0 = 1;                       // 1..3 MMA issuers (1 also owns TMEM)
+constexpr int kWarpDr0 = 4;                        // 4..7 drain
+constexpr int kWarpDq0 = 8;                        // 8..15 dequant
 constexpr int kWarps = kWarpDq0 + kDqWarps;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kASlots = 4;
+constexpr int kASlots = 3;                         // unit f uses A slot f % 3
+constexpr uint32_t kASlotCols = kUnitGroups * 64;  // fp16 pairs of 128 rows x 256 k
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAcol0 = 0;
-constexpr uint32_t kDcol0 = kASlots * 64;
-constexpr int kScaleAhead = 4;                    // drain-side scale prefetch distance
-constexpr int kStageGroups = 4;                   // groups fetched per stage
+constexpr uint32_t kDcol0 = kASlots * kASlotCols;
+constexpr int kAhead = 16;                         // groups of scales / zeros kept in flight
+constexpr int kRing = 32;                          // ring entries (> kAhead + 1)
 
 template <int NBLK>
 struct Layout {
-    static constexpr int kRows = 16 * NBLK;             // activation rows per box
-    static constexpr int kActBox = kRows * 128;         // one 64-k block, swizzled
+    static constexpr int kRows = 16 * NBLK;                    // activation rows per box
+    static constexpr int kActBox = kRows * 128;                // one 64-k block, swizzled
     static constexpr int kAct = 2 * kStageGroups * kActBox;
     static constexpr int kW = kAct;
-    static constexpr int kStage = kW + kStageGroups * kBlockBytes;
+    static constexpr int kStage = kW + kStageGroups * kGroupBytes;
     static constexpr int kStages = (192 * 1024) / kStage;
-    static constexpr int kDSets = 8;                    // ring of per-unit accumulator sets
-    static constexpr uint32_t kDSet = 16 * NBLK;        // columns per set
+    static constexpr uint32_t kDUnit = kUnitGroups * 16 * NBLK;   // accumulator columns per unit
+    static constexpr int kDSets = int((kTmemCols - kDcol0) / kDUnit);
     static constexpr int kBar = kStages * kStage;
     // full, empty per stage; afull, aempty per A slot; dfull, dempty per set; done; drain sync
     static constexpr int kNumBars = 2 * kStages + 2 * kASlots + 2 * kDSets + 2;
-    static constexpr int kMisc = kBar + 8 * kNumBars;
-    static constexpr int kBytes = kMisc + 64 + 1024;     // + alignment slack
+    static constexpr int kScl = kBar + ((8 * kNumBars + 127) & ~127);
+    static constexpr int kZro = kScl + kDrWarps * kRing * 64;    // 32 fp16 scales per entry
+    static constexpr int kMisc = kZro + kDqWarps * kRing * 32;   // 32 uint8 zeros per entry
+    static constexpr int kBytes = kMisc + 64 + 1024;             // + alignment slack
     static_assert(kStage % 1024 == 0, "stage alignment");
-    static_assert(kDcol0 + kDSets * kDSet <= kTmemCols, "tensor memory plan");
+    static_assert(kStages >= 2, "pipeline depth");
+    static_assert(kDSets >= 2, "tensor memory plan");
     static_assert(kBytes <= 227 * 1024, "shared memory plan");
 };
 
@@ -89,36 +111,60 @@ struct Args {
     uint32_t *tile_cnt;    // [n_tiles]
     uint32_t *status;
     int M, N, K;
-    int n_tiles, n_groups;
+    int n_tiles, n_groups, n_pairs;   // n_pairs = units per tile
     int P;
-    long long U;
+    long long U;                      // units
 };
 
-// Stages: runs of at most kStageGroups consecutive groups of one tile.
-struct StageWalk {
-    int t, g, G, left;
-    __device__ StageWalk(long long u, int n_groups, int units)
-        : t(static_cast<int>(u / n_groups)), g(static_cast<int>(u % n_groups)), G(n_groups), left(units) {}
-    __device__ int size() const { return min(min(kStageGroups, G - g), left); }
-    __device__ void next(int ng) {
-        g += ng;
-        left -= ng;
-        if (g == G) {
-            g = 0;
+// A unit: tile t, pair p (groups 2p and, if it exists, 2p + 1).
+struct UnitPos {
+    int t, p, nP, G;
+    __device__ UnitPos(long long u, int n_pairs, int n_groups)
+        : t(static_cast<int>(u / n_pairs)), p(static_cast<int>(u % n_pairs)), nP(n_pairs), G(n_groups) {}
+    __device__ int g0() const { return 2 * p; }
+    __device__ int ng() const { return min(kUnitGroups, G - 2 * p); }
+    __device__ bool tile_last() const { return p == nP - 1; }
+    __device__ void next() {
+        if (++p == nP) {
+            p = 0;
             ++t;
         }
     }
 };
 
-// Walks (tile, group) in unit order without dividing per unit.
-struct UnitWalk {
-    int t, g, G;
-    __device__ UnitWalk(long long u, int n_groups)
-        : t(static_cast<int>(u / n_groups)), g(static_cast<int>(u % n_groups)), G(n_groups) {}
-    __device__ void next() {
-        if (++g == G) {
-            g = 0;
+// Stages: runs of at most kStageUnits consecutive units of one tile.
+struct StageWalk {
+    int t, p, nP, G, left;
+    __device__ StageWalk(long long u, int n_pairs, int n_groups, int units)
+        : t(static_cast<int>(u / n_pairs)), p(static_cast<int>(u % n_pairs)), nP(n_pairs), G(n_groups), left(units) {}
+    __device__ int size() const { return min(min(kStageUnits, nP - p), left); }
+    __device__ int gbeg() const { return 2 * p; }
+    __device__ int gend(int n) const { return min(2 * (p + n), G); }
+    __device__ void next(int n) {
+        p += n;
+        left -= n;
+        if (p == nP) {
+            p = 0;
             ++t;
+        }
+    }
+};
+
+// Groups of every `step`-th unit starting at the CTA's local unit `first`,
+// in order: drives the scale and zero-point rings.
+struct GroupWalk {
+    UnitPos u;
+    int f, step, nunits, gi;
+    __device__ GroupWalk(long long ub, int first, int stride, int units, int n_pairs, int n_groups)
+        : u(ub + first, n_pairs, n_groups), f(first), step(stride), nunits(units), gi(0) {}
+    __device__ bool more() const { return f < nunits; }
+    __device__ int t() const { return u.t; }
+    __device__ int g() const { return u.g0() + gi; }
+    __device__ void next() {
+        if (++gi == u.ng()) {
+            gi = 0;
+            f += step;
+            for (int k = 0; k < step; ++k) u.next();
         }
     }
 };
@@ -128,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     using L = Layout<NBLK>;
     constexpr int S = L::kStages;
+    constexpr int DS = L::kDSets;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -139,8 +186,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     auto afull = [&](int a) { return bar0 + 8u * (2 * S + a); };
     auto aempty = [&](int a) { return bar0 + 8u * (2 * S + kASlots + a); };
     auto dfull = [&](int b) { return bar0 + 8u * (2 * S + 2 * kASlots + b); };
-    auto dempty = [&](int b) { return bar0 + 8u * (2 * S + 2 * kASlots + L::kDSets + b); };
-    const uint32_t done_bar = bar0 + 8u * (2 * S + 2 * kASlots + 2 * L::kDSets);
+    auto dempty = [&](int b) { return bar0 + 8u * (2 * S + 2 * kASlots + DS + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * S + 2 * kASlots + 2 * DS);
     const uint32_t drain_bar = done_bar + 8u;
     // [0] tmem base, [1] abort flag, [2..3] pending tile + 1 per slot, [4..5] last-arriver flags
     uint32_t *misc = reinterpret_cast<uint32_t *>(base + L::kMisc);
@@ -151,6 +198,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     const long long ub = split_begin(cta, p.U, p.P);
     const long long ue = split_begin(cta + 1, p.U, p.P);
     const int nunits = static_cast<int>(ue - ub);
+    const int G = p.n_groups;
+    const int nP = p.n_pairs;
     AbortState ab{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.status};
 
     if (threadIdx.x == 0) {
@@ -159,11 +208,11 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             mbar_init(empty(s), kDqWarps + kIssuers);
         }
         for (int a = 0; a < kASlots; ++a) {
-            mbar_init(afull(a), kDqWarps);
-            mbar_init(aempty(a), 1);
+            mbar_init(afull(a), kDqWarps / 2);     // the four quarter warps of the unit's parity
+            mbar_init(aempty(a), kUnitGroups);     // one commit per group issuer
         }
-        for (int b = 0; b < L::kDSets; ++b) {
-            mbar_init(dfull(b), 1);
+        for (int b = 0; b < DS; ++b) {
+            mbar_init(dfull(b), kUnitGroups);
             mbar_init(dempty(b), kDrWarps);
         }
         mbar_init(done_bar, kIssuers);
@@ -179,26 +228,43 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
+    grid_dep_launch();
 
     if (warp == kWarpProd) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
             prefetch_tensormap(&xmap);
-            const uint64_t pol_w = l2_policy_evict_first();
-            const uint64_t pol_x = l2_policy_evict_last();
-            StageWalk sw(ub, p.n_groups, nunits);
-            int issued = 0;
+            {
+                // Only L2 is warmed before the dependency wait: L2 is the
+                // point of coherence, so this stays correct even if the
+                // previous kernel writes the weights.
+                StageWalk pw(ub, nP, G, nunits);
+                for (int st = 0; st < S && pw.left > 0; ++st) {
+                    const int n = pw.size();
+                    prefetch_l2(p.wq + (size_t(pw.t) * G + pw.gbeg()) * kGroupBytes,
+                                (pw.gend(n) - pw.gbeg()) * kGroupBytes);
+                    pw.next(n);
+                }
+            }
+        }
+        const uint64_t pol_w = l2_policy_evict_first();
+        const uint64_t pol_x = l2_policy_evict_last();
+        StageWalk sw(ub, nP, G, nunits);
+        int issued = 0;
+        grid_dep_wait();
+        if (lane == 0) {
             for (int st = 0; sw.left > 0; ++st) {
-                const int ng = sw.size();
+                const int n = sw.size();
                 const int s = st % S;
                 if (st >= S && !mbar_wait(empty(s), ((st / S) - 1) & 1, ab)) break;
                 const uint32_t sa = base_s + s * L::kStage;
-                mbar_arrive_expect_tx(full(s), ng * kBlockBytes + L::kAct);
-                bulk_load(sa + L::kW, p.wq + (size_t(sw.t) * p.n_groups + sw.g) * kBlockBytes, ng * kBlockBytes,
-                          full(s), pol_w);
-                tma_load_3d(sa, &xmap, 0, 0, 2 * sw.g, full(s), pol_x);
+                const int g0 = sw.gbeg();
+                const uint32_t wbytes = (sw.gend(n) - g0) * kGroupBytes;
+                mbar_arrive_expect_tx(full(s), wbytes + L::kAct);
+                bulk_load(sa + L::kW, p.wq + (size_t(sw.t) * G + g0) * kGroupBytes, wbytes, full(s), pol_w);
+                tma_load_3d(sa, &xmap, 0, 0, 2 * g0, full(s), pol_x);
                 ++issued;
-                sw.next(ng);
+                sw.next(n);
             }
             if (*ab.flag) {
                 // Let every copy still in flight land before the CTA exits.
@@ -208,46 +274,59 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         }
     } else if (warp >= kWarpIss0 && warp < kWarpIss0 + kIssuers) {
         // ------------------------------------------------------ MMA issuers
+        grid_dep_wait();
         if (lane == 0) {
             const int me = warp - kWarpIss0;
             constexpr uint32_t idesc = idesc_f16_f32(128, 16);
-            StageWalk sw(ub, p.n_groups, nunits);
+            StageWalk sw(ub, nP, G, nunits);
             bool ok = true;
-            int i = 0;                          // first unit of the stage
+            int f0 = 0;                          // first unit of the stage
             for (int st = 0; sw.left > 0 && ok; ++st) {
-                const int ng = sw.size();
+                const int n = sw.size();
                 const int s = st % S;
                 // Every issuer waits for every stage, so its once-per-stage
                 // release below always lands in the phase of this stage.
                 if (!mbar_wait(full(s), (st / S) & 1, ab)) break;
-                for (int jj = 0; jj < ng; ++jj) {
-                    const int u = i + jj;
-                    if (u % kIssuers != me) continue;
-                    const int slot = u % kASlots;
-                    const int set = u % L::kDSets;
-                    if (!mbar_wait(afull(slot), (u / kASlots) & 1, ab) ||
-                        (u >= L::kDSets && !mbar_wait(dempty(set), ((u / L::kDSets) - 1) & 1, ab))) {
+                for (int jj = 0; jj < n; ++jj) {
+                    const int f = f0 + jj;
+                    // group gg of unit f belongs to issuer (2f + gg) % 3; a
+                    // unit with one group gets both of its commits from that
+                    // group's issuer
+                    const int ng = min(kUnitGroups, G - 2 * (sw.p + jj));
+                    const int i0 = (2 * f) % kIssuers, i1 = (2 * f + 1) % kIssuers;
+                    const bool mine0 = i0 == me, mine1 = ng > 1 ? i1 == me : false;
+                    if (!mine0 && !mine1) continue;
+                    const int slot = f % kASlots;
+                    const int set = f % DS;
+                    if (!mbar_wait(afull(slot), (f / kASlots) & 1, ab) ||
+                        (f >= DS && !mbar_wait(dempty(set), ((f / DS) - 1) & 1, ab))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t act = base_s + s * L::kStage + 2 * jj * L::kActBox;
-                    const uint32_t dset = tmem + kDcol0 + set * L::kDSet;
+                    const uint32_t dset = tmem + kDcol0 + set * L::kDUnit;
+                    for (int gg = 0; gg < ng; ++gg) {
+                        if (!(gg == 0 ? mine0 : mine1)) continue;
+                        const uint32_t act = base_s + s * L::kStage + 2 * (kUnitGroups * jj + gg) * L::kActBox;
 #pragma unroll
-                    for (int j = 0; j < kGroup / 16; ++j) {
+                        for (int j = 0; j < kGroup / 16; ++j) {
 #pragma unroll
-                        for (int b = 0; b < NBLK; ++b) {
-                            const uint32_t baddr = act + (j >> 2) * L::kActBox + b * 2048 + (j & 3) * 32;
-                            mma_f16_ts(dset + 16 * b, tmem + kAcol0 + slot * 64 + 8 * j, sdesc_sw128(baddr), idesc,
-                                       j > 0 ? 1u : 0u);
+                            for (int b = 0; b < NBLK; ++b) {
+                                const uint32_t baddr = act + (j >> 2) * L::kActBox + b * 2048 + (j & 3) * 32;
+                                mma_f16_ts(dset + (gg * NBLK + b) * 16, tmem + slot * kASlotCols + gg * 64 + 8 * j,
+                                           sdesc_sw128(baddr), idesc, j > 0 ? 1u : 0u);
+                            }
                         }
                     }
-                    mma_commit(aempty(slot));
-                    mma_commit(dfull(set));
+                    const int commits = (mine0 ? 1 : 0) + (mine1 ? 1 : 0) + (ng == 1 ? 1 : 0);
+                    for (int c = 0; c < commits; ++c) {
+                        mma_commit(aempty(slot));
+                        mma_commit(dfull(set));
+                    }
                 }
                 mma_commit(empty(s));
-                i += ng;
-                sw.next(ng);
+                f0 += n;
+                sw.next(n);
             }
             // Every MMA of this issuer has finished once this arrives.
             mma_commit(done_bar);
@@ -257,33 +336,49 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         // --------------------------------------------------------- dequant
         const int dq = warp - kWarpDq0;
         const int q = warp & 3;                 // TMEM lane quarter
-        const int kh = dq >> 2;                 // k half: chunks 2kh, 2kh+1 of the packed row
+        const int par = dq >> 2;                // units f with f % 2 == par
         const int r = 32 * q + lane;            // row inside the tile
         const uint32_t lane_base = uint32_t(32 * q) << 16;
         const __half2 sixteenth = __float2half2_rn(0.0625f);
-        StageWalk sw(ub, p.n_groups, nunits);
-        int d_st = 0, d_jj = 0, d_ng = sw.size();
+        grid_dep_wait();
 
-        // Loads the next unit's 64 codes of this row and k half (units are
-        // taken in order), releases its stage after the stage's last unit and
-        // dequantizes into 32 half2 registers.
-        auto load_dequant = [&](uint32_t (&regs)[32]) -> bool {
-            const int s = d_st % S;
-            if (d_jj == 0 && !warp_wait(full(s), (d_st / S) & 1, ab)) return false;
-            const uint8_t *st = base + s * L::kStage + L::kW + d_jj * kBlockBytes;
-            const uint4 va = *reinterpret_cast<const uint4 *>(st + ((2 * kh) * 128 + r) * 16);
-            const uint4 vb = *reinterpret_cast<const uint4 *>(st + ((2 * kh + 1) * 128 + r) * 16);
-            uint32_t z = 8;
-            const int n = sw.t * kTileN + r;
-            if (p.zeros != nullptr && n < p.N) z = __ldg(p.zeros + size_t(sw.g + d_jj) * p.N + n);
-            if (++d_jj == d_ng) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty(s));
-                sw.next(d_ng);
-                ++d_st;
-                d_jj = 0;
-                d_ng = sw.size();
+        // Zero points of this warp's 32 rows for the groups of its units,
+        // kAhead groups ahead (rows past N read as 0 and are never stored).
+        const bool has_zeros = p.zeros != nullptr;
+        const uint8_t *zring = base + L::kZro + dq * kRing * 32;
+        GroupWalk zw(ub, par, 2, nunits, nP, G);
+        int zissued = 0, zused = 0;
+        auto zero_issue = [&]() {
+            if (zw.more()) {
+                if (lane < 4) {
+                    const int n0 = zw.t() * kTileN + 32 * q + 8 * lane;
+                    const bool in = n0 < p.N;
+                    cp_async<8>(smem_u32(zring + (zissued % kRing) * 32 + 8 * lane),
+                                in ? static_cast<const void *>(p.zeros + size_t(zw.g()) * p.N + n0) : p.zeros,
+                                in ? 8u : 0u);
+                }
+                zw.next();
             }
+            ++zissued;
+            cp_async_commit();
+        };
+        auto zero_take = [&]() -> uint32_t {
+            cp_async_wait<kAhead - 1>();
+            __syncwarp();
+            const uint32_t z = zring[(zused % kRing) * 32 + lane];
+            ++zused;
+            __syncwarp();
+            zero_issue();
+            return z;
+        };
+        if (has_zeros)
+            for (int k = 0; k < kAhead; ++k) zero_issue();
+
+        // One 64-k step: chunks 2kh, 2kh+1 of the packed group at `grp`,
+        // dequantized with zero point z into 32 half2 registers.
+        auto dequant = [&](const uint8_t *grp, int kh, uint32_t z, uint32_t (&regs)[32]) {
+            const uint4 va = *reinterpret_cast<const uint4 *>(grp + ((2 * kh) * 128 + r) * 16);
+            const uint4 vb = *reinterpret_cast<const uint4 *>(grp + ((2 * kh + 1) * 128 + r) * 16);
             const __half2 zlo = u32_as_h2((0x6400u + z) * 0x10001u);          // 1024 + z
             const __half2 zhi = __float2half2_rn(-(64.f + float(z)));
             const uint32_t words[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
@@ -301,35 +396,63 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 regs[4 * wi + 2] = h2_as_u32(__hsub2(u32_as_h2(lo1), zlo));
                 regs[4 * wi + 3] = h2_as_u32(__hfma2(u32_as_h2(hi1), sixteenth, zhi));
             }
-            return true;
+        };
+        auto release = [&](int s) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(s));
         };
 
-        // Store unit i's registers into its A slot, dequantize the next unit
-        // into the other register set while the store runs, then publish.
-        auto store = [&](int i, const uint32_t (&regs)[32]) -> bool {
-            const int slot = i % kASlots;
-            if (i >= kASlots && !warp_wait(aempty(slot), ((i / kASlots) - 1) & 1, ab)) return false;
-            tc_fence_after();
-            tmem_st_32x32b_x32(tmem + lane_base + kAcol0 + slot * 64 + 32 * kh, regs);
-            return true;
-        };
-        auto publish = [&](int i, const uint32_t (&regs)[32]) {
-            tc_wait_st();
-            tc_keep_alive<32>(regs);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(afull(i % kASlots));
-        };
+        StageWalk sw(ub, nP, G, nunits);
+        int f0 = 0;
         uint32_t ra[32], rb[32];
-        bool ok = nunits > 0 && load_dequant(ra);
-        for (int i = 0; i < nunits && ok; i += 2) {
-            if (!store(i, ra)) break;
-            if (i + 1 < nunits) ok = load_dequant(rb);
-            publish(i, ra);
-            if (!ok || i + 1 >= nunits) break;
-            if (!store(i + 1, rb)) break;
-            if (i + 2 < nunits) ok = load_dequant(ra);
-            publish(i + 1, rb);
+        for (int st = 0; sw.left > 0; ++st) {
+            const int n = sw.size();
+            const int s = st % S;
+            // Every dequant warp waits for every stage and releases it once.
+            if (!warp_wait(full(s), (st / S) & 1, ab)) break;
+            const int jj = (par - f0) & 1;       // this warp's unit in the stage, if any
+            if (jj >= n) {
+                release(s);
+            } else {
+                const int f = f0 + jj;
+                const int ng = min(kUnitGroups, G - 2 * (sw.p + jj));
+                const int slot = f % kASlots;
+                const uint8_t *g0p = base + s * L::kStage + L::kW + (kUnitGroups * jj) * kGroupBytes;
+                const uint8_t *g1p = g0p + kGroupBytes;
+                const uint32_t z0 = has_zeros ? zero_take() : 8u;
+                const uint32_t z1 = (has_zeros && ng > 1) ? zero_take() : 8u;
+                const uint32_t col = tmem + lane_base + slot * kASlotCols;
+                dequant(g0p, 0, z0, ra);
+                if (f >= kASlots && !warp_wait(aempty(slot), ((f / kASlots) - 1) & 1, ab)) {
+                    release(s);
+                    break;
+                }
+                tc_fence_after();
+                tmem_st_32x32b_x32(col + 0, ra);
+                dequant(g0p, 1, z0, rb);
+                if (ng == 1) release(s);         // last shared-memory read of the stage
+                tc_wait_st();
+                tc_keep_alive<32>(ra);
+                tmem_st_32x32b_x32(col + 32, rb);
+                if (ng > 1) {
+                    dequant(g1p, 0, z1, ra);
+                    tc_wait_st();
+                    tc_keep_alive<32>(rb);
+                    tmem_st_32x32b_x32(col + 64, ra);
+                    dequant(g1p, 1, z1, rb);
+                    release(s);
+                    tc_wait_st();
+                    tc_keep_alive<32>(ra);
+                    tmem_st_32x32b_x32(col + 96, rb);
+                }
+                tc_wait_st();
+                tc_keep_alive<32>(rb);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(afull(slot));
+            }
+            f0 += n;
+            sw.next(n);
         }
     } else if (warp >= kWarpDr0 && warp < kWarpDr0 + kDrWarps) {
         // ----------------------------------------------------------- drain
@@ -349,28 +472,44 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             if (lane == 0) mbar_arrive(drain_bar);
             return warp_wait(drain_bar, (drain_syncs++) & 1, ab);
         };
+        grid_dep_wait();
 
-        // Group scales, prefetched kScaleAhead units ahead.
-        UnitWalk ws(ub, p.n_groups);
-        float sp[kScaleAhead];
-        auto load_scale = [&](int i) -> float {
-            float v = 0.f;
-            if (i < nunits) {
-                const int n = ws.t * kTileN + r;
-                if (n < p.N) v = __half2float(__ldg(p.scales + size_t(ws.g) * p.N + n));
-                ws.next();
+        // Group scales of this warp's 32 rows, kAhead groups ahead (rows past
+        // N read as 0 and are never stored).
+        const __half *sring = reinterpret_cast<const __half *>(base + L::kScl) + dr * kRing * 32;
+        GroupWalk sgw(ub, 0, 1, nunits, nP, G);
+        int sissued = 0, sused = 0;
+        auto scale_issue = [&]() {
+            if (sgw.more()) {
+                if (lane < 4) {
+                    const int n0 = sgw.t() * kTileN + 32 * q + 8 * lane;
+                    const bool in = n0 < p.N;
+                    cp_async<16>(smem_u32(sring + (sissued % kRing) * 32 + 8 * lane),
+                                 in ? static_cast<const void *>(p.scales + size_t(sgw.g()) * p.N + n0) : p.scales,
+                                 in ? 16u : 0u);
+                }
+                sgw.next();
             }
+            ++sissued;
+            cp_async_commit();
+        };
+        auto scale_take = [&]() -> float {
+            cp_async_wait<kAhead - 1>();
+            __syncwarp();
+            const float v = __half2float(sring[(sused % kRing) * 32 + lane]);
+            ++sused;
+            __syncwarp();
+            scale_issue();
             return v;
         };
-#pragma unroll
-        for (int k = 0; k < kScaleAhead; ++k) sp[k] = load_scale(k);
+        for (int k = 0; k < kAhead; ++k) scale_issue();
 
         // Tile finished by this CTA alone: write C.  Otherwise publish the fp32
         // partial tile and count this CTA in; whether it arrived last is read
-        // back after the CTA's last group (see fixup).
+        // back after the CTA's last unit (see fixup).
         auto flush = [&](int t) -> bool {
-            const long long t0u = (long long)t * p.n_groups;
-            const long long t1u = t0u + p.n_groups;
+            const long long t0u = (long long)t * nP;
+            const long long t1u = t0u + nP;
             const int n = t * kTileN + r;
             if (ub <= t0u && t1u <= ue) {
                 if (n < p.N) {
@@ -397,113 +536,87 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             if (!drain_sync()) return false;
             if (dr == 0 && lane == 0) {
                 misc[2 + slot] = uint32_t(t) + 1u;
-                pend_prev[slot] = atom_add_release_gpu(&p.tile_cnt[t], 1u);
+                pend_prev[slot] = atom_add_acq_rel_gpu(&p.tile_cnt[t], 1u);
             }
             return true;
         };
 
-        // After the CTA's last group: for each published partial tile, if this
-        // CTA arrived last, sum every contributor's partial in CTA order.
-        auto fixup = [&]() -> bool {
+        // After the CTA's last unit: decide, for each published partial tile,
+        // whether this CTA arrived last (the sum itself is shared by all
+        // threads after the role loops).
+        auto mark_last = [&]() {
             if (dr == 0 && lane == 0) {
                 for (int sl = 0; sl < 2; ++sl) {
                     const uint32_t tp = misc[2 + sl];
                     uint32_t last = 0u;
                     if (tp != 0u) {
-                        const long long t0u = (long long)(tp - 1u) * p.n_groups;
+                        const long long t0u = (long long)(tp - 1u) * nP;
                         const int cf = split_owner(t0u, p.U, p.P);
-                        const int cl = split_owner(t0u + p.n_groups - 1, p.U, p.P);
+                        const int cl = split_owner(t0u + nP - 1, p.U, p.P);
                         last = pend_prev[sl] == uint32_t(cl - cf) ? 1u : 0u;
-                        if (last) {
-                            fence_acq_rel_gpu();
-                            p.tile_cnt[tp - 1u] = 0u;
-                        }
+                        if (last) p.tile_cnt[tp - 1u] = 0u;
                     }
                     misc[4 + sl] = last;
                 }
             }
-            if (!drain_sync()) return false;
-            constexpr int kPart = 16 * NBLK * kTileN;
-            for (int sl = 0; sl < 2; ++sl) {
-                if (!misc[4 + sl]) continue;
-                const int t = int(misc[2 + sl]) - 1;
-                const long long t0u = (long long)t * p.n_groups;
-                const int cf = split_owner(t0u, p.U, p.P);
-                const int cl = split_owner(t0u + p.n_groups - 1, p.U, p.P);
-                const int n = t * kTileN + r;
-                float sum[NBLK][16];
-#pragma unroll
-                for (int b = 0; b < NBLK; ++b)
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) sum[b][j] = 0.f;
-                constexpr int kBatch = NBLK == 1 ? 4 : 2;     // independent loads in flight
-                for (int c0 = cf; c0 <= cl; c0 += kBatch) {
-                    float v[kBatch][NBLK][16];
-#pragma unroll
-                    for (int u = 0; u < kBatch; ++u) {
-                        const int cc = c0 + u;
-                        const int sl2 = (cc <= cl && split_begin(cc, p.U, p.P) >= t0u) ? 0 : 1;
-                        const float *src = p.partial + (size_t(cc <= cl ? cc : cl) * 2 + sl2) * kPart;
-#pragma unroll
-                        for (int b = 0; b < NBLK; ++b)
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int m = 16 * b + j;
-                                v[u][b][j] = (cc <= cl && m < p.M) ? __ldcg(src + m * kTileN + r) : 0.f;
-                            }
-                    }
-#pragma unroll
-                    for (int u = 0; u < kBatch; ++u)
-                        if (c0 + u <= cl) {
-#pragma unroll
-                            for (int b = 0; b < NBLK; ++b)
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) sum[b][j] += v[u][b][j];
-                        }
-                }
-                if (n < p.N) {
-#pragma unroll
-                    for (int b = 0; b < NBLK; ++b)
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int m = 16 * b + j;
-                            if (m < p.M) p.C[size_t(m) * p.N + n] = __float2half_rn(sum[b][j]);
-                        }
-                }
-            }
-            return true;
         };
 
-        UnitWalk wd(ub, p.n_groups);
+        UnitPos wd(ub, nP, G);
         bool ok = true;
-        for (int i = 0; i < nunits && ok; ++i) {
-            const int set = i % L::kDSets;
-            if (!warp_wait(dfull(set), (i / L::kDSets) & 1, ab)) {
+        for (int f = 0; f < nunits && ok; ++f) {
+            const int set = f % DS;
+            if (!warp_wait(dfull(set), (f / DS) & 1, ab)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float sc = sp[0];
+            const int ng = wd.ng();
+            const uint32_t dset = tmem + lane_base + kDcol0 + set * L::kDUnit;
+            // accumulators [group][block][16]; group 1 only if the unit has it
+            uint32_t d[kUnitGroups * NBLK][16];
+            if constexpr (NBLK == 1) {
+                uint32_t d2[32];
+                tmem_ld_32x32b_x32(dset, d2);
+                tc_wait_ld_keep<32>(d2);
 #pragma unroll
-            for (int k = 0; k + 1 < kScaleAhead; ++k) sp[k] = sp[k + 1];
-            sp[kScaleAhead - 1] = load_scale(i + kScaleAhead);
-            const uint32_t dset = tmem + lane_base + kDcol0 + set * L::kDSet;
-            uint32_t d[NBLK][16];
+                for (int j = 0; j < 16; ++j) {
+                    d[0][j] = d2[j];
+                    d[1][j] = d2[16 + j];
+                }
+            } else {
+                uint32_t d2[32], d3[32];
+                tmem_ld_32x32b_x32(dset, d2);
+                tmem_ld_32x32b_x32(dset + 32, d3);
+                tc_wait_ld_keep<32>(d2);
+                tc_wait_ld_keep<32>(d3);
 #pragma unroll
-            for (int b = 0; b < NBLK; ++b) tmem_ld_32x32b_x16(dset + 16 * b, d[b]);
-#pragma unroll
-            for (int b = 0; b < NBLK; ++b) tc_wait_ld_keep<16>(d[b]);
+                for (int j = 0; j < 16; ++j) {
+                    d[0][j] = d2[j];
+                    d[1][j] = d2[16 + j];
+                    d[2][j] = d3[j];
+                    d[3][j] = d3[16 + j];
+                }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dempty(set));
+            // groups in ascending order, each scaled in fp32
+            const float s0 = scale_take();
 #pragma unroll
             for (int b = 0; b < NBLK; ++b)
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[b][j] = fmaf(sc, __uint_as_float(d[b][j]), acc[b][j]);
+                for (int j = 0; j < 16; ++j) acc[b][j] = fmaf(s0, __uint_as_float(d[b][j]), acc[b][j]);
+            if (ng > 1) {
+                const float s1 = scale_take();
+#pragma unroll
+                for (int b = 0; b < NBLK; ++b)
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[b][j] = fmaf(s1, __uint_as_float(d[NBLK + b][j]), acc[b][j]);
+            }
             const int t = wd.t;
-            const bool tile_end = wd.g == p.n_groups - 1;
+            const bool tile_end = wd.tile_last();
             wd.next();
-            if (tile_end || i == nunits - 1) {
+            if (tile_end || f == nunits - 1) {
                 if (!flush(t)) {
                     ok = false;
                     break;
@@ -514,7 +627,57 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                     for (int j = 0; j < 16; ++j) acc[b][j] = 0.f;
             }
         }
-        if (ok) fixup();
+        if (ok) mark_last();
+    }
+
+    // ------------------------------------------- split-tile fix-up (all threads)
+    __syncthreads();
+    if (*ab.flag == 0u) {
+        constexpr int kPart = 16 * NBLK * kTileN;
+        constexpr int kBatch = 8;                           // contributors loaded at once
+        for (int sl = 0; sl < 2; ++sl) {
+            if (!misc[4 + sl]) continue;
+            const int t = int(misc[2 + sl]) - 1;
+            const long long t0u = (long long)t * nP;
+            const int cf = split_owner(t0u, p.U, p.P);
+            const int cl = split_owner(t0u + nP - 1, p.U, p.P);
+            for (int e4 = threadIdx.x; e4 < kPart / 4; e4 += kThreads) {   // float4 of the [m][128] tile
+                const int m = e4 / (kTileN / 4);
+                const int n0 = t * kTileN + 4 * (e4 % (kTileN / 4));
+                if (m >= p.M) continue;
+                float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int c0 = cf; c0 <= cl; c0 += kBatch) {
+                    float4 v[kBatch];
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u) {
+                        const int cc = c0 + u;
+                        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (cc <= cl) {
+                            const int sl2 = split_begin(cc, p.U, p.P) >= t0u ? 0 : 1;
+                            const float4 *src = reinterpret_cast<const float4 *>(
+                                p.partial + (size_t(cc) * 2 + sl2) * kPart + size_t(m) * kTileN + (n0 - t * kTileN));
+                            v[u] = __ldcg(src);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u)
+                        if (c0 + u <= cl) {
+                            sum.x += v[u].x;
+                            sum.y += v[u].y;
+                            sum.z += v[u].z;
+                            sum.w += v[u].w;
+                        }
+                }
+                if (n0 < p.N) {
+                    const __half2 lo = __floats2half2_rn(sum.x, sum.y);
+                    const __half2 hi = __floats2half2_rn(sum.z, sum.w);
+                    uint2 packed;
+                    packed.x = h2_as_u32(lo);
+                    packed.y = h2_as_u32(hi);
+                    *reinterpret_cast<uint2 *>(p.C + size_t(m) * p.N + n0) = packed;
+                }
+            }
+        }
     }
 
     tc_fence_before();
@@ -539,8 +702,11 @@ w4v_status launch(const CUtensorMap &xmap, const Args &a, cudaStream_t stream) {
         }
         configured_for = dev;
     }
-    w4a16_decode_kernel<NBLK><<<a.P, kThreads, L::kBytes, stream>>>(xmap, a);
-    return cudaGetLastError() == cudaSuccess ? W4V_OK : W4V_ERR_CUDA;
+    if (launch_pdl(w4a16_decode_kernel<NBLK>, dim3(a.P), dim3(kThreads), L::kBytes, stream, xmap, a) != cudaSuccess) {
+        cudaGetLastError();
+        return W4V_ERR_CUDA;
+    }
+    return W4V_OK;
 }
 
 }  // namespace
@@ -570,7 +736,8 @@ w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t
     a.K = K;
     a.n_tiles = (N + kTileN - 1) / kTileN;
     a.n_groups = K / kGroup;
-    a.U = (long long)a.n_tiles * a.n_groups;
+    a.n_pairs = (a.n_groups + kUnitGroups - 1) / kUnitGroups;
+    a.U = (long long)a.n_tiles * a.n_pairs;
     a.P = static_cast<int>(std::min<long long>(std::min(info->sm_count, kMaxCtas), a.U));
     a.partial = static_cast<float *>(ws);
     a.tile_cnt = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) +

@@ -112,6 +112,8 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
+    grid_dep_launch();
+    grid_dep_wait();
 
     // Tiles are taken round-robin; consecutive CTAs share an activation tile
     // (weights tile index varies fastest), so activations are reused in L2.
@@ -309,8 +311,11 @@ w4v_status launch_w4a16_prefill(const uint16_t *A, const void *Bq, const uint16_
     }
     const long long tiles = (long long)a.n_tiles_n * a.n_tiles_m;
     const int grid = static_cast<int>(std::min<long long>(2LL * info->sm_count, tiles));
-    w4a16_prefill_kernel<<<grid, kThreads, kBytes, stream>>>(xmap, a);
-    return cudaGetLastError() == cudaSuccess ? W4V_OK : W4V_ERR_CUDA;
+    if (launch_pdl(w4a16_prefill_kernel, dim3(grid), dim3(kThreads), kBytes, stream, xmap, a) != cudaSuccess) {
+        cudaGetLastError();
+        return W4V_ERR_CUDA;
+    }
+    return W4V_OK;
 }
 
 }  // namespace w4v

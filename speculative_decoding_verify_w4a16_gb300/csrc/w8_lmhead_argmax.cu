@@ -30,8 +30,10 @@
 //     lowest-index maximum; a shared-memory 64-bit atomicMax of (key, ~index)
 //     keeps the CTA's best per row.
 //   * Each CTA folds its best keys into one global 64-bit atomicMax per row;
-//     the last CTA to arrive (release/acquire counter, no waiting) reads and
+//     the last CTA to arrive (acquire-release counter, no waiting) reads and
 //     clears them and writes the token ids.
+//   * Launched with programmatic stream serialization: set-up and an L2
+//     prefetch of the first weight stages overlap the previous kernel's end.
 #include "runtime.h"
 #include "sm103_ptx.cuh"
 
@@ -181,12 +183,23 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
+    grid_dep_launch();
 
     if (warp == kWarpProd) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
             prefetch_tensormap(&wmap);
             prefetch_tensormap(&xmap);
+            // Only L2 is warmed before the dependency wait (L2 is the point
+            // of coherence, so this is safe whatever the previous kernel writes).
+            ChunkWalk pw(p.n_chunks, ntiles);
+            for (int st = 0; st < S && pw.more(); ++st) {
+                prefetch_l2_3d(&wmap, 0, (tb + pw.j) * kTileV, pw.c);
+                pw.next(pw.size());
+            }
+        }
+        grid_dep_wait();
+        if (lane == 0) {
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_x = l2_policy_evict_last();
             int issued = 0;
@@ -209,6 +222,7 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
         }
     } else if (warp >= kWarpIss0 && warp < kWarpIss0 + kIssuers) {
         // ------------------------------------------------------ MMA issuers
+        grid_dep_wait();
         if (lane == 0) {
             const int me = warp - kWarpIss0;
             constexpr uint32_t idesc = idesc_f16_f32(128, 16);
@@ -252,6 +266,7 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
             mbar_wait_bounded(done_bar, 0);
         }
     } else if (warp >= kWarpDq0) {
+        grid_dep_wait();
         // --------------------------------------------------------- dequant
         const int dq = warp - kWarpDq0;
         const int q = warp & 3;
@@ -325,6 +340,7 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
         }
     } else if (warp >= kWarpDr0 && warp < kWarpDr0 + kDrWarps) {
         // ----------------------------------------------------------- drain
+        grid_dep_wait();
         const int dr = warp - kWarpDr0;
         const int q = warp & 3;
         const int r = 32 * q + lane;
@@ -407,12 +423,9 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
         }
         if (ok) {
             if (tid == 0) {
-                const uint32_t prev = atom_add_release_gpu(p.counter, 1u);
+                const uint32_t prev = atom_add_acq_rel_gpu(p.counter, 1u);
                 const bool last = prev == uint32_t(p.P - 1);
-                if (last) {
-                    fence_acq_rel_gpu();
-                    *p.counter = 0u;
-                }
+                if (last) *p.counter = 0u;
                 misc[2] = last ? 1u : 0u;
             }
             ok = drain_sync();
@@ -446,8 +459,12 @@ w4v_status launch(const CUtensorMap &xmap, const CUtensorMap &wmap, const Args &
         }
         configured_for = dev;
     }
-    w8_lmhead_argmax_kernel<NBLK><<<a.P, kThreads, L::kBytes, stream>>>(xmap, wmap, a);
-    return cudaGetLastError() == cudaSuccess ? W4V_OK : W4V_ERR_CUDA;
+    if (launch_pdl(w8_lmhead_argmax_kernel<NBLK>, dim3(a.P), dim3(kThreads), L::kBytes, stream, xmap, wmap, a) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return W4V_ERR_CUDA;
+    }
+    return W4V_OK;
 }
 
 }  // namespace
