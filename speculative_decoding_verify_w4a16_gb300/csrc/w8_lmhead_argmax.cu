@@ -15,11 +15,16 @@
 //     so a stage is two k-chunks of a tile: one 3-D TMA of 32 KB of int8
 //     weights (128-byte swizzle, straight from the row-major [V][K] matrix)
 //     and one 3-D TMA of the matching activation slices, both issued by one
-//     producer thread.
+//     producer thread.  A unit is one stage: 128 rows x 256 k.  Every
+//     hand-off between roles costs a few hundred cycles of latency whatever
+//     it carries, so units are as large as tensor memory allows (A slots of
+//     128 columns).
 //   * Eight dequant warps widen int8 to exact fp16 (XOR 0x80, PRMT into the
 //     mantissa of 1024, subtract 1152) and store it into tensor memory with
-//     32-column stores; two register sets alternate so the store of one unit
-//     overlaps the dequant of the next.
+//     32-column stores.  Warp (quarter, parity) owns its 32 rows of every
+//     other unit and does the unit's whole k in four 64-k steps, alternating
+//     two register sets so each store overlaps the next step's arithmetic;
+//     the two warps sharing a scheduler work on different units.
 //   * Three issuer threads (one MMA per ~55 cycles each) run tcgen05.mma with
 //     A from TMEM, accumulating the whole K of a tile in TMEM; the k-steps go
 //     round-robin into independent accumulators, each (accumulator, column
@@ -53,11 +58,10 @@ constexpr int kWarpDr0 = 4;                 // 4..7
 constexpr int kWarpDq0 = 8;                 // 8..15
 constexpr int kWarps = kWarpDq0 + kDqWarps;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kASlots = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAcol0 = 0;
-constexpr uint32_t kDcol0 = kASlots * 64;
-constexpr int kStageChunks = 2;             // k-chunks fetched per stage
+constexpr int kStageChunks = 2;             // k-chunks per stage = per unit
+constexpr uint32_t kASlotCols = kStageChunks * 64;
 
 template <int NBLK>
 struct Layout {
@@ -71,6 +75,9 @@ struct Layout {
     // so the per-logit arithmetic does not depend on M there.
     static constexpr int kAcc = NBLK <= 2 ? 3 : 8 / NBLK;
     static constexpr uint32_t kDSet = kAcc * 16 * NBLK;  // laid out [block][acc][16]
+    // A slots: as many 128-column units as fit beside two accumulator sets
+    static constexpr int kASlots = NBLK == 1 ? 3 : 2;
+    static constexpr uint32_t kDcol0 = kASlots * kASlotCols;
     static constexpr int kBar = kStages * kStage;
     static constexpr int kNumBars = 2 * kStages + 2 * kASlots + 4 + 2;
     static constexpr int kBest = ((kBar + 8 * kNumBars + 7) / 8) * 8;   // u64 [128]
@@ -129,6 +136,8 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
                         const Args p) {
     using L = Layout<NBLK>;
     constexpr int S = L::kStages;
+    constexpr int kASlots = L::kASlots;
+    constexpr uint32_t kDcol0 = L::kDcol0;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -158,10 +167,10 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), kDqWarps + kIssuers);
+            mbar_init(empty(s), kDqWarps / 2 + kIssuers);   // the unit's four dequant warps + issuers
         }
         for (int a = 0; a < kASlots; ++a) {
-            mbar_init(afull(a), kDqWarps);
+            mbar_init(afull(a), kDqWarps / 2);
             mbar_init(aempty(a), kIssuers);
         }
         for (int b = 0; b < 2; ++b) {
@@ -228,23 +237,22 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
             constexpr uint32_t idesc = idesc_f16_f32(128, 16);
             ChunkWalk cw(p.n_chunks, ntiles);
             bool ok = true;
-            int i = 0;
-            for (int st = 0; cw.more() && ok; ++st) {
+            for (int st = 0; cw.more() && ok; ++st) {      // unit st = stage st
                 const int ng = cw.size();
                 const int s = st % S;
-                if (!mbar_wait(full(s), (st / S) & 1, ab)) break;
-                for (int jj = 0; jj < ng; ++jj, ++i) {
-                    const int j = cw.j, c = cw.c + jj;
-                    const int slot = i % kASlots;
-                    const int buf = j & 1;
-                    if (!mbar_wait(afull(slot), (i / kASlots) & 1, ab) ||
-                        (c == 0 && j >= 2 && !mbar_wait(dempty(buf), ((j >> 1) - 1) & 1, ab))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                const int j = cw.j;
+                const int slot = st % kASlots;
+                const int buf = j & 1;
+                if (!mbar_wait(full(s), (st / S) & 1, ab) || !mbar_wait(afull(slot), (st / kASlots) & 1, ab) ||
+                    (cw.c == 0 && j >= 2 && !mbar_wait(dempty(buf), ((j >> 1) - 1) & 1, ab))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dset = tmem + kDcol0 + buf * L::kDSet;
+                for (int jj = 0; jj < ng; ++jj) {
+                    const int c = cw.c + jj;
                     const uint32_t act = base_s + s * L::kStage + 2 * jj * L::kActBox;
-                    const uint32_t dset = tmem + kDcol0 + buf * L::kDSet;
 #pragma unroll
                     for (int kk = 0; kk < kChunk / 16; ++kk) {
 #pragma unroll
@@ -252,14 +260,15 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
                             const int a = kk % L::kAcc;
                             if ((a * NBLK + b) % kIssuers != me) continue;
                             const uint32_t baddr = act + (kk >> 2) * L::kActBox + b * 2048 + (kk & 3) * 32;
-                            mma_f16_ts(dset + (b * L::kAcc + a) * 16, tmem + kAcol0 + slot * 64 + 8 * kk,
-                                       sdesc_sw128(baddr), idesc, (c > 0 || kk >= L::kAcc) ? 1u : 0u);
+                            mma_f16_ts(dset + (b * L::kAcc + a) * 16,
+                                       tmem + kAcol0 + slot * kASlotCols + jj * 64 + 8 * kk, sdesc_sw128(baddr),
+                                       idesc, (c > 0 || kk >= L::kAcc) ? 1u : 0u);
                         }
                     }
-                    mma_commit(aempty(slot));
-                    if (c == p.n_chunks - 1) mma_commit(dfull(buf));
-                    if (jj == ng - 1) mma_commit(empty(s));
                 }
+                mma_commit(aempty(slot));
+                if (cw.c + ng == p.n_chunks) mma_commit(dfull(buf));
+                mma_commit(empty(s));
                 cw.next(ng);
             }
             mma_commit(done_bar);
@@ -270,33 +279,20 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
         // --------------------------------------------------------- dequant
         const int dq = warp - kWarpDq0;
         const int q = warp & 3;
-        const int kh = dq >> 2;                 // 64-byte half of the 128-byte row
+        const int par = dq >> 2;                // units (stages) st with st % 2 == par
         const int r = 32 * q + lane;
         const uint32_t lane_base = uint32_t(32 * q) << 16;
         const __half2 bias = u32_as_h2(0x64806480u);    // 1152 = 1024 + 128 in both halves
 
-        ChunkWalk cw(p.n_chunks, ntiles);
-        int d_st = 0, d_jj = 0, d_ng = cw.size();
-        // Loads the next unit's 64 bytes of this row (units in order), releases
-        // its stage after the stage's last unit and widens them to 32 half2.
-        auto load_dequant = [&](uint32_t (&regs)[32]) -> bool {
-            const int s = d_st % S;
-            if (d_jj == 0 && !warp_wait(full(s), (d_st / S) & 1, ab)) return false;
-            const uint8_t *st = base + s * L::kStage + L::kW + d_jj * kWBytes;
+        // 64 bytes (half kh of chunk row r) of the chunk at `ch`, widened to
+        // 32 half2 registers.
+        auto dequant = [&](const uint8_t *ch, int kh, uint32_t (&regs)[32]) {
             uint4 w[4];
 #pragma unroll
             for (int ci = 0; ci < 4; ++ci) {
                 const int chunk = 4 * kh + ci;
                 const int phys = chunk ^ (r & 7);            // 128-byte swizzle of the TMA box
-                w[ci] = *reinterpret_cast<const uint4 *>(st + r * 128 + phys * 16);
-            }
-            if (++d_jj == d_ng) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty(s));
-                cw.next(d_ng);
-                ++d_st;
-                d_jj = 0;
-                d_ng = cw.more() ? cw.size() : 0;
+                w[ci] = *reinterpret_cast<const uint4 *>(ch + r * 128 + phys * 16);
             }
 #pragma unroll
             for (int ci = 0; ci < 4; ++ci) {
@@ -310,33 +306,52 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
                     regs[8 * ci + 2 * wd + 1] = h2_as_u32(__hsub2(u32_as_h2(p23), bias));
                 }
             }
-            return true;
+        };
+        auto release = [&](int s) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(s));
         };
 
-        auto store = [&](int i, const uint32_t (&regs)[32]) -> bool {
-            const int slot = i % kASlots;
-            if (i >= kASlots && !warp_wait(aempty(slot), ((i / kASlots) - 1) & 1, ab)) return false;
+        ChunkWalk cw(p.n_chunks, ntiles);
+        uint32_t ra[32], rb[32];
+        for (int st = 0; cw.more(); ++st) {
+            const int ng = cw.size();
+            cw.next(ng);
+            if ((st & 1) != par) continue;
+            const int s = st % S;
+            const int slot = st % kASlots;
+            if (!warp_wait(full(s), (st / S) & 1, ab)) break;
+            const uint8_t *c0p = base + s * L::kStage + L::kW;
+            const uint8_t *c1p = c0p + kWBytes;
+            const uint32_t col = tmem + lane_base + kAcol0 + slot * kASlotCols;
+            dequant(c0p, 0, ra);
+            if (st >= kASlots && !warp_wait(aempty(slot), ((st / kASlots) - 1) & 1, ab)) {
+                release(s);
+                break;
+            }
             tc_fence_after();
-            tmem_st_32x32b_x32(tmem + lane_base + kAcol0 + slot * 64 + 32 * kh, regs);
-            return true;
-        };
-        auto publish = [&](int i, const uint32_t (&regs)[32]) {
+            tmem_st_32x32b_x32(col + 0, ra);
+            dequant(c0p, 1, rb);
+            if (ng == 1) release(s);             // last shared-memory read of the stage
             tc_wait_st();
-            tc_keep_alive<32>(regs);
+            tc_keep_alive<32>(ra);
+            tmem_st_32x32b_x32(col + 32, rb);
+            if (ng > 1) {
+                dequant(c1p, 0, ra);
+                tc_wait_st();
+                tc_keep_alive<32>(rb);
+                tmem_st_32x32b_x32(col + 64, ra);
+                dequant(c1p, 1, rb);
+                release(s);
+                tc_wait_st();
+                tc_keep_alive<32>(ra);
+                tmem_st_32x32b_x32(col + 96, rb);
+            }
+            tc_wait_st();
+            tc_keep_alive<32>(rb);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(afull(i % kASlots));
-        };
-        uint32_t ra[32], rb[32];
-        bool ok = nunits > 0 && load_dequant(ra);
-        for (int i = 0; i < nunits && ok; i += 2) {
-            if (!store(i, ra)) break;
-            if (i + 1 < nunits) ok = load_dequant(rb);
-            publish(i, ra);
-            if (!ok || i + 1 >= nunits) break;
-            if (!store(i + 1, rb)) break;
-            if (i + 2 < nunits) ok = load_dequant(ra);
-            publish(i + 1, rb);
+            if (lane == 0) mbar_arrive(afull(slot));
         }
     } else if (warp >= kWarpDr0 && warp < kWarpDr0 + kDrWarps) {
         // ----------------------------------------------------------- drain
