@@ -72,22 +72,29 @@ __device__ __forceinline__ void raise_abort(const AbortState &ab) {
     atomicOr(ab.status, 1u << kStatusTimeout);
 }
 
+// Slow path of mbar_wait, kept out of line so the many wait sites of a
+// kernel stay small in the instruction cache.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t *flag,
+                                            uint32_t *status) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 7u) == 0u) {
+            if (*flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                raise_abort(AbortState{flag, status});
+                return false;
+            }
+        }
+    }
+}
+
 // Waits until the phase with the given parity has completed.  Returns false
 // (after raising the abort state) if the limit passes or another role of the
 // CTA has aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const AbortState &ab) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 7u) == 0u) {
-            if (*ab.flag) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                raise_abort(ab);
-                return false;
-            }
-        }
-    }
+    return mbar_wait_slow(bar, parity, ab.flag, ab.status);
 }
 
 // Whole-warp wait: every lane waits (each gets the barrier's acquire), the

@@ -422,28 +422,35 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 const uint32_t z0 = has_zeros ? zero_take() : 8u;
                 const uint32_t z1 = (has_zeros && ng > 1) ? zero_take() : 8u;
                 const uint32_t col = tmem + lane_base + slot * kASlotCols;
-                dequant(g0p, 0, z0, ra);
-                if (f >= kASlots && !warp_wait(aempty(slot), ((f / kASlots) - 1) & 1, ab)) {
-                    release(s);
-                    break;
-                }
-                tc_fence_after();
-                tmem_st_32x32b_x32(col + 0, ra);
-                dequant(g0p, 1, z0, rb);
-                if (ng == 1) release(s);         // last shared-memory read of the stage
-                tc_wait_st();
-                tc_keep_alive<32>(ra);
-                tmem_st_32x32b_x32(col + 32, rb);
-                if (ng > 1) {
-                    dequant(g1p, 0, z1, ra);
-                    tc_wait_st();
-                    tc_keep_alive<32>(rb);
-                    tmem_st_32x32b_x32(col + 64, ra);
-                    dequant(g1p, 1, z1, rb);
-                    release(s);
+                // group gg: half 0 into ra, half 1 into rb; each store
+                // overlaps the next half's arithmetic (one copy of the
+                // dequant code per register set keeps the kernel small)
+                bool aborted = false;
+#pragma unroll 1
+                for (int gg = 0; gg < ng; ++gg) {
+                    const uint8_t *gp = gg == 0 ? g0p : g1p;
+                    const uint32_t z = gg == 0 ? z0 : z1;
+                    dequant(gp, 0, z, ra);
+                    if (gg == 0) {
+                        if (f >= kASlots && !warp_wait(aempty(slot), ((f / kASlots) - 1) & 1, ab)) {
+                            aborted = true;
+                            break;
+                        }
+                        tc_fence_after();
+                    } else {
+                        tc_wait_st();
+                        tc_keep_alive<32>(rb);
+                    }
+                    tmem_st_32x32b_x32(col + 64 * gg, ra);
+                    dequant(gp, 1, z, rb);
+                    if (gg == ng - 1) release(s);     // last shared-memory read of the stage
                     tc_wait_st();
                     tc_keep_alive<32>(ra);
-                    tmem_st_32x32b_x32(col + 96, rb);
+                    tmem_st_32x32b_x32(col + 64 * gg + 32, rb);
+                }
+                if (aborted) {
+                    release(s);
+                    break;
                 }
                 tc_wait_st();
                 tc_keep_alive<32>(rb);

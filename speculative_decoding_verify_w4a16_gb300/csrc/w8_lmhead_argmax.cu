@@ -161,7 +161,6 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
     const int tb = static_cast<int>(split_begin(cta, p.n_tiles, p.P));
     const int te = static_cast<int>(split_begin(cta + 1, p.n_tiles, p.P));
     const int ntiles = te - tb;
-    const int nunits = ntiles * p.n_chunks;
     AbortState ab{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.status};
 
     if (threadIdx.x == 0) {

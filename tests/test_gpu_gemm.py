@@ -32,7 +32,7 @@ def test_cfg0_linear(w4v_mod, gpu, oracle_mod):
 
 @pytest.mark.parametrize("M,N,K", [(1, 512, 256), (2, 128, 128), (5, 200, 384), (8, 1024, 1024),
                                    (16, 2560, 2560), (17, 520, 640), (21, 768, 1280), (32, 384, 2560),
-                                   (16, 2560, 9728)])
+                                   (16, 2560, 9728), (9, 384, 768), (12, 136, 1664), (31, 264, 1152)])
 def test_shapes(w4v_mod, gpu, oracle_mod, M, N, K):
     A = inputs.activations(M, M, K, "shape")
     q = inputs.w4_codes(M, N, K, "shape")
@@ -41,8 +41,10 @@ def test_shapes(w4v_mod, gpu, oracle_mod, M, N, K):
     assert gemm_rel_err(C, oracle_mod.w4a16_gemm(A, q, s)) <= GEMM_TOL
 
 
-def test_zero_points(w4v_mod, gpu, oracle_mod):
-    M, N, K = 16, 512, 512
+@pytest.mark.parametrize("M,N,K", [(16, 512, 512), (3, 272, 640), (24, 400, 3200)])
+def test_zero_points(w4v_mod, gpu, oracle_mod, M, N, K):
+    """Per-(group, row) zero points, including odd group counts (a unit
+    with a single group at each tile end) and a partial last tile."""
     A = inputs.activations(3, M, K)
     q = inputs.w4_codes(3, N, K)
     s = inputs.w4_scales(3, N, K)
