@@ -166,6 +166,23 @@ def capture(torch, fn):
     return g
 
 
+def reduce_step_time(ms_local, world, device=None):
+    """Per-step time of the whole job: the maximum over ranks (every rank
+    runs the same replica workload; the job ends with the slowest)."""
+    if world <= 1:
+        return ms_local
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(bytes_per_rank, ms_step, world):
+    """Whole-job throughput in GB/s: every rank's bytes over the job's step time."""
+    return world * bytes_per_rank / (ms_step * 1e-3) / 1e9
+
+
 def run_gpu(args, rank, world):
     import torch
     from speculative_decoding_verify_w4a16_gb300 import _build, w4v
@@ -205,13 +222,8 @@ def run_gpu(args, rank, world):
         end.record()
         torch.cuda.synchronize()
     ms_total = start.elapsed_time(end)
-    ms_step_local = ms_total / args.steps
-    ms_step = ms_step_local
-    if world > 1:
-        t = torch.tensor([ms_step_local], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * total_bytes / (ms_step * 1e-3) / 1e9
+    ms_step = reduce_step_time(ms_total / args.steps, world, dev)
+    value = job_value(total_bytes, ms_step, world)
 
     # ---- per-kernel durations: each kernel alone in a graph of repeated launches
     kern = {}
@@ -294,15 +306,17 @@ def run_e2e(args, step, torch, total_bytes, world):
         graphs[c].replay()
     torch.cuda.synchronize()
     steps = args.steps
+    if world > 1:
+        torch.distributed.barrier()
     t0 = time.perf_counter()
     for i in range(steps):
         graphs[i % COPIES].replay()
         torch.cuda.current_stream().synchronize()     # the host reads the accepted tokens every step
         _ = int(h_n[0])
-    dt = (time.perf_counter() - t0) / steps
+    ms = reduce_step_time((time.perf_counter() - t0) / steps * 1e3, world, step.draft.device)
     h2d = sum(v.numel() * v.element_size() for v in h_acts.values()) + h_X.numel() * 2 + h_d.numel() * 4
     d2h = h_n.numel() * 4 + h_tok.numel() * 4
-    return {"value": round(world * total_bytes / dt / 1e9, 1), "unit": "GB/s", "ms_per_step": round(dt * 1e3, 5),
+    return {"value": round(job_value(total_bytes, ms, world), 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "how": "pinned host -> device activations and drafts, one CUDA graph of the step, "
                    "device -> host accepted tokens, host synchronize each step (wall clock)"}

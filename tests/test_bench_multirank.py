@@ -1,0 +1,55 @@
+"""Host logic of bench.py's multi-GPU mode on CPU: two gloo ranks stand in for
+two GPUs.  Each rank runs the same replica workload; the job's step time is
+the maximum over ranks and the job's throughput counts every rank's bytes.
+The reference arm runs on rank 0 only."""
+import os
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _worker(rank, world, port, out):
+    import torch
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms_local = 1.0 + 0.5 * rank            # rank 1 is the slow one
+        ms = bench.reduce_step_time(ms_local, world)
+        value = bench.job_value(1e9, ms, world)
+        out[rank] = (ms, value)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_value():
+    world = 2
+    port = 29500 + (os.getpid() % 1000)
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    assert res[0][0] == res[1][0] == pytest.approx(1.5)
+    # 2 ranks x 1 GB in 1.5 ms each step
+    assert res[0][1] == res[1][1] == pytest.approx(2 * 1e9 / 1.5e-3 / 1e9)
+
+
+def test_single_rank_passthrough():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.reduce_step_time(0.25, 1) == 0.25
+    assert bench.job_value(5e8, 0.5, 1) == pytest.approx(1000.0)
+
+
+def test_reference_arm_only_on_rank0():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3"], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
