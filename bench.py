@@ -166,6 +166,42 @@ def capture(torch, fn):
     return g
 
 
+LM_HEAD_SOURCES = ("w8_lmhead_argmax.cu", "sm103_ptx.cuh", "runtime.h")
+LM_HEAD_PROFILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "w8_lmhead_argmax_m16.md")
+
+
+def kernel_source_sha(names):
+    """Short fingerprint of the sources a kernel is compiled from."""
+    import hashlib
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "speculative_decoding_verify_w4a16_gb300", "csrc")
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(profile, names):
+    """DRAM bytes per launch (read + write) from the committed ncu summary of a
+    kernel, or None when the summary was taken from other sources than the
+    ones the kernel is built from now."""
+    try:
+        lines = open(profile).read().splitlines()
+    except OSError:
+        return None
+    vals = {}
+    for ln in lines:
+        if ":" in ln and ln.split(":", 1)[0].strip() in ("source_sha256", "dram_bytes_read", "dram_bytes_write"):
+            k, v = ln.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_sha256") != kernel_source_sha(names):
+        return None
+    try:
+        return int(vals["dram_bytes_read"]) + int(vals["dram_bytes_write"])
+    except (KeyError, ValueError):
+        return None
+
+
 def reduce_step_time(ms_local, world, device=None):
     """Per-step time of the whole job: the maximum over ranks (every rank
     runs the same replica workload; the job ends with the slowest)."""
@@ -258,7 +294,10 @@ def run_gpu(args, rank, world):
         "roofline": {"bound": "hbm", "kernel": "w8_lmhead_argmax (M=16, V=151936, K=2560), %d launches "
                                "in one graph, CUDA events on the launching stream" % reps,
                      "achieved": round(lm["GB/s"], 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(lm["frac"], 4), "traffic": None,
+                     "frac": round(lm["frac"], 4),
+                     "traffic": profiled_traffic(LM_HEAD_PROFILE, LM_HEAD_SOURCES),
+                     "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum per launch, ncu summary "
+                                       "profiles/w8_lmhead_argmax_m16.md (null if taken from other sources)",
                      "peak_source": peaks["source"] + " (hbm copy, burst)"},
         "gemm_m16": {"GB/s": round(gemm_gbs, 1), "frac": round(gemm_gbs / peaks["hbm_gbs"], 4),
                      "ms": round(gemm_ms, 5), "bytes": proj_bytes},

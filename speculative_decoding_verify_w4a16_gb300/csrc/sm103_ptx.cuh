@@ -338,6 +338,29 @@ __device__ __forceinline__ void tc_wait_ld_keep(uint32_t (&r)[n]) {
                      "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])::"memory");
 }
 
+// --------------------------------------------------------- shared-memory loads
+// Explicit shared-space loads (the address is a shared-window offset), so no
+// access goes through the generic path.  They are ordered after the barrier
+// waits that publish the data (volatile asm with a memory clobber).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint16_t lds_u16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // ------------------------------------------------------- gpu-scope atomics
 // Release-only increment: publishes this CTA's earlier writes without making
 // later memory operations wait for the atomic to return.

@@ -365,7 +365,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         auto zero_take = [&]() -> uint32_t {
             cp_async_wait<kAhead - 1>();
             __syncwarp();
-            const uint32_t z = zring[(zused % kRing) * 32 + lane];
+            const uint32_t z = lds_u8(smem_u32(zring) + (zused % kRing) * 32 + lane);
             ++zused;
             __syncwarp();
             zero_issue();
@@ -374,11 +374,11 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         if (has_zeros)
             for (int k = 0; k < kAhead; ++k) zero_issue();
 
-        // One 64-k step: chunks 2kh, 2kh+1 of the packed group at `grp`,
+        // One 64-k step: chunks 2kh, 2kh+1 of the packed group at shared address `grp`,
         // dequantized with zero point z into 32 half2 registers.
-        auto dequant = [&](const uint8_t *grp, int kh, uint32_t z, uint32_t (&regs)[32]) {
-            const uint4 va = *reinterpret_cast<const uint4 *>(grp + ((2 * kh) * 128 + r) * 16);
-            const uint4 vb = *reinterpret_cast<const uint4 *>(grp + ((2 * kh + 1) * 128 + r) * 16);
+        auto dequant = [&](uint32_t grp, int kh, uint32_t z, uint32_t (&regs)[32]) {
+            const uint4 va = lds128(grp + ((2 * kh) * 128 + r) * 16);
+            const uint4 vb = lds128(grp + ((2 * kh + 1) * 128 + r) * 16);
             const __half2 zlo = u32_as_h2((0x6400u + z) * 0x10001u);          // 1024 + z
             const __half2 zhi = __float2half2_rn(-(64.f + float(z)));
             const uint32_t words[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
@@ -417,8 +417,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 const int f = f0 + jj;
                 const int ng = min(kUnitGroups, G - 2 * (sw.p + jj));
                 const int slot = f % kASlots;
-                const uint8_t *g0p = base + s * L::kStage + L::kW + (kUnitGroups * jj) * kGroupBytes;
-                const uint8_t *g1p = g0p + kGroupBytes;
+                const uint32_t g0p = base_s + s * L::kStage + L::kW + (kUnitGroups * jj) * kGroupBytes;
+                const uint32_t g1p = g0p + kGroupBytes;
                 const uint32_t z0 = has_zeros ? zero_take() : 8u;
                 const uint32_t z1 = (has_zeros && ng > 1) ? zero_take() : 8u;
                 const uint32_t col = tmem + lane_base + slot * kASlotCols;
@@ -428,7 +428,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 bool aborted = false;
 #pragma unroll 1
                 for (int gg = 0; gg < ng; ++gg) {
-                    const uint8_t *gp = gg == 0 ? g0p : g1p;
+                    const uint32_t gp = gg == 0 ? g0p : g1p;
                     const uint32_t z = gg == 0 ? z0 : z1;
                     dequant(gp, 0, z, ra);
                     if (gg == 0) {
@@ -503,7 +503,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         auto scale_take = [&]() -> float {
             cp_async_wait<kAhead - 1>();
             __syncwarp();
-            const float v = __half2float(sring[(sused % kRing) * 32 + lane]);
+            const float v = __half2float(__ushort_as_half(lds_u16(smem_u32(sring + (sused % kRing) * 32 + lane))));
             ++sused;
             __syncwarp();
             scale_issue();

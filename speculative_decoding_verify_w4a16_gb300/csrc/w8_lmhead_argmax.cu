@@ -283,15 +283,15 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
         const uint32_t lane_base = uint32_t(32 * q) << 16;
         const __half2 bias = u32_as_h2(0x64806480u);    // 1152 = 1024 + 128 in both halves
 
-        // 64 bytes (half kh of chunk row r) of the chunk at `ch`, widened to
+        // 64 bytes (half kh of chunk row r) of the chunk at shared address `ch`, widened to
         // 32 half2 registers.
-        auto dequant = [&](const uint8_t *ch, int kh, uint32_t (&regs)[32]) {
+        auto dequant = [&](uint32_t ch, int kh, uint32_t (&regs)[32]) {
             uint4 w[4];
 #pragma unroll
             for (int ci = 0; ci < 4; ++ci) {
                 const int chunk = 4 * kh + ci;
                 const int phys = chunk ^ (r & 7);            // 128-byte swizzle of the TMA box
-                w[ci] = *reinterpret_cast<const uint4 *>(ch + r * 128 + phys * 16);
+                w[ci] = lds128(ch + r * 128 + phys * 16);
             }
 #pragma unroll
             for (int ci = 0; ci < 4; ++ci) {
@@ -320,8 +320,8 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
             const int s = st % S;
             const int slot = st % kASlots;
             if (!warp_wait(full(s), (st / S) & 1, ab)) break;
-            const uint8_t *c0p = base + s * L::kStage + L::kW;
-            const uint8_t *c1p = c0p + kWBytes;
+            const uint32_t c0p = base_s + s * L::kStage + L::kW;
+            const uint32_t c1p = c0p + kWBytes;
             const uint32_t col = tmem + lane_base + kAcol0 + slot * kASlotCols;
             dequant(c0p, 0, ra);
             if (st >= kASlots && !warp_wait(aempty(slot), ((st / kASlots) - 1) & 1, ab)) {
