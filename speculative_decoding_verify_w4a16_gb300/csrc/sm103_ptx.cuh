@@ -338,6 +338,61 @@ __device__ __forceinline__ void tc_wait_ld_keep(uint32_t (&r)[n]) {
                      "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])::"memory");
 }
 
+// ----------------------------------------------------- thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of all CTAs of the cluster; makes every CTA's barrier
+// initialisation visible before any CTA touches another's shared memory.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+// Arrive on an mbarrier of another CTA of the cluster, releasing this
+// thread's earlier shared-memory writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Bounded wait with cluster-scope acquire (sees other CTAs' released writes).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const AbortState &ab) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0;; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((it & 7u) == 7u) {
+            if (*ab.flag) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                raise_abort(ab);
+                return false;
+            }
+        }
+    }
+}
+
 // --------------------------------------------------------- shared-memory loads
 // Explicit shared-space loads (the address is a shared-window offset), so no
 // access goes through the generic path.  They are ordered after the barrier
@@ -348,6 +403,14 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr)
                  : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
 __device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {

@@ -41,16 +41,23 @@
 //     them, and a global load takes over a microsecond when HBM is busy:
 //     each warp keeps the next 16 groups' values in flight with cp.async
 //     into a shared-memory ring.
-//   * Work is the flat list of units split evenly over one CTA per SM; a
-//     tile shared by several CTAs is finished by the last one to arrive
-//     (acquire-release counter, no waiting between CTAs), which sums the fp32
-//     partial tiles in CTA order, so the result is deterministic.  All 512
-//     threads of that CTA share the sum, each loading every contributor's
-//     float4 at once: on this two-die part an L2 round trip can take well
-//     over a microsecond, so the fix-up is one round of loads, not several.
+//   * Work split.  With few 128-row tiles, each tile belongs to a
+//     thread-block cluster of C CTAs (C up to 4, as many as fit one wave)
+//     that split its k range; each member leaves its fp32 partial tile in
+//     its own shared memory and the cluster's first CTA reads them through
+//     distributed shared memory, adds them in rank order and writes C: no
+//     global round trip, which on this two-die part costs well over a
+//     microsecond each.  With at least
+//     as many tiles as SMs, the flat list of units is split evenly over one
+//     CTA per SM (stream-K); a tile shared by several CTAs is finished by the
+//     last one to arrive (acquire-release counter, no waiting between CTAs),
+//     whose threads all load every contributor's float4 at once and add them
+//     in CTA order.  Both orders are fixed, so the result is deterministic.
 //   * The kernel is launched with programmatic stream serialization: barrier
 //     set-up, tensor-memory allocation and an L2 prefetch of the first
 //     weight stages overlap the end of the previous kernel in the stream.
+#include <mutex>
+
 #include "runtime.h"
 #include "sm103_ptx.cuh"
 
@@ -79,6 +86,12 @@ constexpr uint32_t kDcol0 = kASlots * kASlotCols;
 constexpr int kAhead = 16;                         // groups of scales / zeros kept in flight
 constexpr int kRing = 32;                          // ring entries (> kAhead + 1)
 
+constexpr int kMaxStages = 4;
+constexpr int kMaxSmem = 227 * 1024;
+
+// Shared memory: S stages, then a fixed block of barriers, rings and flags.
+// A cluster member's partial tile is left in its first stage once all its
+// MMAs have completed.
 template <int NBLK>
 struct Layout {
     static constexpr int kRows = 16 * NBLK;                    // activation rows per box
@@ -86,20 +99,25 @@ struct Layout {
     static constexpr int kAct = 2 * kStageGroups * kActBox;
     static constexpr int kW = kAct;
     static constexpr int kStage = kW + kStageGroups * kGroupBytes;
-    static constexpr int kStages = (192 * 1024) / kStage;
     static constexpr uint32_t kDUnit = kUnitGroups * 16 * NBLK;   // accumulator columns per unit
     static constexpr int kDSets = int((kTmemCols - kDcol0) / kDUnit);
-    static constexpr int kBar = kStages * kStage;
-    // full, empty per stage; afull, aempty per A slot; dfull, dempty per set; done; drain sync
-    static constexpr int kNumBars = 2 * kStages + 2 * kASlots + 2 * kDSets + 2;
-    static constexpr int kScl = kBar + ((8 * kNumBars + 127) & ~127);
-    static constexpr int kZro = kScl + kDrWarps * kRing * 64;    // 32 fp16 scales per entry
-    static constexpr int kMisc = kZro + kDqWarps * kRing * 32;   // 32 uint8 zeros per entry
-    static constexpr int kBytes = kMisc + 64 + 1024;             // + alignment slack
+    // full, empty per stage (room for kMaxStages); afull, aempty per A slot;
+    // dfull, dempty per set; done; drain sync; cluster reduction
+    static constexpr int kNumBars = 2 * kMaxStages + 2 * kASlots + 2 * kDSets + 3;
+    static constexpr int kBarBytes = (8 * kNumBars + 127) & ~127;
+    static constexpr int kScl = kBarBytes;                         // offsets inside the fixed block
+    static constexpr int kZro = kScl + kDrWarps * kRing * 64;      // 32 fp16 scales per entry
+    static constexpr int kMisc = kZro + kDqWarps * kRing * 32;     // 32 uint8 zeros per entry
+    static constexpr int kFixed = kMisc + 128;
+    static constexpr int kPart = 16 * NBLK * kTileN;               // floats of one partial tile
+    __host__ __device__ static constexpr int bytes(int stages) { return stages * kStage + kFixed + 1024; }
     static_assert(kStage % 1024 == 0, "stage alignment");
-    static_assert(kStages >= 2, "pipeline depth");
     static_assert(kDSets >= 2, "tensor memory plan");
-    static_assert(kBytes <= 227 * 1024, "shared memory plan");
+    static constexpr int kStagesMax = (kMaxSmem - kFixed - 1024) / kStage < kMaxStages
+                                          ? (kMaxSmem - kFixed - 1024) / kStage
+                                          : kMaxStages;
+    static_assert(kStagesMax >= 2 && bytes(kStagesMax) <= kMaxSmem, "shared memory plan");
+    static_assert(kPart * 4 <= kStage, "partial tile fits a stage");
 };
 
 struct Args {
@@ -107,13 +125,15 @@ struct Args {
     const __half *scales;
     const uint8_t *zeros;
     __half *C;
-    float *partial;        // [P][2][16*NBLK][128]
-    uint32_t *tile_cnt;    // [n_tiles]
+    float *partial;        // [P][2][16*NBLK][128] (stream-K only)
+    uint32_t *tile_cnt;    // [n_tiles] (stream-K only)
     uint32_t *status;
     int M, N, K;
     int n_tiles, n_groups, n_pairs;   // n_pairs = units per tile
-    int P;
+    int P;                            // CTAs
     long long U;                      // units
+    int stages;                       // pipeline stages in shared memory
+    int cluster;                      // CTAs per tile (cluster size); 0 = stream-K
 };
 
 // A unit: tile t, pair p (groups 2p and, if it exists, 2p + 1).
@@ -150,6 +170,22 @@ struct StageWalk {
     }
 };
 
+// Position in the ring of S stages: slot and phase parity of the current use
+// (kept incrementally; S is a launch parameter).
+struct StageRing {
+    int S, s = 0;
+    uint32_t ph = 0;
+    bool wrapped = false;
+    __device__ explicit StageRing(int stages) : S(stages) {}
+    __device__ void next() {
+        if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+            wrapped = true;
+        }
+    }
+};
+
 // Groups of every `step`-th unit starting at the CTA's local unit `first`,
 // in order: drives the scale and zero-point rings.
 struct GroupWalk {
@@ -173,33 +209,46 @@ template <int NBLK>
 __global__ void __launch_bounds__(kThreads, 1)
 w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     using L = Layout<NBLK>;
-    constexpr int S = L::kStages;
     constexpr int DS = L::kDSets;
+    constexpr int MS = kMaxStages;
+    const int S = p.stages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     uint8_t *base = smem_raw + (base_s - raw_s);
+    const uint32_t fixed_off = uint32_t(S) * L::kStage;
 
-    const uint32_t bar0 = base_s + L::kBar;
+    const uint32_t bar0 = base_s + fixed_off;
     auto full = [&](int s) { return bar0 + 8u * s; };
-    auto empty = [&](int s) { return bar0 + 8u * (S + s); };
-    auto afull = [&](int a) { return bar0 + 8u * (2 * S + a); };
-    auto aempty = [&](int a) { return bar0 + 8u * (2 * S + kASlots + a); };
-    auto dfull = [&](int b) { return bar0 + 8u * (2 * S + 2 * kASlots + b); };
-    auto dempty = [&](int b) { return bar0 + 8u * (2 * S + 2 * kASlots + DS + b); };
-    const uint32_t done_bar = bar0 + 8u * (2 * S + 2 * kASlots + 2 * DS);
+    auto empty = [&](int s) { return bar0 + 8u * (MS + s); };
+    auto afull = [&](int a) { return bar0 + 8u * (2 * MS + a); };
+    auto aempty = [&](int a) { return bar0 + 8u * (2 * MS + kASlots + a); };
+    auto dfull = [&](int b) { return bar0 + 8u * (2 * MS + 2 * kASlots + b); };
+    auto dempty = [&](int b) { return bar0 + 8u * (2 * MS + 2 * kASlots + DS + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * MS + 2 * kASlots + 2 * DS);
     const uint32_t drain_bar = done_bar + 8u;
+    const uint32_t red_bar = drain_bar + 8u;
     // [0] tmem base, [1] abort flag, [2..3] pending tile + 1 per slot, [4..5] last-arriver flags
-    uint32_t *misc = reinterpret_cast<uint32_t *>(base + L::kMisc);
+    uint32_t *misc = reinterpret_cast<uint32_t *>(base + fixed_off + L::kMisc);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
-    const long long ub = split_begin(cta, p.U, p.P);
-    const long long ue = split_begin(cta + 1, p.U, p.P);
-    const int nunits = static_cast<int>(ue - ub);
     const int G = p.n_groups;
     const int nP = p.n_pairs;
+    const int CL = p.cluster;                 // 0: stream-K
+    const int crank = CL > 0 ? static_cast<int>(cluster_ctarank()) : 0;
+    long long ub, ue;
+    if (CL > 0) {
+        // one tile per cluster; member `crank` takes its share of the tile's units
+        const long long t0u = (long long)(cta / CL) * nP;
+        ub = t0u + (long long)crank * nP / CL;
+        ue = t0u + (long long)(crank + 1) * nP / CL;
+    } else {
+        ub = split_begin(cta, p.U, p.P);
+        ue = split_begin(cta + 1, p.U, p.P);
+    }
+    const int nunits = static_cast<int>(ue - ub);
     AbortState ab{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.status};
 
     if (threadIdx.x == 0) {
@@ -217,6 +266,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         }
         mbar_init(done_bar, kIssuers);
         mbar_init(drain_bar, kDrWarps);
+        mbar_init(red_bar, CL > 1 ? (CL - 1) * kDrWarps : 1);
         for (int k = 1; k < 16; ++k) misc[k] = 0;
         fence_barrier_init();
     }
@@ -228,6 +278,9 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
+    // every CTA of the cluster has initialised its barriers before any
+    // member arrives on the leader's
+    if (CL > 1) cluster_sync_all();
     grid_dep_launch();
 
     if (warp == kWarpProd) {
@@ -253,10 +306,11 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         int issued = 0;
         grid_dep_wait();
         if (lane == 0) {
-            for (int st = 0; sw.left > 0; ++st) {
+            StageRing rg(S);
+            for (; sw.left > 0; rg.next()) {
                 const int n = sw.size();
-                const int s = st % S;
-                if (st >= S && !mbar_wait(empty(s), ((st / S) - 1) & 1, ab)) break;
+                const int s = rg.s;
+                if (rg.wrapped && !mbar_wait(empty(s), rg.ph ^ 1u, ab)) break;
                 const uint32_t sa = base_s + s * L::kStage;
                 const int g0 = sw.gbeg();
                 const uint32_t wbytes = (sw.gend(n) - g0) * kGroupBytes;
@@ -269,7 +323,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             if (*ab.flag) {
                 // Let every copy still in flight land before the CTA exits.
                 for (int i = max(0, issued - S); i < issued; ++i)
-                    mbar_wait_bounded(full(i % S), (i / S) & 1);
+                    mbar_wait_bounded(full(i % S), uint32_t(i / S) & 1u);
             }
         }
     } else if (warp >= kWarpIss0 && warp < kWarpIss0 + kIssuers) {
@@ -281,12 +335,13 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             StageWalk sw(ub, nP, G, nunits);
             bool ok = true;
             int f0 = 0;                          // first unit of the stage
-            for (int st = 0; sw.left > 0 && ok; ++st) {
+            StageRing rg(S);
+            for (; sw.left > 0 && ok; rg.next()) {
                 const int n = sw.size();
-                const int s = st % S;
+                const int s = rg.s;
                 // Every issuer waits for every stage, so its once-per-stage
                 // release below always lands in the phase of this stage.
-                if (!mbar_wait(full(s), (st / S) & 1, ab)) break;
+                if (!mbar_wait(full(s), rg.ph, ab)) break;
                 for (int jj = 0; jj < n; ++jj) {
                     const int f = f0 + jj;
                     // group gg of unit f belongs to issuer (2f + gg) % 3; a
@@ -345,7 +400,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         // Zero points of this warp's 32 rows for the groups of its units,
         // kAhead groups ahead (rows past N read as 0 and are never stored).
         const bool has_zeros = p.zeros != nullptr;
-        const uint8_t *zring = base + L::kZro + dq * kRing * 32;
+        const uint8_t *zring = base + fixed_off + L::kZro + dq * kRing * 32;
         GroupWalk zw(ub, par, 2, nunits, nP, G);
         int zissued = 0, zused = 0;
         auto zero_issue = [&]() {
@@ -405,11 +460,12 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         StageWalk sw(ub, nP, G, nunits);
         int f0 = 0;
         uint32_t ra[32], rb[32];
-        for (int st = 0; sw.left > 0; ++st) {
+        StageRing rg(S);
+        for (; sw.left > 0; rg.next()) {
             const int n = sw.size();
-            const int s = st % S;
+            const int s = rg.s;
             // Every dequant warp waits for every stage and releases it once.
-            if (!warp_wait(full(s), (st / S) & 1, ab)) break;
+            if (!warp_wait(full(s), rg.ph, ab)) break;
             const int jj = (par - f0) & 1;       // this warp's unit in the stage, if any
             if (jj >= n) {
                 release(s);
@@ -483,7 +539,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
 
         // Group scales of this warp's 32 rows, kAhead groups ahead (rows past
         // N read as 0 and are never stored).
-        const __half *sring = reinterpret_cast<const __half *>(base + L::kScl) + dr * kRing * 32;
+        const __half *sring = reinterpret_cast<const __half *>(base + fixed_off + L::kScl) + dr * kRing * 32;
         GroupWalk sgw(ub, 0, 1, nunits, nP, G);
         int sissued = 0, sused = 0;
         auto scale_issue = [&]() {
@@ -518,6 +574,51 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             const long long t0u = (long long)t * nP;
             const long long t1u = t0u + nP;
             const int n = t * kTileN + r;
+            if (CL > 1) {
+                if (crank != 0) {
+                    // member: partial tile [m][128] into its own first stage
+                    // (every MMA of this CTA has completed), then arrive on
+                    // the leader's barrier
+#pragma unroll
+                    for (int b = 0; b < NBLK; ++b)
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int m = 16 * b + j;
+                            if (m < p.M) sts_f32(base_s + uint32_t(m * kTileN + r) * 4u, acc[b][j]);
+                        }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(mapa_shared(red_bar, 0u));
+                    return true;
+                }
+                // leader: own partial first, then the members' in rank order
+                if (!mbar_wait_cluster(red_bar, 0, ab)) return false;
+                for (int k = 1; k < CL; ++k) {
+                    float v[NBLK][16];
+#pragma unroll
+                    for (int b = 0; b < NBLK; ++b)
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int m = 16 * b + j;
+                            v[b][j] = m < p.M ? ld_cluster_f32(mapa_shared(base_s + uint32_t(m * kTileN + r) * 4u,
+                                                                           uint32_t(k)))
+                                              : 0.f;
+                        }
+#pragma unroll
+                    for (int b = 0; b < NBLK; ++b)
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[b][j] += v[b][j];
+                }
+                if (n < p.N) {
+#pragma unroll
+                    for (int b = 0; b < NBLK; ++b)
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int m = 16 * b + j;
+                            if (m < p.M) p.C[size_t(m) * p.N + n] = __float2half_rn(acc[b][j]);
+                        }
+                }
+                return true;
+            }
             if (ub <= t0u && t1u <= ue) {
                 if (n < p.N) {
 #pragma unroll
@@ -637,9 +738,9 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         if (ok) mark_last();
     }
 
-    // ------------------------------------------- split-tile fix-up (all threads)
+    // ----------------------------- stream-K split-tile fix-up (all threads)
     __syncthreads();
-    if (*ab.flag == 0u) {
+    if (CL == 0 && *ab.flag == 0u) {
         constexpr int kPart = 16 * NBLK * kTileN;
         constexpr int kBatch = 8;                           // contributors loaded at once
         for (int sl = 0; sl < 2; ++sl) {
@@ -687,6 +788,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         }
     }
 
+    // a member's partial tile is read by the leader: nobody leaves before it has
+    if (CL > 1) cluster_sync_all();
     tc_fence_before();
     __syncthreads();
     if (warp == kWarpIss0) {
@@ -695,25 +798,97 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     }
 }
 
+// CTAs per tile.  Measured on the 4B shapes at M = 16: beyond four members
+// the leader's extra distributed-shared-memory reads cost more than the
+// shorter k range saves.
+constexpr int kMaxCluster = 4;
+// A stream-K fix-up (counter round trip plus one round of partial loads)
+// costs about as much as this many units of work.
+constexpr int kFixupUnits = 2;
+
+// Cluster size for a shape: the largest c <= kMaxCluster, <= units per tile and
+// <= SMs per tile whose clusters all fit one wave, or 0 for stream-K when
+// that leaves each CTA more than kFixupUnits units beyond stream-K's share.
+// It depends on the shape only (never on M), so every M <= 32 splits k the
+// same way and sums the same partials in the same order (batch invariance).
+int pick_cluster(int n_tiles, int n_pairs, int sm_count) {
+    if (n_tiles * 2 > sm_count) return 0;
+    const long long units = (long long)n_tiles * n_pairs;
+    const long long streamk_share = (units + sm_count - 1) / sm_count;
+    int c = std::min(kMaxCluster, std::min(n_pairs, sm_count / n_tiles));
+    if ((n_pairs + c - 1) / c > streamk_share + kFixupUnits) return 0;
+    for (; c >= 2; --c) {
+        // one CTA per SM for either variant; the larger one's query bounds both
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(n_tiles * c);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = Layout<2>::bytes(Layout<2>::kStagesMax);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = c;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int fit = 0;
+        if (cudaOccupancyMaxActiveClusters(&fit, w4a16_decode_kernel<2>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (fit >= n_tiles) return c;
+    }
+    return 0;
+}
+
 template <int NBLK>
-w4v_status launch(const CUtensorMap &xmap, const Args &a, cudaStream_t stream) {
-    using L = Layout<NBLK>;
+w4v_status configure() {
     static int configured_for = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_for != dev) {
         if (cudaFuncSetAttribute(w4a16_decode_kernel<NBLK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 L::kBytes) != cudaSuccess) {
+                                 kMaxSmem) != cudaSuccess) {
             cudaGetLastError();
             return W4V_ERR_CUDA;
         }
         configured_for = dev;
     }
-    if (launch_pdl(w4a16_decode_kernel<NBLK>, dim3(a.P), dim3(kThreads), L::kBytes, stream, xmap, a) != cudaSuccess) {
+    return W4V_OK;
+}
+
+template <int NBLK>
+w4v_status launch(const CUtensorMap &xmap, Args &a, int cluster, cudaStream_t stream) {
+    using L = Layout<NBLK>;
+    w4v_status st = configure<NBLK>();
+    if (st != W4V_OK) return st;
+    a.cluster = cluster;
+    a.stages = L::kStagesMax;
+    if (cluster > 0) a.P = a.n_tiles * cluster;
+    const size_t smem = size_t(L::bytes(a.stages));
+    if (launch_pdl_cluster(w4a16_decode_kernel<NBLK>, dim3(a.P), dim3(kThreads), smem, stream, cluster, xmap, a) !=
+        cudaSuccess) {
         cudaGetLastError();
         return W4V_ERR_CUDA;
     }
     return W4V_OK;
+}
+
+// Cluster size per (device, tiles, units per tile), cached (the occupancy
+// query needs both kernel variants configured).
+int cluster_for(int n_tiles, int n_pairs, int sm_count) {
+    struct Entry { int dev, n_tiles, n_pairs, cluster; };
+    static Entry cache[64];
+    static int n_cache = 0;
+    static std::mutex mu;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_cache; ++i)
+        if (cache[i].dev == dev && cache[i].n_tiles == n_tiles && cache[i].n_pairs == n_pairs) return cache[i].cluster;
+    if (configure<1>() != W4V_OK || configure<2>() != W4V_OK) return 0;
+    const int c = pick_cluster(n_tiles, n_pairs, sm_count);
+    if (n_cache < 64) cache[n_cache++] = Entry{dev, n_tiles, n_pairs, c};
+    return c;
 }
 
 }  // namespace
@@ -754,8 +929,9 @@ w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t
     st = encode_tmap_kblocks(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, uint64_t(K), uint64_t(M), 64, 16 * nblk,
                              2 * kStageGroups, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != W4V_OK) return st;
-    if (nblk == 1) return launch<1>(xmap, a, stream);
-    return launch<2>(xmap, a, stream);
+    const int cluster = cluster_for(a.n_tiles, a.n_pairs, info->sm_count);
+    if (nblk == 1) return launch<1>(xmap, a, cluster, stream);
+    return launch<2>(xmap, a, cluster, stream);
 }
 
 }  // namespace w4v
