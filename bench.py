@@ -151,7 +151,8 @@ class VerifyStep:
     def enqueue(self, copy):
         w4v = self.w4v
         for p, packed, s in self.projs[copy]:
-            w4v.w4a16_gemm(self.acts[p.name], packed, s, p.N, out=self.outs[p.name], ws=self.ws[p.name])
+            w4v.w4a16_gemm(self.acts[p.name], packed, s, p.N, out=self.outs[p.name], ws=self.ws[p.name],
+                           static_weights=True)
         self.lm_head()
         w4v.spec_accept(self.tok.view(1, M_VERIFY), self.draft, n_out=self.n_acc, tok_out=self.out_tok)
 
@@ -290,7 +291,9 @@ def run_gpu(args, rank, world):
                    "M": M_VERIFY, "K_draft": K_DRAFT, "bytes_per_step": total_bytes,
                    "l2": "inputs larger than L2: 442 MB read per step, projection weights rotate over "
                          "%d copies" % COPIES,
-                   "graph": "one CUDA graph per step", "parallelism": "replicas" if world > 1 else "1 GPU"},
+                   "graph": "one CUDA graph per step", "parallelism": "replicas" if world > 1 else "1 GPU",
+                   "weights": "static (W4V_STATIC_WEIGHTS: projection weights may be loaded before the previous "
+                              "kernel ends; inputs and outputs wait for it)"},
         "roofline": {"bound": "hbm", "kernel": "w8_lmhead_argmax (M=16, V=151936, K=2560), %d launches "
                                "in one graph, CUDA events on the launching stream" % reps,
                      "achieved": round(lm["GB/s"], 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -419,7 +422,8 @@ class Stack:
         def run():
             for lay in self.layers:
                 p, packed, sc = lay[k]
-                self.w4v.w4a16_gemm(acts[p.name], packed, sc, p.N, out=outs[p.name], ws=wss[p.name])
+                self.w4v.w4a16_gemm(acts[p.name], packed, sc, p.N, out=outs[p.name], ws=wss[p.name],
+                                    static_weights=True)
 
         return time_graph(self.torch, run) / self.LAYERS
 
@@ -431,7 +435,8 @@ class Stack:
             def run():
                 for lay in self.layers:
                     for (p, packed, sc) in lay:
-                        self.w4v.w4a16_gemm(acts[p.name], packed, sc, p.N, out=outs[p.name], ws=wss[p.name])
+                        self.w4v.w4a16_gemm(acts[p.name], packed, sc, p.N, out=outs[p.name], ws=wss[p.name],
+                                    static_weights=True)
 
             ms = time_graph(self.torch, run)
             b = self.LAYERS * sum(p.N * p.K // 2 + (p.K // 128) * p.N * 2 + M * p.K * 2 for p in inputs.LAYER_PROJS)

@@ -114,6 +114,21 @@ w4v_status w4a16_gemm(const uint16_t *A, const void *Bq, const uint16_t *scales,
                       const uint8_t *zeros, int group, uint16_t *C, int M, int N, int K,
                       void *workspace, size_t workspace_bytes, w4v_stream_t stream);
 
+/* w4a16_gemm with flags (w4a16_gemm is w4a16_gemm_ex with flags == 0).
+ *   W4V_STATIC_WEIGHTS: Bq, scales and zeros are not written by any GPU
+ *     work that may still be running when this call's kernel starts (the
+ *     weights of a model during inference).  The verify-sized kernel then
+ *     loads and dequantizes its first weight stages while the previous
+ *     kernel of the stream is still finishing; A is still read, and C and
+ *     the workspace still written, only after that kernel has completed.
+ *     Without the flag the weights are only prefetched into L2 early.
+ * Unknown flag bits: W4V_ERR_ARG.  The pages have no counterpart: it is a
+ * scheduling promise of the caller, the result is the same either way. */
+#define W4V_STATIC_WEIGHTS 1u
+w4v_status w4a16_gemm_ex(const uint16_t *A, const void *Bq, const uint16_t *scales,
+                         const uint8_t *zeros, int group, uint16_t *C, int M, int N, int K,
+                         void *workspace, size_t workspace_bytes, unsigned flags, w4v_stream_t stream);
+
 /* ------------------------------------------------------- w8_lmhead_argmax
  * Greedy token per row: argmax_out[r] = argmax_v scale[v] * sum_k X[r][k]*W[v][k],
  * int8 weights, one fp16 scale per vocabulary row, fp32 accumulation with

@@ -90,7 +90,7 @@ __host__ __device__ inline int split_owner(long long u, long long units, long lo
 // Launchers (one per kernel family), called after argument validation.
 w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t *scales,
                                const uint8_t *zeros, uint16_t *C, int M, int N, int K,
-                               void *ws, cudaStream_t stream);
+                               void *ws, bool static_weights, cudaStream_t stream);
 size_t w4a16_decode_ws_bytes(int M, int N, int K);
 w4v_status launch_w4a16_prefill(const uint16_t *A, const void *Bq, const uint16_t *scales, const uint8_t *zeros,
                                 uint16_t *C, int M, int N, int K, cudaStream_t stream);

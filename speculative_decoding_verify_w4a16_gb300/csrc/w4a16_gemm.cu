@@ -56,6 +56,11 @@
 //   * The kernel is launched with programmatic stream serialization: barrier
 //     set-up, tensor-memory allocation and an L2 prefetch of the first
 //     weight stages overlap the end of the previous kernel in the stream.
+//     When the caller declares the weights static (nothing still running
+//     writes them), the first stages' weights are loaded, and their units
+//     dequantized into tensor memory, before the dependency wait; only the
+//     activation copies and the output wait for the previous kernel.  Each
+//     stage therefore has separate weight and activation barriers.
 #include <mutex>
 
 #include "runtime.h"
@@ -101,9 +106,9 @@ struct Layout {
     static constexpr int kStage = kW + kStageGroups * kGroupBytes;
     static constexpr uint32_t kDUnit = kUnitGroups * 16 * NBLK;   // accumulator columns per unit
     static constexpr int kDSets = int((kTmemCols - kDcol0) / kDUnit);
-    // full, empty per stage (room for kMaxStages); afull, aempty per A slot;
+    // wfull, xfull, empty per stage (room for kMaxStages); afull, aempty per A slot;
     // dfull, dempty per set; done; drain sync; cluster reduction
-    static constexpr int kNumBars = 2 * kMaxStages + 2 * kASlots + 2 * kDSets + 3;
+    static constexpr int kNumBars = 3 * kMaxStages + 2 * kASlots + 2 * kDSets + 3;
     static constexpr int kBarBytes = (8 * kNumBars + 127) & ~127;
     static constexpr int kScl = kBarBytes;                         // offsets inside the fixed block
     static constexpr int kZro = kScl + kDrWarps * kRing * 64;      // 32 fp16 scales per entry
@@ -134,6 +139,7 @@ struct Args {
     long long U;                      // units
     int stages;                       // pipeline stages in shared memory
     int cluster;                      // CTAs per tile (cluster size); 0 = stream-K
+    int static_w;                     // weights, scales, zeros not written by earlier work in flight
 };
 
 // A unit: tile t, pair p (groups 2p and, if it exists, 2p + 1).
@@ -219,13 +225,14 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     const uint32_t fixed_off = uint32_t(S) * L::kStage;
 
     const uint32_t bar0 = base_s + fixed_off;
-    auto full = [&](int s) { return bar0 + 8u * s; };
-    auto empty = [&](int s) { return bar0 + 8u * (MS + s); };
-    auto afull = [&](int a) { return bar0 + 8u * (2 * MS + a); };
-    auto aempty = [&](int a) { return bar0 + 8u * (2 * MS + kASlots + a); };
-    auto dfull = [&](int b) { return bar0 + 8u * (2 * MS + 2 * kASlots + b); };
-    auto dempty = [&](int b) { return bar0 + 8u * (2 * MS + 2 * kASlots + DS + b); };
-    const uint32_t done_bar = bar0 + 8u * (2 * MS + 2 * kASlots + 2 * DS);
+    auto wfull = [&](int s) { return bar0 + 8u * s; };          // stage's weights landed
+    auto xfull = [&](int s) { return bar0 + 8u * (MS + s); };   // stage's activations landed
+    auto empty = [&](int s) { return bar0 + 8u * (2 * MS + s); };
+    auto afull = [&](int a) { return bar0 + 8u * (3 * MS + a); };
+    auto aempty = [&](int a) { return bar0 + 8u * (3 * MS + kASlots + a); };
+    auto dfull = [&](int b) { return bar0 + 8u * (3 * MS + 2 * kASlots + b); };
+    auto dempty = [&](int b) { return bar0 + 8u * (3 * MS + 2 * kASlots + DS + b); };
+    const uint32_t done_bar = bar0 + 8u * (3 * MS + 2 * kASlots + 2 * DS);
     const uint32_t drain_bar = done_bar + 8u;
     const uint32_t red_bar = drain_bar + 8u;
     // [0] tmem base, [1] abort flag, [2..3] pending tile + 1 per slot, [4..5] last-arriver flags
@@ -253,7 +260,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full(s), 1);
+            mbar_init(wfull(s), 1);
+            mbar_init(xfull(s), 1);
             mbar_init(empty(s), kDqWarps + kIssuers);
         }
         for (int a = 0; a < kASlots; ++a) {
@@ -285,23 +293,34 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
 
     if (warp == kWarpProd) {
         // ---------------------------------------------------------- producer
-        if (lane == 0) {
-            prefetch_tensormap(&xmap);
-            {
-                // Only L2 is warmed before the dependency wait: L2 is the
-                // point of coherence, so this stays correct even if the
-                // previous kernel writes the weights.
-                StageWalk pw(ub, nP, G, nunits);
-                for (int st = 0; st < S && pw.left > 0; ++st) {
-                    const int n = pw.size();
-                    prefetch_l2(p.wq + (size_t(pw.t) * G + pw.gbeg()) * kGroupBytes,
-                                (pw.gend(n) - pw.gbeg()) * kGroupBytes);
-                    pw.next(n);
-                }
-            }
-        }
         const uint64_t pol_w = l2_policy_evict_first();
         const uint64_t pol_x = l2_policy_evict_last();
+        auto load_weights = [&](const StageWalk &w, int n, int s) {
+            const int g0 = w.gbeg();
+            const uint32_t wbytes = (w.gend(n) - g0) * kGroupBytes;
+            mbar_arrive_expect_tx(wfull(s), wbytes);
+            bulk_load(base_s + s * L::kStage + L::kW, p.wq + (size_t(w.t) * G + g0) * kGroupBytes, wbytes, wfull(s),
+                      pol_w);
+        };
+        int w_early = 0;                         // stages whose weights went out before the wait
+        if (lane == 0) {
+            prefetch_tensormap(&xmap);
+            StageWalk pw(ub, nP, G, nunits);
+            for (int st = 0; st < S && pw.left > 0; ++st) {
+                const int n = pw.size();
+                if (p.static_w) {
+                    load_weights(pw, n, st);
+                    ++w_early;
+                } else {
+                    // Only L2 is warmed before the dependency wait: L2 is the
+                    // point of coherence, so this stays correct even if the
+                    // previous kernel writes the weights.
+                    prefetch_l2(p.wq + (size_t(pw.t) * G + pw.gbeg()) * kGroupBytes,
+                                (pw.gend(n) - pw.gbeg()) * kGroupBytes);
+                }
+                pw.next(n);
+            }
+        }
         StageWalk sw(ub, nP, G, nunits);
         int issued = 0;
         grid_dep_wait();
@@ -311,24 +330,24 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 const int n = sw.size();
                 const int s = rg.s;
                 if (rg.wrapped && !mbar_wait(empty(s), rg.ph ^ 1u, ab)) break;
-                const uint32_t sa = base_s + s * L::kStage;
-                const int g0 = sw.gbeg();
-                const uint32_t wbytes = (sw.gend(n) - g0) * kGroupBytes;
-                mbar_arrive_expect_tx(full(s), wbytes + L::kAct);
-                bulk_load(sa + L::kW, p.wq + (size_t(sw.t) * G + g0) * kGroupBytes, wbytes, full(s), pol_w);
-                tma_load_3d(sa, &xmap, 0, 0, 2 * g0, full(s), pol_x);
+                if (issued >= w_early) load_weights(sw, n, s);
+                mbar_arrive_expect_tx(xfull(s), L::kAct);
+                tma_load_3d(base_s + s * L::kStage, &xmap, 0, 0, 2 * sw.gbeg(), xfull(s), pol_x);
                 ++issued;
                 sw.next(n);
             }
             if (*ab.flag) {
                 // Let every copy still in flight land before the CTA exits.
+                const int w_issued = max(issued, w_early);
+                for (int i = max(0, w_issued - S); i < w_issued; ++i)
+                    mbar_wait_bounded(wfull(i % S), uint32_t(i / S) & 1u);
                 for (int i = max(0, issued - S); i < issued; ++i)
-                    mbar_wait_bounded(full(i % S), uint32_t(i / S) & 1u);
+                    mbar_wait_bounded(xfull(i % S), uint32_t(i / S) & 1u);
             }
         }
     } else if (warp >= kWarpIss0 && warp < kWarpIss0 + kIssuers) {
         // ------------------------------------------------------ MMA issuers
-        grid_dep_wait();
+        // (shared and tensor memory only: ordered by the stage barriers)
         if (lane == 0) {
             const int me = warp - kWarpIss0;
             constexpr uint32_t idesc = idesc_f16_f32(128, 16);
@@ -341,7 +360,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 const int s = rg.s;
                 // Every issuer waits for every stage, so its once-per-stage
                 // release below always lands in the phase of this stage.
-                if (!mbar_wait(full(s), rg.ph, ab)) break;
+                if (!mbar_wait(xfull(s), rg.ph, ab)) break;
                 for (int jj = 0; jj < n; ++jj) {
                     const int f = f0 + jj;
                     // group gg of unit f belongs to issuer (2f + gg) % 3; a
@@ -395,7 +414,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         const int r = 32 * q + lane;            // row inside the tile
         const uint32_t lane_base = uint32_t(32 * q) << 16;
         const __half2 sixteenth = __float2half2_rn(0.0625f);
-        grid_dep_wait();
+        // reads only weights, zero points and shared memory
+        if (!p.static_w) grid_dep_wait();
 
         // Zero points of this warp's 32 rows for the groups of its units,
         // kAhead groups ahead (rows past N read as 0 and are never stored).
@@ -465,7 +485,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             const int n = sw.size();
             const int s = rg.s;
             // Every dequant warp waits for every stage and releases it once.
-            if (!warp_wait(full(s), rg.ph, ab)) break;
+            if (!warp_wait(wfull(s), rg.ph, ab)) break;
             const int jj = (par - f0) & 1;       // this warp's unit in the stage, if any
             if (jj >= n) {
                 release(s);
@@ -535,7 +555,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             if (lane == 0) mbar_arrive(drain_bar);
             return warp_wait(drain_bar, (drain_syncs++) & 1, ab);
         };
-        grid_dep_wait();
+        if (!p.static_w) grid_dep_wait();
 
         // Group scales of this warp's 32 rows, kAhead groups ahead (rows past
         // N read as 0 and are never stored).
@@ -566,6 +586,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             return v;
         };
         for (int k = 0; k < kAhead; ++k) scale_issue();
+        if (p.static_w) grid_dep_wait();     // before any write of C or the workspace
 
         // Tile finished by this CTA alone: write C.  Otherwise publish the fp32
         // partial tile and count this CTA in; whether it arrived last is read
@@ -741,6 +762,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     // ----------------------------- stream-K split-tile fix-up (all threads)
     __syncthreads();
     if (CL == 0 && *ab.flag == 0u) {
+        grid_dep_wait();                      // every thread that writes C waits itself
         constexpr int kPart = 16 * NBLK * kTileN;
         constexpr int kBatch = 8;                           // contributors loaded at once
         for (int sl = 0; sl < 2; ++sl) {
@@ -903,7 +925,7 @@ size_t w4a16_decode_ws_bytes(int M, int N, int K) {
 
 w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t *scales,
                                const uint8_t *zeros, uint16_t *C, int M, int N, int K,
-                               void *ws, cudaStream_t stream) {
+                               void *ws, bool static_weights, cudaStream_t stream) {
     const DeviceInfo *info = nullptr;
     w4v_status st = device_info(&info);
     if (st != W4V_OK) return st;
@@ -925,6 +947,7 @@ w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t
     a.tile_cnt = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) +
                                               size_t(kMaxCtas) * 2 * 16 * nblk * kTileN * sizeof(float));
     a.status = info->status;
+    a.static_w = static_weights ? 1 : 0;
     CUtensorMap xmap;
     st = encode_tmap_kblocks(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, uint64_t(K), uint64_t(M), 64, 16 * nblk,
                              2 * kStageGroups, CU_TENSOR_MAP_SWIZZLE_128B);

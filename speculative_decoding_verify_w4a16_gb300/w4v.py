@@ -56,6 +56,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.w4a16_workspace_bytes.restype = S
             lib.w4a16_gemm.argtypes = [P, P, P, P, I, P, I, I, I, P, S, P]
             lib.w4a16_gemm.restype = I
+            lib.w4a16_gemm_ex.argtypes = [P, P, P, P, I, P, I, I, I, P, S, ctypes.c_uint, P]
+            lib.w4a16_gemm_ex.restype = I
             lib.w8_lmhead_argmax_workspace_bytes.argtypes = [I, I]
             lib.w8_lmhead_argmax_workspace_bytes.restype = S
             lib.w8_lmhead_argmax.argtypes = [P, P, P, I, I, I, P, P, P, P, S, P]
@@ -144,16 +146,21 @@ def workspace(nbytes: int, device="cuda"):
 
 
 # ------------------------------------------------------------------ compute --
-def w4a16_gemm(A, Bq, scales, N: int, zeros=None, out=None, ws=None, stream=None):
-    """C = A @ deq(Bq, scales, zeros)^T on the GPU.  A fp16 [M][K] cuda, Bq packed uint8 cuda."""
+STATIC_WEIGHTS = 1
+
+
+def w4a16_gemm(A, Bq, scales, N: int, zeros=None, out=None, ws=None, stream=None, static_weights=False):
+    """C = A @ deq(Bq, scales, zeros)^T on the GPU.  A fp16 [M][K] cuda, Bq packed uint8 cuda.
+    static_weights: the caller promises no GPU work still in flight writes Bq, scales or zeros
+    (w4a16_gemm_ex with W4V_STATIC_WEIGHTS)."""
     import torch
     M, K = A.shape
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=A.device)
     if ws is None:
         ws = workspace(w4a16_workspace_bytes(M, N, K), A.device)
-    code = load().w4a16_gemm(_ptr(A), _ptr(Bq), _ptr(scales), _ptr(zeros), GROUP, _ptr(out), M, N, K,
-                             _ptr(ws), ws.numel(), _stream(stream))
+    code = load().w4a16_gemm_ex(_ptr(A), _ptr(Bq), _ptr(scales), _ptr(zeros), GROUP, _ptr(out), M, N, K,
+                                _ptr(ws), ws.numel(), STATIC_WEIGHTS if static_weights else 0, _stream(stream))
     _check(code, "w4a16_gemm")
     return out
 

@@ -89,6 +89,10 @@ def test_argument_validation_before_launch(w4v_mod):
     assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 512, 256, FAKE, ws_small, None) == w4v_mod.ERR_WORKSPACE
     assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 512, 256, None, 1 << 30, None) == w4v_mod.ERR_WORKSPACE
     assert lib.w4a16_gemm(None, None, None, None, 128, None, 0, 512, 256, None, 0, None) == w4v_mod.OK   # M == 0
+    # w4a16_gemm_ex: the same checks plus unknown flag bits
+    assert lib.w4a16_gemm_ex(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 512, 256, FAKE, 1 << 30, 2, None) == w4v_mod.ERR_ARG
+    assert lib.w4a16_gemm_ex(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 500, 256, FAKE, 1 << 30, 1, None) == w4v_mod.ERR_SHAPE
+    assert lib.w4a16_gemm_ex(None, None, None, None, 128, None, 0, 512, 256, None, 0, 1, None) == w4v_mod.OK
     # w8_lmhead_argmax
     assert lib.w8_lmhead_argmax(FAKE, FAKE, FAKE, 129, 256, 1024, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
     assert lib.w8_lmhead_argmax(FAKE, FAKE, FAKE, 16, 200, 1024, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE

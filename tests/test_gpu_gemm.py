@@ -12,11 +12,12 @@ from speculative_decoding_verify_w4a16_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-def _gpu_gemm(w4v_mod, gpu, A, q, s, zeros=None, ws=None):
+def _gpu_gemm(w4v_mod, gpu, A, q, s, zeros=None, ws=None, static_weights=False):
     N = q.shape[0]
     packed = to_dev(w4v_mod.pack_int4(q), gpu)
     C = w4v_mod.w4a16_gemm(to_dev(A, gpu), packed, to_dev(s, gpu), N,
-                           zeros=None if zeros is None else to_dev(zeros, gpu), ws=ws)
+                           zeros=None if zeros is None else to_dev(zeros, gpu), ws=ws,
+                           static_weights=static_weights)
     torch.cuda.synchronize()
     return C.cpu().numpy().astype(np.float64)
 
@@ -66,6 +67,23 @@ def test_closed_forms_gpu(w4v_mod, gpu):
     q[np.arange(N), pi] = 7
     C = _gpu_gemm(w4v_mod, gpu, A, q, s)
     assert np.array_equal(C, -A.astype(np.float64)[:, pi])
+
+
+@pytest.mark.parametrize("M,N,K,zeros", [(16, 2560, 2560, False), (16, 7680, 2560, False), (16, 2560, 9728, False),
+                                         (5, 200, 384, False), (24, 400, 3200, True), (16, 19456, 2560, False)])
+def test_static_weights(w4v_mod, gpu, oracle_mod, M, N, K, zeros):
+    """With the static-weights promise the first weight stages are loaded and
+    dequantized before the previous kernel ends; the arithmetic is the same,
+    so the result equals the plain call bit for bit (both work splits)."""
+    A = inputs.activations(9, M, K, "static")
+    q = inputs.w4_codes(9, N, K, "static")
+    s = inputs.w4_scales(9, N, K, "static")
+    z = inputs.w4_zeros(9, N, K, "static") if zeros else None
+    plain = _gpu_gemm(w4v_mod, gpu, A, q, s, zeros=z)
+    early = _gpu_gemm(w4v_mod, gpu, A, q, s, zeros=z, static_weights=True)
+    assert np.array_equal(plain, early)
+    if N * K <= 2560 * 2560:
+        assert gemm_rel_err(early, oracle_mod.w4a16_gemm(A, q, s, zeros=z)) <= GEMM_TOL
 
 
 def test_batch_invariance(w4v_mod, gpu):
