@@ -93,10 +93,14 @@ constexpr int kRing = 32;                          // ring entries (> kAhead + 1
 
 constexpr int kMaxStages = 4;
 constexpr int kMaxSmem = 227 * 1024;
+// CTAs per tile.  Measured on the 4B shapes at M = 16: beyond four members
+// the leader's extra distributed-shared-memory reads cost more than the
+// shorter k range saves.
+constexpr int kMaxCluster = 4;
 
 // Shared memory: S stages, then a fixed block of barriers, rings and flags.
-// A cluster member's partial tile is left in its first stage once all its
-// MMAs have completed.
+// A cluster member's partial tile ([row][16 NBLK] fp32) is left in its first
+// stage once all its MMAs have completed.
 template <int NBLK>
 struct Layout {
     static constexpr int kRows = 16 * NBLK;                    // activation rows per box
@@ -597,37 +601,46 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             const int n = t * kTileN + r;
             if (CL > 1) {
                 if (crank != 0) {
-                    // member: partial tile [m][128] into its own first stage
-                    // (every MMA of this CTA has completed), then arrive on
-                    // the leader's barrier
+                    // member: partial tile [row][16 NBLK] into its own first
+                    // stage (every MMA of this CTA has completed), then arrive
+                    // on the leader's barrier
+                    const uint32_t dst = base_s + uint32_t(r) * (16 * NBLK * 4);
 #pragma unroll
                     for (int b = 0; b < NBLK; ++b)
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int m = 16 * b + j;
-                            if (m < p.M) sts_f32(base_s + uint32_t(m * kTileN + r) * 4u, acc[b][j]);
-                        }
+                        for (int j = 0; j < 16; j += 4)
+                            sts_f32x4(dst + (16 * b + j) * 4, acc[b][j], acc[b][j + 1], acc[b][j + 2], acc[b][j + 3]);
                     __syncwarp();
                     if (lane == 0) mbar_arrive_remote(mapa_shared(red_bar, 0u));
                     return true;
                 }
-                // leader: own partial first, then the members' in rank order
+                // leader: own partial first, then the members' in rank order;
+                // all members' rows are loaded at once (one remote round trip)
                 if (!mbar_wait_cluster(red_bar, 0, ab)) return false;
-                for (int k = 1; k < CL; ++k) {
-                    float v[NBLK][16];
+                const uint32_t src = base_s + uint32_t(r) * (16 * NBLK * 4);
+                constexpr int kBatch = NBLK == 1 ? kMaxCluster - 1 : 1;
+                for (int k0 = 1; k0 < CL; k0 += kBatch) {
+                    float4 v[kBatch][4 * NBLK];
 #pragma unroll
-                    for (int b = 0; b < NBLK; ++b)
+                    for (int u = 0; u < kBatch; ++u)
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int m = 16 * b + j;
-                            v[b][j] = m < p.M ? ld_cluster_f32(mapa_shared(base_s + uint32_t(m * kTileN + r) * 4u,
-                                                                           uint32_t(k)))
-                                              : 0.f;
+                        for (int i = 0; i < 4 * NBLK; ++i)
+                            v[u][i] = k0 + u < CL ? ld_cluster_f32x4(mapa_shared(src + 16 * i, uint32_t(k0 + u)))
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int u = 0; u < kBatch; ++u)
+                        if (k0 + u < CL) {
+#pragma unroll
+                            for (int b = 0; b < NBLK; ++b)
+#pragma unroll
+                                for (int j = 0; j < 16; j += 4) {
+                                    const float4 w = v[u][(16 * b + j) / 4];
+                                    acc[b][j] += w.x;
+                                    acc[b][j + 1] += w.y;
+                                    acc[b][j + 2] += w.z;
+                                    acc[b][j + 3] += w.w;
+                                }
                         }
-#pragma unroll
-                    for (int b = 0; b < NBLK; ++b)
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) acc[b][j] += v[b][j];
                 }
                 if (n < p.N) {
 #pragma unroll
@@ -820,10 +833,6 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     }
 }
 
-// CTAs per tile.  Measured on the 4B shapes at M = 16: beyond four members
-// the leader's extra distributed-shared-memory reads cost more than the
-// shorter k range saves.
-constexpr int kMaxCluster = 4;
 // A stream-K fix-up (counter round trip plus one round of partial loads)
 // costs about as much as this many units of work.
 constexpr int kFixupUnits = 2;
