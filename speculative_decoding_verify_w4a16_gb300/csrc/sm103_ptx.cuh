@@ -72,10 +72,17 @@ __device__ __forceinline__ void raise_abort(const AbortState &ab) {
     atomicOr(ab.status, 1u << kStatusTimeout);
 }
 
-// Slow path of mbar_wait.  (Kept inline: as a real call it cost the prefill
-// kernel 8% of its throughput.)
-__device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t *flag,
-                                            uint32_t *status) {
+// Slow path of mbar_wait.  A translation unit that defines
+// W4V_COMPACT_WAITS before including this header gets it as an out-of-line
+// call: that keeps a kernel with many wait sites small in the instruction
+// cache (the decode GEMM gains ~5%), while the prefill kernel loses 8% to the
+// call and keeps it inline.
+#ifdef W4V_COMPACT_WAITS
+#define W4V_SLOW_WAIT static __device__ __noinline__
+#else
+#define W4V_SLOW_WAIT __device__ __forceinline__
+#endif
+W4V_SLOW_WAIT bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t *flag, uint32_t *status) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;

@@ -64,6 +64,7 @@
 #include <mutex>
 
 #include "runtime.h"
+#define W4V_COMPACT_WAITS 1
 #include "sm103_ptx.cuh"
 
 namespace w4v {
