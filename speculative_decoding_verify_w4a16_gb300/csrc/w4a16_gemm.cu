@@ -43,11 +43,12 @@
 //     into a shared-memory ring.
 //   * Work split.  With few 128-row tiles, each tile belongs to a
 //     thread-block cluster of C CTAs (C up to 4, as many as fit one wave)
-//     that split its k range; each member leaves its fp32 partial tile in
-//     its own shared memory and the cluster's first CTA reads them through
-//     distributed shared memory, adds them in rank order and writes C: no
-//     global round trip, which on this two-die part costs well over a
-//     microsecond each.  With at least
+//     that split its k range; each CTA leaves its fp32 partial tile in its
+//     own shared memory, and after one cluster barrier every CTA finishes
+//     1/C of the tile's rows, reading the others' partials through
+//     distributed shared memory and adding them in rank order: no global
+//     round trip (well over a microsecond each on this two-die part), and
+//     the remote reads are spread over the whole cluster.  With at least
 //     as many tiles as SMs, the flat list of units is split evenly over one
 //     CTA per SM (stream-K); a tile shared by several CTAs is finished by the
 //     last one to arrive (acquire-release counter, no waiting between CTAs),
@@ -100,8 +101,8 @@ constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMaxCluster = 4;
 
 // Shared memory: S stages, then a fixed block of barriers, rings and flags.
-// A cluster member's partial tile ([row][16 NBLK] fp32) is left in its first
-// stage once all its MMAs have completed.
+// In cluster mode each CTA's partial tile ([row][16 NBLK] fp32) is left in
+// its first stage once all its MMAs have completed.
 template <int NBLK>
 struct Layout {
     static constexpr int kRows = 16 * NBLK;                    // activation rows per box
@@ -112,8 +113,8 @@ struct Layout {
     static constexpr uint32_t kDUnit = kUnitGroups * 16 * NBLK;   // accumulator columns per unit
     static constexpr int kDSets = int((kTmemCols - kDcol0) / kDUnit);
     // wfull, xfull, empty per stage (room for kMaxStages); afull, aempty per A slot;
-    // dfull, dempty per set; done; drain sync; cluster reduction
-    static constexpr int kNumBars = 3 * kMaxStages + 2 * kASlots + 2 * kDSets + 3;
+    // dfull, dempty per set; done; drain sync
+    static constexpr int kNumBars = 3 * kMaxStages + 2 * kASlots + 2 * kDSets + 2;
     static constexpr int kBarBytes = (8 * kNumBars + 127) & ~127;
     static constexpr int kScl = kBarBytes;                         // offsets inside the fixed block
     static constexpr int kZro = kScl + kDrWarps * kRing * 64;      // 32 fp16 scales per entry
@@ -239,7 +240,6 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     auto dempty = [&](int b) { return bar0 + 8u * (3 * MS + 2 * kASlots + DS + b); };
     const uint32_t done_bar = bar0 + 8u * (3 * MS + 2 * kASlots + 2 * DS);
     const uint32_t drain_bar = done_bar + 8u;
-    const uint32_t red_bar = drain_bar + 8u;
     // [0] tmem base, [1] abort flag, [2..3] pending tile + 1 per slot, [4..5] last-arriver flags
     uint32_t *misc = reinterpret_cast<uint32_t *>(base + fixed_off + L::kMisc);
 
@@ -279,7 +279,6 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         }
         mbar_init(done_bar, kIssuers);
         mbar_init(drain_bar, kDrWarps);
-        mbar_init(red_bar, CL > 1 ? (CL - 1) * kDrWarps : 1);
         for (int k = 1; k < 16; ++k) misc[k] = 0;
         fence_barrier_init();
     }
@@ -601,57 +600,15 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             const long long t1u = t0u + nP;
             const int n = t * kTileN + r;
             if (CL > 1) {
-                if (crank != 0) {
-                    // member: partial tile [row][16 NBLK] into its own first
-                    // stage (every MMA of this CTA has completed), then arrive
-                    // on the leader's barrier
-                    const uint32_t dst = base_s + uint32_t(r) * (16 * NBLK * 4);
+                // cluster: partial tile [row][16 NBLK] into this CTA's first
+                // stage (every MMA of this CTA has completed); the cluster
+                // adds the partials after the role loops
+                const uint32_t dst = base_s + uint32_t(r) * (16 * NBLK * 4);
 #pragma unroll
-                    for (int b = 0; b < NBLK; ++b)
+                for (int b = 0; b < NBLK; ++b)
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4)
-                            sts_f32x4(dst + (16 * b + j) * 4, acc[b][j], acc[b][j + 1], acc[b][j + 2], acc[b][j + 3]);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_remote(mapa_shared(red_bar, 0u));
-                    return true;
-                }
-                // leader: own partial first, then the members' in rank order;
-                // all members' rows are loaded at once (one remote round trip)
-                if (!mbar_wait_cluster(red_bar, 0, ab)) return false;
-                const uint32_t src = base_s + uint32_t(r) * (16 * NBLK * 4);
-                constexpr int kBatch = NBLK == 1 ? kMaxCluster - 1 : 1;
-                for (int k0 = 1; k0 < CL; k0 += kBatch) {
-                    float4 v[kBatch][4 * NBLK];
-#pragma unroll
-                    for (int u = 0; u < kBatch; ++u)
-#pragma unroll
-                        for (int i = 0; i < 4 * NBLK; ++i)
-                            v[u][i] = k0 + u < CL ? ld_cluster_f32x4(mapa_shared(src + 16 * i, uint32_t(k0 + u)))
-                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int u = 0; u < kBatch; ++u)
-                        if (k0 + u < CL) {
-#pragma unroll
-                            for (int b = 0; b < NBLK; ++b)
-#pragma unroll
-                                for (int j = 0; j < 16; j += 4) {
-                                    const float4 w = v[u][(16 * b + j) / 4];
-                                    acc[b][j] += w.x;
-                                    acc[b][j + 1] += w.y;
-                                    acc[b][j + 2] += w.z;
-                                    acc[b][j + 3] += w.w;
-                                }
-                        }
-                }
-                if (n < p.N) {
-#pragma unroll
-                    for (int b = 0; b < NBLK; ++b)
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int m = 16 * b + j;
-                            if (m < p.M) p.C[size_t(m) * p.N + n] = __float2half_rn(acc[b][j]);
-                        }
-                }
+                    for (int j = 0; j < 16; j += 4)
+                        sts_f32x4(dst + (16 * b + j) * 4, acc[b][j], acc[b][j + 1], acc[b][j + 2], acc[b][j + 3]);
                 return true;
             }
             if (ub <= t0u && t1u <= ue) {
@@ -773,8 +730,46 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         if (ok) mark_last();
     }
 
-    // ----------------------------- stream-K split-tile fix-up (all threads)
     __syncthreads();
+    if (CL > 1) {
+        // -------------------- cluster reduction: each CTA finishes 1/CL of the rows
+        cluster_sync_all();                       // every CTA's partial is in its shared memory
+        if (*ab.flag == 0u) {
+            grid_dep_wait();                      // every thread that writes C waits itself
+            const int t = cta / CL;
+            const int r0 = crank * kTileN / CL, r1 = (crank + 1) * kTileN / CL;
+            const int nrows = r1 - r0;
+            for (int item = threadIdx.x; item < nrows * 4 * NBLK; item += kThreads) {
+                const int m4 = item / nrows, row = r0 + item % nrows;   // consecutive threads: consecutive rows
+                const uint32_t off = base_s + uint32_t(row) * (16 * NBLK * 4) + uint32_t(m4) * 16;
+                float4 v[kMaxCluster];
+#pragma unroll
+                for (int k = 0; k < kMaxCluster; ++k)
+                    if (k < CL) v[k] = k == crank ? ld_shared_f32x4(off) : ld_cluster_f32x4(mapa_shared(off, uint32_t(k)));
+                float4 sum = v[0];                 // ranks in order: the k range in order
+#pragma unroll
+                for (int k = 1; k < kMaxCluster; ++k)
+                    if (k < CL) {
+                        sum.x += v[k].x;
+                        sum.y += v[k].y;
+                        sum.z += v[k].z;
+                        sum.w += v[k].w;
+                    }
+                const int n = t * kTileN + row;
+                if (n < p.N) {
+                    const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int m = 4 * m4 + i;
+                        if (m < p.M) p.C[size_t(m) * p.N + n] = __float2half_rn(sv[i]);
+                    }
+                }
+            }
+        }
+        cluster_sync_all();                       // nobody leaves while another CTA reads its partial
+    }
+
+    // ----------------------------- stream-K split-tile fix-up (all threads)
     if (CL == 0 && *ab.flag == 0u) {
         grid_dep_wait();                      // every thread that writes C waits itself
         constexpr int kPart = 16 * NBLK * kTileN;
@@ -824,8 +819,6 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         }
     }
 
-    // a member's partial tile is read by the leader: nobody leaves before it has
-    if (CL > 1) cluster_sync_all();
     tc_fence_before();
     __syncthreads();
     if (warp == kWarpIss0) {
