@@ -42,7 +42,8 @@
 //     each warp keeps the next 16 groups' values in flight with cp.async
 //     into a shared-memory ring.
 //   * Work split.  With few 128-row tiles, each tile belongs to a
-//     thread-block cluster of C CTAs (C up to 4, as many as fit one wave)
+//     thread-block cluster of C CTAs (C about the square root of the units
+//     per tile, at most 8, all clusters in one wave)
 //     that split its k range; each CTA leaves its fp32 partial tile in its
 //     own shared memory, and after one cluster barrier every CTA finishes
 //     1/C of the tile's rows, reading the others' partials through
@@ -95,10 +96,10 @@ constexpr int kRing = 32;                          // ring entries (> kAhead + 1
 
 constexpr int kMaxStages = 4;
 constexpr int kMaxSmem = 227 * 1024;
-// CTAs per tile.  Measured on the 4B shapes at M = 16: beyond four members
-// the leader's extra distributed-shared-memory reads cost more than the
-// shorter k range saves.
-constexpr int kMaxCluster = 4;
+// Largest cluster (portable size).  Measured on the 4B shapes at M = 16, each
+// extra member costs about as much as one more unit per CTA, so the cluster
+// size chosen is about the square root of the units per tile.
+constexpr int kMaxCluster = 8;
 
 // Shared memory: S stages, then a fixed block of barriers, rings and flags.
 // In cluster mode each CTA's partial tile ([row][16 NBLK] fp32) is left in
@@ -840,7 +841,10 @@ int pick_cluster(int n_tiles, int n_pairs, int sm_count) {
     if (n_tiles * 2 > sm_count) return 0;
     const long long units = (long long)n_tiles * n_pairs;
     const long long streamk_share = (units + sm_count - 1) / sm_count;
-    int c = std::min(kMaxCluster, std::min(n_pairs, sm_count / n_tiles));
+    int root = 1;
+    while ((root + 1) * (root + 1) <= n_pairs) ++root;
+    if (root * (root + 1) < n_pairs) ++root;          // nearest integer to sqrt(n_pairs)
+    int c = std::min(std::min(kMaxCluster, std::max(2, root)), std::min(n_pairs, sm_count / n_tiles));
     if ((n_pairs + c - 1) / c > streamk_share + kFixupUnits) return 0;
     for (; c >= 2; --c) {
         // one CTA per SM for either variant; the larger one's query bounds both
