@@ -53,3 +53,19 @@ def test_reference_arm_only_on_rank0():
                         "--steps", "1", "--warmup", "3"], env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_profiled_traffic_needs_matching_sources(tmp_path):
+    """The roofline's DRAM traffic comes from a committed ncu summary and is
+    used only while the summary names the fingerprint of the sources being
+    built; otherwise it is null."""
+    sys.path.insert(0, ROOT)
+    import bench
+    sha = bench.kernel_source_sha(bench.LM_HEAD_SOURCES)
+    good = tmp_path / "good.md"
+    good.write_text("# summary\nsource_sha256: %s\ndram_bytes_read: 389400320\ndram_bytes_write: 2908160\n" % sha)
+    assert bench.profiled_traffic(str(good), bench.LM_HEAD_SOURCES) == 389400320 + 2908160
+    stale = tmp_path / "stale.md"
+    stale.write_text("source_sha256: 0000000000000000\ndram_bytes_read: 1\ndram_bytes_write: 2\n")
+    assert bench.profiled_traffic(str(stale), bench.LM_HEAD_SOURCES) is None
+    assert bench.profiled_traffic(str(tmp_path / "missing.md"), bench.LM_HEAD_SOURCES) is None
