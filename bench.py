@@ -5,7 +5,8 @@ Workload (the 4B-shaped verify step at M = 16, i.e. K = 15 drafts + 1): the
 four W4A16 g128 projections of one decoder layer set (qkv 2560->7680,
 o 2560->2560, gate_up 2560->19456, down 9728->2560), the int8 lm_head
 2560->151936 with fused greedy argmax, and longest-prefix acceptance of 15
-seeded drafts.  One step = all of it once, captured as one CUDA graph.
+seeded drafts (run by the lm_head's last CTA, in the same launch).  One step
+= all of it once, captured as one CUDA graph.
 
 value      = algorithmic input bytes per step (packed int4 + fp16 group
              scales + fp16 activations, int8 lm_head + row scales + its
@@ -146,7 +147,7 @@ class VerifyStep:
         self.draft = t(d)
         self.n_acc = torch.empty(1, dtype=torch.int32, device=dev)
         self.out_tok = torch.empty((1, K_DRAFT + 1), dtype=torch.int32, device=dev)
-        self.launches_per_step = len(inputs.LAYER_PROJS) + 2
+        self.launches_per_step = len(inputs.LAYER_PROJS) + 1
 
     def enqueue(self, copy):
         w4v = self.w4v
@@ -154,10 +155,11 @@ class VerifyStep:
             w4v.w4a16_gemm(self.acts[p.name], packed, s, p.N, out=self.outs[p.name], ws=self.ws[p.name],
                            static_weights=True)
         self.lm_head()
-        w4v.spec_accept(self.tok.view(1, M_VERIFY), self.draft, n_out=self.n_acc, tok_out=self.out_tok)
 
     def lm_head(self):
-        self.w4v.w8_lmhead_argmax(self.X, self.W8, self.s8, out=self.tok, ws=self.ws_lm)
+        """lm_head argmax and acceptance of the drafts, one launch."""
+        self.w4v.w8_lmhead_argmax_accept(self.X, self.W8, self.s8, self.draft, out=self.tok, n_out=self.n_acc,
+                                         tok_out=self.out_tok, ws=self.ws_lm)
 
 
 def capture(torch, fn):
@@ -294,7 +296,8 @@ def run_gpu(args, rank, world):
                    "graph": "one CUDA graph per step", "parallelism": "replicas" if world > 1 else "1 GPU",
                    "weights": "static (W4V_STATIC_WEIGHTS: projection weights may be loaded before the previous "
                               "kernel ends; inputs and outputs wait for it)"},
-        "roofline": {"bound": "hbm", "kernel": "w8_lmhead_argmax (M=16, V=151936, K=2560), %d launches "
+        "roofline": {"bound": "hbm", "kernel": "w8_lmhead_argmax_accept (M=16, V=151936, K=2560, 15 drafts), "
+                               "%d launches "
                                "in one graph, CUDA events on the launching stream" % reps,
                      "achieved": round(lm["GB/s"], 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(lm["frac"], 4),
@@ -312,6 +315,7 @@ def run_gpu(args, rank, world):
     }
     if args.sweep:
         result["sweep"] = stack.sweep(peaks)
+        result["verify_36_layers"] = stack.full_verify(step.W8, step.s8, peaks)
     del stack
     torch.cuda.empty_cache()
     if args.prefill:
@@ -445,6 +449,40 @@ class Stack:
                                "launches": 4 * self.LAYERS}
         return out
 
+    def full_verify(self, W8, s8, peaks):
+        """The whole 36-layer verify step as one CUDA graph: every projection of
+        every layer, then the lm_head argmax with acceptance of M-1 drafts in one
+        launch (M = 16: K = 15; M = 21: K = 20 with seeded -1 padding)."""
+        torch, w4v = self.torch, self.w4v
+        H, V = inputs.H_4B, inputs.V_4B
+        out = {}
+        for M in (16, 21):
+            acts, outs, wss = self._buffers(M)
+            X = torch.randn((M, H), generator=self.g, device=self.dev).half()
+            d = inputs.rng(SEED, "stack-drafts", M).integers(0, V, size=(1, M - 1)).astype(np.int32)
+            if M == 21:
+                d[0, 12:] = -1
+            d = torch.from_numpy(d).to(self.dev)
+            tok = torch.empty(M, dtype=torch.int32, device=self.dev)
+            n = torch.empty(1, dtype=torch.int32, device=self.dev)
+            o = torch.empty((1, M), dtype=torch.int32, device=self.dev)
+            ws = w4v.workspace(w4v.w8_lmhead_argmax_workspace_bytes(M, V), self.dev)
+
+            def run():
+                for lay in self.layers:
+                    for (p, packed, sc) in lay:
+                        w4v.w4a16_gemm(acts[p.name], packed, sc, p.N, out=outs[p.name], ws=wss[p.name],
+                                       static_weights=True)
+                w4v.w8_lmhead_argmax_accept(X, W8, s8, d, out=tok, n_out=n, tok_out=o, ws=ws)
+
+            ms = time_graph(torch, run)
+            b = self.LAYERS * sum(p.N * p.K // 2 + (p.K // 128) * p.N * 2 + M * p.K * 2 for p in inputs.LAYER_PROJS)
+            b += V * H + 2 * V + 2 * M * H
+            gbs = b / (ms * 1e-3) / 1e9
+            out["M=%d" % M] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
+                               "launches": 4 * self.LAYERS + 1, "K_draft": M - 1}
+        return out
+
 
 def run_prefill(dev, w4v, torch, peaks):
     """The layer set at prefill sizes (M = 2048 and 8192): tensor-bound."""
@@ -498,8 +536,7 @@ def run_lmhead_batched(dev, w4v, torch, peaks):
         o = torch.empty((B, K1), dtype=torch.int32, device=dev)
 
         def step():
-            w4v.w8_lmhead_argmax(X, Wd, sd, out=tok, ws=ws)
-            w4v.spec_accept(tok.view(B, K1), d, n_out=n, tok_out=o)
+            w4v.w8_lmhead_argmax_accept(X, Wd, sd, d, out=tok, n_out=n, tok_out=o, ws=ws)
 
         ms = time_graph(torch, lambda: [step() for _ in range(10)]) / 10
         b = V * H + 2 * V + 2 * M * H
@@ -591,7 +628,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")

@@ -191,6 +191,27 @@ w4v_status w8_lmhead_argmax_noalloc(const uint16_t *X, const int8_t *W, const ui
 w4v_status spec_accept(const int32_t *target, const int32_t *draft, int B, int K,
                        int32_t *n_accepted, int32_t *out_tokens, w4v_stream_t stream);
 
+/* ----------------------------------------------- w8_lmhead_argmax_accept
+ * The last two operations of a verify step in one launch: the int8 lm_head
+ * argmax of w8_lmhead_argmax over M = B*(n_draft+1) rows, then the greedy
+ * acceptance of spec_accept with target = those tokens viewed as
+ * [B][n_draft+1] (row b*(n_draft+1)+j is position j of verify block b).
+ * Results are identical to w8_lmhead_argmax followed by spec_accept; the
+ * acceptance runs in the lm_head's last CTA, on the tokens it has just
+ * written, so no second launch or dependency is needed.
+ *   X, W, scale, argmax_out, maxlogit, workspace: as w8_lmhead_argmax
+ *   draft       device, int32 [B][n_draft] (may be NULL when n_draft == 0)
+ *   n_accepted  device, int32 [B]
+ *   out_tokens  device, int32 [B][n_draft+1] or NULL (as spec_accept)
+ * Sizes: B >= 0 (0 is a no-op), n_draft >= 0, B*(n_draft+1) <= 128,
+ * K % 128 == 0, V % 8 == 0, V > 0.  Workspace: w8_lmhead_argmax_workspace_bytes
+ * for M = B*(n_draft+1). */
+w4v_status w8_lmhead_argmax_accept(const uint16_t *X, const int8_t *W, const uint16_t *scale,
+                                   int B, int n_draft, int K, int V, const int32_t *draft,
+                                   int32_t *argmax_out, int32_t *n_accepted, int32_t *out_tokens,
+                                   float *maxlogit, void *workspace, size_t workspace_bytes,
+                                   w4v_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

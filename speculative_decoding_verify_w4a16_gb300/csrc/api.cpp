@@ -142,6 +142,29 @@ w4v_status w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uint16_t *
                                         reinterpret_cast<cudaStream_t>(stream));
 }
 
+w4v_status w8_lmhead_argmax_accept(const uint16_t *X, const int8_t *W, const uint16_t *scale, int B, int n_draft,
+                                   int K, int V, const int32_t *draft, int32_t *argmax_out, int32_t *n_accepted,
+                                   int32_t *out_tokens, float *maxlogit, void *ws, size_t ws_bytes,
+                                   w4v_stream_t stream) {
+    if (B < 0 || n_draft < 0 || K <= 0 || V <= 0 || K % 128 != 0 || V % 8 != 0) return W4V_ERR_SHAPE;
+    if (B > 128 || long(B) * (n_draft + 1) > 128) return W4V_ERR_SHAPE;
+    if (B == 0) return W4V_OK;
+    const int M = B * (n_draft + 1);
+    if (X == nullptr || W == nullptr || scale == nullptr || argmax_out == nullptr || n_accepted == nullptr ||
+        (n_draft > 0 && draft == nullptr))
+        return W4V_ERR_ARG;
+    if (!w4v::aligned16(X) || !w4v::aligned16(W) || !w4v::aligned16(scale)) return W4V_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(argmax_out) & 3u) || (reinterpret_cast<uintptr_t>(maxlogit) & 3u) ||
+        (reinterpret_cast<uintptr_t>(draft) & 3u) || (reinterpret_cast<uintptr_t>(n_accepted) & 3u) ||
+        (reinterpret_cast<uintptr_t>(out_tokens) & 3u))
+        return W4V_ERR_ALIGN;
+    if (ws == nullptr || ws_bytes < w4v::w8_lmhead_ws_bytes(M, V)) return W4V_ERR_WORKSPACE;
+    if (!w4v::aligned16(ws)) return W4V_ERR_ALIGN;
+    const w4v::LmAccept acc{draft, B, n_draft, n_accepted, out_tokens};
+    return w4v::launch_w8_lmhead_argmax(X, W, scale, M, K, V, argmax_out, maxlogit, nullptr, ws,
+                                        reinterpret_cast<cudaStream_t>(stream), &acc);
+}
+
 w4v_status spec_accept(const int32_t *target, const int32_t *draft, int B, int K, int32_t *n_accepted,
                        int32_t *out_tokens, w4v_stream_t stream) {
     if (B < 0 || K < 0 || K > 1024) return W4V_ERR_SHAPE;

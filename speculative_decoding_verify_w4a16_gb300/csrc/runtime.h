@@ -97,9 +97,18 @@ w4v_status launch_w4a16_prefill(const uint16_t *A, const void *Bq, const uint16_
 // Rows up to which the verify-sized (HBM-bound) kernel is used.
 constexpr int kDecodeMaxRows = 32;
 
+// Greedy acceptance fused into the lm_head's last CTA: the M = B*(n_draft+1)
+// rows are B verify blocks of n_draft+1 positions each.
+struct LmAccept {
+    const int32_t *draft;      // [B][n_draft]
+    int B, n_draft;
+    int32_t *n_accepted;       // [B]
+    int32_t *out_tokens;       // [B][n_draft+1] or null
+};
 w4v_status launch_w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uint16_t *scale,
                                    int M, int K, int V, int32_t *argmax_out, float *maxlogit,
-                                   float *logits, void *ws, cudaStream_t stream);
+                                   float *logits, void *ws, cudaStream_t stream,
+                                   const LmAccept *accept = nullptr);
 size_t w8_lmhead_ws_bytes(int M, int V);
 
 w4v_status launch_spec_accept(const int32_t *target, const int32_t *draft, int B, int K,

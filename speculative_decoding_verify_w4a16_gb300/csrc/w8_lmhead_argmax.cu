@@ -36,7 +36,10 @@
 //     keeps the CTA's best per row.
 //   * Each CTA folds its best keys into one global 64-bit atomicMax per row;
 //     the last CTA to arrive (acquire-release counter, no waiting) reads and
-//     clears them and writes the token ids.
+//     clears them and writes the token ids.  When the rows are verify blocks
+//     with drafts attached, that CTA also runs the greedy acceptance on the
+//     tokens it just wrote (one warp per block, from shared memory), so the
+//     verify step's last two operations are one launch.
 //   * Launched with programmatic stream serialization: set-up and an L2
 //     prefetch of the first weight stages overlap the previous kernel's end.
 #include "runtime.h"
@@ -112,6 +115,10 @@ struct Args {
     unsigned long long *keys;   // [128], zero between calls
     uint32_t *counter;
     uint32_t *status;
+    const int32_t *draft;       // acceptance epilogue (B > 0): drafts [B][n_draft]
+    int32_t *n_accepted;
+    int32_t *out_tokens;
+    int B, n_draft;
     int M, K, V;
     int n_tiles, n_chunks;
     int P;
@@ -444,10 +451,45 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
             }
             ok = drain_sync();
         }
-        if (ok && misc[2] && tid < p.M) {
-            const unsigned long long k = atomicExch(p.keys + tid, 0ull);
-            p.argmax_out[tid] = static_cast<int32_t>(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFull));
-            if (p.maxlogit != nullptr) p.maxlogit[tid] = key_logit(uint32_t(k >> 32));
+        if (ok && misc[2]) {
+            // The CTA's own best keys are folded already: their shared array
+            // now holds the finished tokens for the acceptance epilogue.
+            int32_t *tok_s = reinterpret_cast<int32_t *>(best);
+            if (tid < p.M) {
+                const unsigned long long k = atomicExch(p.keys + tid, 0ull);
+                const int32_t t = static_cast<int32_t>(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFull));
+                p.argmax_out[tid] = t;
+                tok_s[tid] = t;
+                if (p.maxlogit != nullptr) p.maxlogit[tid] = key_logit(uint32_t(k >> 32));
+            }
+            // Greedy acceptance ("Efficient LLM Challenge Results", section 3):
+            // rows b*(n+1) .. b*(n+1)+n are verify block b; keep the longest
+            // draft prefix equal to the target's tokens, a negative draft (the
+            // -1 sentinel) never matching.  One drain warp per block.
+            if (p.B > 0 && drain_sync()) {
+                const int nd = p.n_draft;
+                for (int b = dr; b < p.B; b += kDrWarps) {
+                    const int32_t *t = tok_s + b * (nd + 1);
+                    const int32_t *d = p.draft + size_t(b) * nd;
+                    int n = nd;
+                    for (int j0 = 0; j0 < nd; j0 += 32) {
+                        const int j = j0 + lane;
+                        bool miss = false;
+                        if (j < nd) {
+                            const int32_t dj = d[j];
+                            miss = !(dj >= 0 && dj == t[j]);
+                        }
+                        const unsigned m = __ballot_sync(0xFFFFFFFFu, miss);
+                        if (m != 0u) {
+                            n = j0 + __ffs(m) - 1;
+                            break;
+                        }
+                    }
+                    if (lane == 0) p.n_accepted[b] = n;
+                    if (p.out_tokens != nullptr)
+                        for (int j = lane; j <= nd; j += 32) p.out_tokens[size_t(b) * (nd + 1) + j] = j <= n ? t[j] : -1;
+                }
+            }
         }
     }
 
@@ -491,7 +533,7 @@ size_t w8_lmhead_ws_bytes(int M, int V) {
 
 w4v_status launch_w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uint16_t *scale,
                                    int M, int K, int V, int32_t *argmax_out, float *maxlogit,
-                                   float *logits, void *ws, cudaStream_t stream) {
+                                   float *logits, void *ws, cudaStream_t stream, const LmAccept *accept) {
     const DeviceInfo *info = nullptr;
     w4v_status st = device_info(&info);
     if (st != W4V_OK) return st;
@@ -506,6 +548,11 @@ w4v_status launch_w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uin
     a.keys = static_cast<unsigned long long *>(ws);
     a.counter = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + size_t(kMaxRows) * sizeof(unsigned long long));
     a.status = info->status;
+    a.draft = accept != nullptr ? accept->draft : nullptr;
+    a.n_accepted = accept != nullptr ? accept->n_accepted : nullptr;
+    a.out_tokens = accept != nullptr ? accept->out_tokens : nullptr;
+    a.B = accept != nullptr ? accept->B : 0;
+    a.n_draft = accept != nullptr ? accept->n_draft : 0;
     a.M = M;
     a.K = K;
     a.V = V;

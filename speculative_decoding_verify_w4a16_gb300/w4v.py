@@ -64,6 +64,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.w8_lmhead_argmax.restype = I
             lib.spec_accept.argtypes = [P, P, I, I, P, P, P]
             lib.spec_accept.restype = I
+            lib.w8_lmhead_argmax_accept.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, S, P]
+            lib.w8_lmhead_argmax_accept.restype = I
             _lib = lib
     return _lib
 
@@ -193,3 +195,28 @@ def spec_accept(target, draft, n_out=None, tok_out=None, stream=None):
                               _ptr(tok_out), _stream(stream))
     _check(code, "spec_accept")
     return n_out, tok_out
+
+
+def w8_lmhead_argmax_accept(X, W, scale, draft, out=None, n_out=None, tok_out=None, maxlogit=None, ws=None,
+                            stream=None):
+    """lm_head argmax of the B*(n+1) rows of X and greedy acceptance of drafts [B][n] in one launch.
+    Returns (tokens [B*(n+1)], n_accepted [B], emitted tokens [B][n+1])."""
+    import torch
+    M, K = X.shape
+    V = W.shape[0]
+    B, nd = draft.shape
+    if out is None:
+        out = torch.empty(M, dtype=torch.int32, device=X.device)
+    if n_out is None:
+        n_out = torch.empty(B, dtype=torch.int32, device=X.device)
+    if tok_out is None:
+        tok_out = torch.empty((B, nd + 1), dtype=torch.int32, device=X.device)
+    if M != B * (nd + 1):
+        raise W4VError(ERR_SHAPE, "w8_lmhead_argmax_accept")
+    if ws is None:
+        ws = workspace(w8_lmhead_argmax_workspace_bytes(M, V), X.device)
+    code = load().w8_lmhead_argmax_accept(_ptr(X), _ptr(W), _ptr(scale), B, nd, K, V,
+                                          _ptr(draft) if nd > 0 else None, _ptr(out), _ptr(n_out),
+                                          _ptr(tok_out), _ptr(maxlogit), _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "w8_lmhead_argmax_accept")
+    return out, n_out, tok_out

@@ -14,7 +14,7 @@ FAKE = 0x10000          # an aligned, never-dereferenced stand-in pointer
 def test_exports_every_header_function(w4v_mod):
     names = w4v_mod.header_functions()
     for required in ("w4v_init", "w4v_get_status", "w4v_pack_int4", "w4a16_gemm",
-                     "w8_lmhead_argmax", "spec_accept"):
+                     "w8_lmhead_argmax", "spec_accept", "w8_lmhead_argmax_accept"):
         assert required in names
     lib = w4v_mod.load()
     for name in names:
@@ -108,6 +108,17 @@ def test_argument_validation_before_launch(w4v_mod):
     assert lib.spec_accept(FAKE, None, 4, 4, FAKE, None, None) == w4v_mod.ERR_ARG
     assert lib.spec_accept(FAKE + 1, FAKE, 4, 4, FAKE, None, None) == w4v_mod.ERR_ALIGN
     assert lib.spec_accept(None, None, 0, 4, None, None, None) == w4v_mod.OK
+    # w8_lmhead_argmax_accept: B*(n_draft+1) rows, at most 128
+    acc = lib.w8_lmhead_argmax_accept
+    assert acc(FAKE, FAKE, FAKE, 8, 16, 256, 1024, FAKE, FAKE, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert acc(FAKE, FAKE, FAKE, 129, 0, 256, 1024, FAKE, FAKE, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert acc(FAKE, FAKE, FAKE, 1, -1, 256, 1024, FAKE, FAKE, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert acc(FAKE, FAKE, FAKE, 1, 15, 200, 1024, FAKE, FAKE, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert acc(FAKE, FAKE, FAKE, 1, 15, 256, 1024, None, FAKE, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_ARG
+    assert acc(FAKE, FAKE, FAKE, 1, 15, 256, 1024, FAKE, FAKE, None, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_ARG
+    assert acc(FAKE, FAKE, FAKE, 1, 15, 256, 1024, FAKE + 2, FAKE, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_ALIGN
+    assert acc(FAKE, FAKE, FAKE, 1, 15, 256, 1024, FAKE, FAKE, FAKE, None, None, FAKE, ws_small, None) == w4v_mod.ERR_WORKSPACE
+    assert acc(None, None, None, 0, 15, 256, 1024, None, None, None, None, None, None, 0, None) == w4v_mod.OK
     # packer
     assert lib.w4v_pack_int4(None, 128, 128, FAKE) == w4v_mod.ERR_ARG
     buf = ctypes.create_string_buffer(16)
