@@ -316,6 +316,14 @@ def run_gpu(args, rank, world):
     if args.sweep:
         result["sweep"] = stack.sweep(peaks)
         result["verify_36_layers"] = stack.full_verify(step.W8, step.s8, peaks)
+        # a 4-bit g128 drafter of the pages' size (277 MB): five layer sets, 263 MB
+        drafter = Stack(dev, w4v, torch, group=128, layers=5)
+        result["drafter_5_layers"] = drafter.stack_graph(peaks)
+        del drafter
+        # the group-size-32 W4A16 target (compressed-tensors format), same shapes
+        g32 = Stack(dev, w4v, torch, group=32)
+        result["gemm_m16_g32"] = g32.layer_set(peaks)
+        del g32
     del stack
     torch.cuda.empty_cache()
     if args.prefill:
@@ -395,10 +403,12 @@ class Stack:
 
     LAYERS = 36
 
-    def __init__(self, dev, w4v, torch):
+    def __init__(self, dev, w4v, torch, group=128, layers=LAYERS):
         self.dev, self.w4v, self.torch = dev, w4v, torch
+        self.group = group
+        self.LAYERS = layers
         g = torch.Generator(device=dev)
-        g.manual_seed(SEED)
+        g.manual_seed(SEED + group)
         self.g = g
         self.layers = []
         for _ in range(self.LAYERS):
@@ -406,9 +416,12 @@ class Stack:
             for p in inputs.LAYER_PROJS:
                 packed = torch.randint(0, 256, (w4v.packed_bytes(p.N, p.K),), generator=g, device=dev,
                                        dtype=torch.uint8)
-                sc = (torch.rand(((p.K // 128), p.N), generator=g, device=dev) * 0.015 + 0.005).half()
+                sc = (torch.rand(((p.K // group), p.N), generator=g, device=dev) * 0.015 + 0.005).half()
                 lay.append((p, packed, sc))
             self.layers.append(lay)
+
+    def proj_bytes(self, p, M):
+        return p.N * p.K // 2 + (p.K // self.group) * p.N * 2 + M * p.K * 2
 
     def _buffers(self, M):
         torch = self.torch
@@ -427,9 +440,38 @@ class Stack:
             for lay in self.layers:
                 p, packed, sc = lay[k]
                 self.w4v.w4a16_gemm(acts[p.name], packed, sc, p.N, out=outs[p.name], ws=wss[p.name],
-                                    static_weights=True)
+                                    static_weights=True, group=self.group)
 
         return time_graph(self.torch, run) / self.LAYERS
+
+    def layer_set(self, peaks, M=M_VERIFY):
+        """Per-projection device time (each in a graph of one launch per layer) and the layer set's GB/s."""
+        out, tot_ms, tot_b = {}, 0.0, 0
+        for p in inputs.LAYER_PROJS:
+            ms = self.time_projection(p, M)
+            b = self.proj_bytes(p, M)
+            out[p.name] = {"ms": round(ms, 5), "GB/s": round(b / (ms * 1e-3) / 1e9, 1)}
+            tot_ms += ms
+            tot_b += b
+        gbs = tot_b / (tot_ms * 1e-3) / 1e9
+        return {"group": self.group, "M": M, "ms": round(tot_ms, 5), "bytes": tot_b, "GB/s": round(gbs, 1),
+                "frac": round(gbs / peaks["hbm_gbs"], 4), "per_projection": out}
+
+    def stack_graph(self, peaks, M=M_VERIFY):
+        """Every projection of every layer in one CUDA graph at M rows."""
+        acts, outs, wss = self._buffers(M)
+
+        def run():
+            for lay in self.layers:
+                for (p, packed, sc) in lay:
+                    self.w4v.w4a16_gemm(acts[p.name], packed, sc, p.N, out=outs[p.name], ws=wss[p.name],
+                                        static_weights=True, group=self.group)
+
+        ms = time_graph(self.torch, run)
+        b = self.LAYERS * sum(self.proj_bytes(p, M) for p in inputs.LAYER_PROJS)
+        gbs = b / (ms * 1e-3) / 1e9
+        return {"layers": self.LAYERS, "group": self.group, "M": M, "ms": round(ms, 4), "bytes": b,
+                "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4), "launches": 4 * self.LAYERS}
 
     def sweep(self, peaks):
         out = {}

@@ -94,16 +94,20 @@ w4v_status w4v_unpack_int4(const void *packed_host, int N, int K, uint8_t *q_hos
  * C[M][N] = A[M][K] * W^T, W[n][k] = scales[k/G][n] * (q[n][k] - z[k/G][n]),
  * z = 8 when zeros == NULL (symmetric GPTQ) else the uint8 table
  * zeros[K/G][N] (values 0..15, AWQ style).  A, scales, C are fp16; products
- * are accumulated in fp32.  For M <= 32 (verify sizes, HBM-bound) each
- * group's fp32 sum is multiplied by its scale in fp32, and the per-element
- * arithmetic does not depend on M; for M > 32 (prefill, tensor-bound) the
- * dequantized weight s*(q-z) is rounded to fp16 once and the whole K is
- * accumulated in fp32.  C is rounded to fp16 (round to nearest even).
+ * are accumulated in fp32.  For M <= 32 (verify sizes, HBM-bound) with
+ * G = 128 each group's fp32 sum is multiplied by its scale in fp32; for
+ * M > 32 (prefill, tensor-bound), and for G = 32 at any M, the dequantized
+ * weight s*(q-z) is rounded to fp16 once.  The whole K is accumulated in
+ * fp32, and for M <= 32 the per-element arithmetic does not depend on M.
+ * C is rounded to fp16 (round to nearest even).  G = 128 is the GPTQ
+ * target of "Efficient LLM Challenge Results" sections 3 and 5; G = 32 is
+ * the group size of the compressed-tensors W4A16 target listed there.
  *   A        device, fp16 [M][K]
- *   Bq       device, packed int4 from w4v_pack_int4 (w4v_packed_bytes(N,K))
+ *   Bq       device, packed int4 from w4v_pack_int4 (w4v_packed_bytes(N,K);
+ *            the packed layout does not depend on G)
  *   scales   device, fp16 [K/G][N]
  *   zeros    device, uint8 [K/G][N] or NULL (requires N % 16 == 0)
- *   group    must be 128
+ *   group    G: 128 or 32
  *   C        device, fp16 [M][N] (written, never read)
  * Sizes: M >= 0 (M == 0 is a no-op), N % 8 == 0, K % 128 == 0.
  * Workspace: w4a16_workspace_bytes(M, N, K) bytes, zero-filled before first

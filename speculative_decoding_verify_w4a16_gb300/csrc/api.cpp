@@ -105,7 +105,7 @@ w4v_status w4a16_gemm_ex(const uint16_t *A, const void *Bq, const uint16_t *scal
                          w4v_stream_t stream) {
     if ((flags & ~unsigned(W4V_STATIC_WEIGHTS)) != 0u) return W4V_ERR_ARG;
     if (M < 0 || N <= 0 || K <= 0) return W4V_ERR_SHAPE;
-    if (group != kGroup) return W4V_ERR_SHAPE;
+    if (group != kGroup && group != 32) return W4V_ERR_SHAPE;
     if (K % kGroup != 0 || N % 8 != 0) return W4V_ERR_SHAPE;
     if (zeros != nullptr && N % 16 != 0) return W4V_ERR_SHAPE;
     if (M == 0) return W4V_OK;
@@ -114,10 +114,11 @@ w4v_status w4a16_gemm_ex(const uint16_t *A, const void *Bq, const uint16_t *scal
         (zeros != nullptr && !w4v::aligned16(zeros)))
         return W4V_ERR_ALIGN;
     if (M > w4v::kDecodeMaxRows)
-        return w4v::launch_w4a16_prefill(A, Bq, scales, zeros, C, M, N, K, reinterpret_cast<cudaStream_t>(stream));
+        return w4v::launch_w4a16_prefill(A, Bq, scales, zeros, group, C, M, N, K,
+                                         reinterpret_cast<cudaStream_t>(stream));
     if (ws == nullptr || ws_bytes < w4v::w4a16_decode_ws_bytes(M, N, K)) return W4V_ERR_WORKSPACE;
     if (!w4v::aligned16(ws)) return W4V_ERR_ALIGN;
-    return w4v::launch_w4a16_decode(A, Bq, scales, zeros, C, M, N, K, ws, (flags & W4V_STATIC_WEIGHTS) != 0u,
+    return w4v::launch_w4a16_decode(A, Bq, scales, zeros, group, C, M, N, K, ws, (flags & W4V_STATIC_WEIGHTS) != 0u,
                                     reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -93,6 +93,12 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDcol0 = kASlots * kASlotCols;
 constexpr int kAhead = 16;                         // groups of scales / zeros kept in flight
 constexpr int kRing = 32;                          // ring entries (> kAhead + 1)
+// Group size 32 (scales folded into the weights): per dequant warp a ring of
+// 128-k groups, each entry four sub-groups' scales and zero points of the
+// warp's 32 rows; it reuses the space of the two rings above.
+constexpr int kFAhead = 3;
+constexpr int kFRing = 4;
+constexpr int kFEntry = 4 * 32 * 2 + 4 * 32;       // 256 B scales + 128 B zeros
 
 constexpr int kMaxStages = 4;
 constexpr int kMaxSmem = 227 * 1024;
@@ -120,6 +126,7 @@ struct Layout {
     static constexpr int kScl = kBarBytes;                         // offsets inside the fixed block
     static constexpr int kZro = kScl + kDrWarps * kRing * 64;      // 32 fp16 scales per entry
     static constexpr int kMisc = kZro + kDqWarps * kRing * 32;     // 32 uint8 zeros per entry
+    static_assert(kDqWarps * kFRing * kFEntry <= kMisc - kScl, "group-32 ring fits the rings' space");
     static constexpr int kFixed = kMisc + 128;
     static constexpr int kPart = 16 * NBLK * kTileN;               // floats of one partial tile
     __host__ __device__ static constexpr int bytes(int stages) { return stages * kStage + kFixed + 1024; }
@@ -218,7 +225,11 @@ struct GroupWalk {
     }
 };
 
-template <int NBLK>
+// kFold: group size 32.  The dequant warps multiply each weight by its
+// sub-group's scale (fp16, one rounding) and the accumulators of a 128-k
+// group are added unscaled; with group size 128 the scale is applied to each
+// group's fp32 sum instead.
+template <int NBLK, bool kFold>
 __global__ void __launch_bounds__(kThreads, 1)
 w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     using L = Layout<NBLK>;
@@ -451,8 +462,55 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             zero_issue();
             return z;
         };
-        if (has_zeros)
+        if (!kFold && has_zeros)
             for (int k = 0; k < kAhead; ++k) zero_issue();
+
+        // Group size 32: scales and zero points of the four sub-groups of each
+        // 128-k group, kFAhead groups ahead (rows past N read as 0 and are
+        // never stored).
+        const uint32_t fring = smem_u32(base + fixed_off + L::kScl) + uint32_t(dq * kFRing * kFEntry);
+        int fissued = 0, fused = 0;
+        auto fold_issue = [&]() {
+            if (zw.more()) {
+                const uint32_t e = fring + uint32_t((fissued % kFRing) * kFEntry);
+                const int g4 = 4 * zw.g();
+                if (lane < 16) {
+                    const int sub = lane >> 2;
+                    const int n0 = zw.t() * kTileN + 32 * q + 8 * (lane & 3);
+                    const bool in = n0 < p.N;
+                    cp_async<16>(e + sub * 64 + (lane & 3) * 16,
+                                 in ? static_cast<const void *>(p.scales + size_t(g4 + sub) * p.N + n0) : p.scales,
+                                 in ? 16u : 0u);
+                } else if (lane < 24 && has_zeros) {
+                    const int sub = (lane - 16) >> 1;
+                    const int n0 = zw.t() * kTileN + 32 * q + 16 * (lane & 1);
+                    const bool in = n0 < p.N;
+                    cp_async<16>(e + 256 + sub * 32 + (lane & 1) * 16,
+                                 in ? static_cast<const void *>(p.zeros + size_t(g4 + sub) * p.N + n0) : p.zeros,
+                                 in ? 16u : 0u);
+                }
+                zw.next();
+            }
+            ++fissued;
+            cp_async_commit();
+        };
+        // The next group's four zero points (bytes of zz) and scales (halves of ss0, ss1).
+        auto fold_take = [&](uint32_t &zz, uint32_t &ss0, uint32_t &ss1) {
+            cp_async_wait<kFAhead - 1>();
+            __syncwarp();
+            const uint32_t e = fring + uint32_t((fused % kFRing) * kFEntry);
+            ss0 = uint32_t(lds_u16(e + 0 * 64 + 2 * lane)) | (uint32_t(lds_u16(e + 1 * 64 + 2 * lane)) << 16);
+            ss1 = uint32_t(lds_u16(e + 2 * 64 + 2 * lane)) | (uint32_t(lds_u16(e + 3 * 64 + 2 * lane)) << 16);
+            zz = 0x08080808u;
+            if (has_zeros)
+                zz = lds_u8(e + 256 + lane) | (lds_u8(e + 256 + 32 + lane) << 8) | (lds_u8(e + 256 + 64 + lane) << 16) |
+                     (lds_u8(e + 256 + 96 + lane) << 24);
+            ++fused;
+            __syncwarp();
+            fold_issue();
+        };
+        if (kFold)
+            for (int k = 0; k < kFAhead; ++k) fold_issue();
 
         // One 64-k step: chunks 2kh, 2kh+1 of the packed group at shared address `grp`,
         // dequantized with zero point z into 32 half2 registers.
@@ -475,6 +533,37 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 regs[4 * wi + 1] = h2_as_u32(__hfma2(u32_as_h2(hi0), sixteenth, zhi));
                 regs[4 * wi + 2] = h2_as_u32(__hsub2(u32_as_h2(lo1), zlo));
                 regs[4 * wi + 3] = h2_as_u32(__hfma2(u32_as_h2(hi1), sixteenth, zhi));
+            }
+        };
+        // Group size 32: the same, each 32-k chunk c (c = 2kh, 2kh+1) with its
+        // own zero point (byte c of zz) and scale (half c of ss0:ss1), and the
+        // exact q - z multiplied by the scale in fp16.
+        auto dequant_fold = [&](uint32_t grp, int kh, uint32_t zz, uint32_t ss0, uint32_t ss1, uint32_t (&regs)[32]) {
+            const uint4 va = lds128(grp + ((2 * kh) * 128 + r) * 16);
+            const uint4 vb = lds128(grp + ((2 * kh + 1) * 128 + r) * 16);
+            const uint32_t ss = kh == 0 ? ss0 : ss1;
+            const uint32_t words[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const uint32_t z = (zz >> (8 * (2 * kh + half))) & 0xFFu;
+                const uint32_t sh = half == 0 ? (ss & 0xFFFFu) : (ss >> 16);
+                const __half2 sc = u32_as_h2(sh * 0x10001u);
+                const __half2 zlo = u32_as_h2((0x6400u + z) * 0x10001u);
+                const __half2 zhi = __float2half2_rn(-(64.f + float(z)));
+#pragma unroll
+                for (int wj = 0; wj < 4; ++wj) {
+                    const int wi = 4 * half + wj;
+                    const uint32_t v = words[wi];
+                    const uint32_t v8 = v >> 8;
+                    const uint32_t lo0 = lop_and_or(v, 0x000F000Fu, 0x64006400u);
+                    const uint32_t hi0 = lop_and_or(v, 0x00F000F0u, 0x64006400u);
+                    const uint32_t lo1 = lop_and_or(v8, 0x000F000Fu, 0x64006400u);
+                    const uint32_t hi1 = lop_and_or(v8, 0x00F000F0u, 0x64006400u);
+                    regs[4 * wi + 0] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(lo0), zlo), sc));
+                    regs[4 * wi + 1] = h2_as_u32(__hmul2(__hfma2(u32_as_h2(hi0), sixteenth, zhi), sc));
+                    regs[4 * wi + 2] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(lo1), zlo), sc));
+                    regs[4 * wi + 3] = h2_as_u32(__hmul2(__hfma2(u32_as_h2(hi1), sixteenth, zhi), sc));
+                }
             }
         };
         auto release = [&](int s) {
@@ -500,8 +589,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 const int slot = f % kASlots;
                 const uint32_t g0p = base_s + s * L::kStage + L::kW + (kUnitGroups * jj) * kGroupBytes;
                 const uint32_t g1p = g0p + kGroupBytes;
-                const uint32_t z0 = has_zeros ? zero_take() : 8u;
-                const uint32_t z1 = (has_zeros && ng > 1) ? zero_take() : 8u;
+                const uint32_t z0 = (!kFold && has_zeros) ? zero_take() : 8u;
+                const uint32_t z1 = (!kFold && has_zeros && ng > 1) ? zero_take() : 8u;
                 const uint32_t col = tmem + lane_base + slot * kASlotCols;
                 // group gg: half 0 into ra, half 1 into rb; each store
                 // overlaps the next half's arithmetic (one copy of the
@@ -511,7 +600,13 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 for (int gg = 0; gg < ng; ++gg) {
                     const uint32_t gp = gg == 0 ? g0p : g1p;
                     const uint32_t z = gg == 0 ? z0 : z1;
-                    dequant(gp, 0, z, ra);
+                    uint32_t zz = 0u, ss0 = 0u, ss1 = 0u;
+                    if constexpr (kFold) {
+                        fold_take(zz, ss0, ss1);
+                        dequant_fold(gp, 0, zz, ss0, ss1, ra);
+                    } else {
+                        dequant(gp, 0, z, ra);
+                    }
                     if (gg == 0) {
                         if (f >= kASlots && !warp_wait(aempty(slot), ((f / kASlots) - 1) & 1, ab)) {
                             aborted = true;
@@ -523,7 +618,10 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                         tc_keep_alive<32>(rb);
                     }
                     tmem_st_32x32b_x32(col + 64 * gg, ra);
-                    dequant(gp, 1, z, rb);
+                    if constexpr (kFold)
+                        dequant_fold(gp, 1, zz, ss0, ss1, rb);
+                    else
+                        dequant(gp, 1, z, rb);
                     if (gg == ng - 1) release(s);     // last shared-memory read of the stage
                     tc_wait_st();
                     tc_keep_alive<32>(ra);
@@ -542,6 +640,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             f0 += n;
             sw.next(n);
         }
+        cp_async_wait<0>();                     // no ring copy outlives the loop (abort path)
     } else if (warp >= kWarpDr0 && warp < kWarpDr0 + kDrWarps) {
         // ----------------------------------------------------------- drain
         const int dr = warp - kWarpDr0;
@@ -590,7 +689,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             scale_issue();
             return v;
         };
-        for (int k = 0; k < kAhead; ++k) scale_issue();
+        if (!kFold)
+            for (int k = 0; k < kAhead; ++k) scale_issue();
         if (p.static_w) grid_dep_wait();     // before any write of C or the workspace
 
         // Tile finished by this CTA alone: write C.  Otherwise publish the fp32
@@ -701,14 +801,15 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dempty(set));
-            // groups in ascending order, each scaled in fp32
-            const float s0 = scale_take();
+            // groups in ascending order, each scaled in fp32 (group size 32:
+            // the weights carry their scales, the sums are added as they are)
+            const float s0 = kFold ? 1.f : scale_take();
 #pragma unroll
             for (int b = 0; b < NBLK; ++b)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) acc[b][j] = fmaf(s0, __uint_as_float(d[b][j]), acc[b][j]);
             if (ng > 1) {
-                const float s1 = scale_take();
+                const float s1 = kFold ? 1.f : scale_take();
 #pragma unroll
                 for (int b = 0; b < NBLK; ++b)
 #pragma unroll
@@ -729,6 +830,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             }
         }
         if (ok) mark_last();
+        cp_async_wait<0>();
     }
 
     __syncthreads();
@@ -860,7 +962,7 @@ int pick_cluster(int n_tiles, int n_pairs, int sm_count) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int fit = 0;
-        if (cudaOccupancyMaxActiveClusters(&fit, w4a16_decode_kernel<2>, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&fit, w4a16_decode_kernel<2, false>, &cfg) != cudaSuccess) {
             cudaGetLastError();
             continue;
         }
@@ -869,13 +971,13 @@ int pick_cluster(int n_tiles, int n_pairs, int sm_count) {
     return 0;
 }
 
-template <int NBLK>
+template <int NBLK, bool kFold>
 w4v_status configure() {
     static int configured_for = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_for != dev) {
-        if (cudaFuncSetAttribute(w4a16_decode_kernel<NBLK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(w4a16_decode_kernel<NBLK, kFold>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kMaxSmem) != cudaSuccess) {
             cudaGetLastError();
             return W4V_ERR_CUDA;
@@ -885,16 +987,17 @@ w4v_status configure() {
     return W4V_OK;
 }
 
-template <int NBLK>
+template <int NBLK, bool kFold>
 w4v_status launch(const CUtensorMap &xmap, Args &a, int cluster, cudaStream_t stream) {
     using L = Layout<NBLK>;
-    w4v_status st = configure<NBLK>();
+    w4v_status st = configure<NBLK, kFold>();
     if (st != W4V_OK) return st;
     a.cluster = cluster;
     a.stages = L::kStagesMax;
     if (cluster > 0) a.P = a.n_tiles * cluster;
     const size_t smem = size_t(L::bytes(a.stages));
-    if (launch_pdl_cluster(w4a16_decode_kernel<NBLK>, dim3(a.P), dim3(kThreads), smem, stream, cluster, xmap, a) !=
+    if (launch_pdl_cluster(w4a16_decode_kernel<NBLK, kFold>, dim3(a.P), dim3(kThreads), smem, stream, cluster, xmap,
+                           a) !=
         cudaSuccess) {
         cudaGetLastError();
         return W4V_ERR_CUDA;
@@ -914,7 +1017,7 @@ int cluster_for(int n_tiles, int n_pairs, int sm_count) {
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < n_cache; ++i)
         if (cache[i].dev == dev && cache[i].n_tiles == n_tiles && cache[i].n_pairs == n_pairs) return cache[i].cluster;
-    if (configure<1>() != W4V_OK || configure<2>() != W4V_OK) return 0;
+    if (configure<1, false>() != W4V_OK || configure<2, false>() != W4V_OK) return 0;
     const int c = pick_cluster(n_tiles, n_pairs, sm_count);
     if (n_cache < 64) cache[n_cache++] = Entry{dev, n_tiles, n_pairs, c};
     return c;
@@ -931,7 +1034,7 @@ size_t w4a16_decode_ws_bytes(int M, int N, int K) {
 }
 
 w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t *scales,
-                               const uint8_t *zeros, uint16_t *C, int M, int N, int K,
+                               const uint8_t *zeros, int group, uint16_t *C, int M, int N, int K,
                                void *ws, bool static_weights, cudaStream_t stream) {
     const DeviceInfo *info = nullptr;
     w4v_status st = device_info(&info);
@@ -960,8 +1063,8 @@ w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t
                              2 * kStageGroups, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != W4V_OK) return st;
     const int cluster = cluster_for(a.n_tiles, a.n_pairs, info->sm_count);
-    if (nblk == 1) return launch<1>(xmap, a, cluster, stream);
-    return launch<2>(xmap, a, cluster, stream);
+    if (group == 32) return nblk == 1 ? launch<1, true>(xmap, a, cluster, stream) : launch<2, true>(xmap, a, cluster, stream);
+    return nblk == 1 ? launch<1, false>(xmap, a, cluster, stream) : launch<2, false>(xmap, a, cluster, stream);
 }
 
 }  // namespace w4v

@@ -68,6 +68,9 @@ struct Args {
     int n_tiles_n, n_tiles_m, n_groups;
 };
 
+// kG32: group size 32, so each 32-k chunk of a 128-k block has its own
+// scale and zero point (four per block instead of one).
+template <bool kG32>
 __global__ void __launch_bounds__(kThreads, 2)
 w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     extern __shared__ uint8_t smem_raw[];
@@ -186,14 +189,24 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             const int tn = tile % p.n_tiles_n;
             const int n = tn * kTileN + r;
             const bool valid = n < p.N;
-            float s_next = valid ? __half2float(__ldg(p.scales + n)) : 0.f;
+            // scale rows per 128-k block: 1, or 4 with group size 32
+            constexpr int kSub = kG32 ? 4 : 1;
+            float s_next[kSub];
+#pragma unroll
+            for (int c = 0; c < kSub; ++c) s_next[c] = valid ? __half2float(__ldg(p.scales + size_t(c) * p.N + n)) : 0.f;
             for (int g = 0; g < p.n_groups; ++g, ++it) {
                 const int s = it % kStages;
                 const int slot = it % kASlots;
-                const float sc = s_next;
-                if (g + 1 < p.n_groups) s_next = valid ? __half2float(__ldg(p.scales + size_t(g + 1) * p.N + n)) : 0.f;
-                uint32_t z = 8;
-                if (p.zeros != nullptr && valid) z = __ldg(p.zeros + size_t(g) * p.N + n);
+                float sc[kSub];
+                uint32_t z[kSub];
+#pragma unroll
+                for (int c = 0; c < kSub; ++c) {
+                    sc[c] = s_next[c];
+                    if (g + 1 < p.n_groups)
+                        s_next[c] = valid ? __half2float(__ldg(p.scales + size_t(kSub * (g + 1) + c) * p.N + n)) : 0.f;
+                    z[c] = 8;
+                    if (p.zeros != nullptr && valid) z[c] = __ldg(p.zeros + size_t(kSub * g + c) * p.N + n);
+                }
                 if (!warp_wait(full(s), (it / kStages) & 1, ab)) {
                     ok = false;
                     break;
@@ -204,12 +217,13 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4 *>(wsm + (j * 128 + r) * 16);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty(s));
-                const __half2 zlo = u32_as_h2((0x6400u + z) * 0x10001u);
-                const __half2 zhi = __float2half2_rn(-(64.f + float(z)));
-                const __half2 scl = __float2half2_rn(sc);
                 uint32_t regs[64];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
+                    const int c = kG32 ? j : 0;          // chunk j holds k = 32j .. 32j+31 of the block
+                    const __half2 zlo = u32_as_h2((0x6400u + z[c]) * 0x10001u);
+                    const __half2 zhi = __float2half2_rn(-(64.f + float(z[c])));
+                    const __half2 scl = __float2half2_rn(sc[c]);
                     const uint32_t words[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
                     for (int wi = 0; wi < 4; ++wi) {
@@ -275,10 +289,30 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     }
 }
 
+template <bool kG32>
+w4v_status launch(const CUtensorMap &xmap, const Args &a, int grid, cudaStream_t stream) {
+    static int configured_for = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_for != dev) {
+        if (cudaFuncSetAttribute(w4a16_prefill_kernel<kG32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return W4V_ERR_CUDA;
+        }
+        configured_for = dev;
+    }
+    if (launch_pdl(w4a16_prefill_kernel<kG32>, dim3(grid), dim3(kThreads), kBytes, stream, xmap, a) != cudaSuccess) {
+        cudaGetLastError();
+        return W4V_ERR_CUDA;
+    }
+    return W4V_OK;
+}
+
 }  // namespace
 
 w4v_status launch_w4a16_prefill(const uint16_t *A, const void *Bq, const uint16_t *scales, const uint8_t *zeros,
-                                uint16_t *C, int M, int N, int K, cudaStream_t stream) {
+                                int group, uint16_t *C, int M, int N, int K, cudaStream_t stream) {
     const DeviceInfo *info = nullptr;
     w4v_status st = device_info(&info);
     if (st != W4V_OK) return st;
@@ -298,24 +332,9 @@ w4v_status launch_w4a16_prefill(const uint16_t *A, const void *Bq, const uint16_
     st = encode_tmap_kblocks(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, uint64_t(K), uint64_t(M), 64, kTileM, 2,
                              CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != W4V_OK) return st;
-    static int configured_for = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_for != dev) {
-        if (cudaFuncSetAttribute(w4a16_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBytes) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            return W4V_ERR_CUDA;
-        }
-        configured_for = dev;
-    }
     const long long tiles = (long long)a.n_tiles_n * a.n_tiles_m;
     const int grid = static_cast<int>(std::min<long long>(2LL * info->sm_count, tiles));
-    if (launch_pdl(w4a16_prefill_kernel, dim3(grid), dim3(kThreads), kBytes, stream, xmap, a) != cudaSuccess) {
-        cudaGetLastError();
-        return W4V_ERR_CUDA;
-    }
-    return W4V_OK;
+    return group == 32 ? launch<true>(xmap, a, grid, stream) : launch<false>(xmap, a, grid, stream);
 }
 
 }  // namespace w4v

@@ -151,8 +151,10 @@ def workspace(nbytes: int, device="cuda"):
 STATIC_WEIGHTS = 1
 
 
-def w4a16_gemm(A, Bq, scales, N: int, zeros=None, out=None, ws=None, stream=None, static_weights=False):
-    """C = A @ deq(Bq, scales, zeros)^T on the GPU.  A fp16 [M][K] cuda, Bq packed uint8 cuda.
+def w4a16_gemm(A, Bq, scales, N: int, zeros=None, out=None, ws=None, stream=None, static_weights=False,
+               group: int = GROUP):
+    """C = A @ deq(Bq, scales, zeros)^T on the GPU.  A fp16 [M][K] cuda, Bq packed uint8 cuda,
+    scales fp16 [K/group][N] (group 128 or 32).
     static_weights: the caller promises no GPU work still in flight writes Bq, scales or zeros
     (w4a16_gemm_ex with W4V_STATIC_WEIGHTS)."""
     import torch
@@ -161,7 +163,7 @@ def w4a16_gemm(A, Bq, scales, N: int, zeros=None, out=None, ws=None, stream=None
         out = torch.empty((M, N), dtype=torch.float16, device=A.device)
     if ws is None:
         ws = workspace(w4a16_workspace_bytes(M, N, K), A.device)
-    code = load().w4a16_gemm_ex(_ptr(A), _ptr(Bq), _ptr(scales), _ptr(zeros), GROUP, _ptr(out), M, N, K,
+    code = load().w4a16_gemm_ex(_ptr(A), _ptr(Bq), _ptr(scales), _ptr(zeros), int(group), _ptr(out), M, N, K,
                                 _ptr(ws), ws.numel(), STATIC_WEIGHTS if static_weights else 0, _stream(stream))
     _check(code, "w4a16_gemm")
     return out

@@ -80,6 +80,8 @@ def test_argument_validation_before_launch(w4v_mod):
     ws_small = 16
     # w4a16_gemm
     assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 64, FAKE, 16, 512, 256, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    # group size 32 passes the shape checks (and fails later on the workspace)
+    assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 32, FAKE, 16, 512, 256, FAKE, ws_small, None) == w4v_mod.ERR_WORKSPACE
     assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, -1, 512, 256, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
     assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 500, 256, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
     assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 512, 200, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE

@@ -51,9 +51,11 @@ def test_permutation_weights_pick_columns(oracle_mod, code, sign):
     assert np.array_equal(C, sign * A.astype(np.float64)[:, pi])
 
 
-def test_group_index_and_scale_orientation(oracle_mod):
-    """Scales are s[k/128][n]: give every (group, column) a distinct power of two
-    and put a single +1 code in one k of one group per column."""
+@pytest.mark.parametrize("G", [128, 32])
+def test_group_index_and_scale_orientation(oracle_mod, G):
+    """Scales are s[k/G][n]: give every (group, column) a distinct power of two
+    and put a single +1 code in one k of one group per column (G = 128, and
+    the group size 32 of the compressed-tensors target)."""
     M, N, K = 2, 16, 512
     ng = K // G
     rng = np.random.default_rng(3)
@@ -65,7 +67,7 @@ def test_group_index_and_scale_orientation(oracle_mod):
     q = np.full((N, K), 8, np.uint8)
     ks = rng.integers(0, K, size=N)
     q[np.arange(N), ks] = 9
-    C = oracle_mod.w4a16_gemm(A, q, s)
+    C = oracle_mod.w4a16_gemm(A, q, s, group=G)
     for n in range(N):
         want = float(s[ks[n] // G, n])
         assert C[0, n] == want and C[1, n] == want
@@ -83,17 +85,18 @@ def test_code_range_and_linearity(oracle_mod):
     assert np.array_equal(C[0], (np.arange(16) - 8) * 0.25 * 0.5)
 
 
-def test_zero_table(oracle_mod):
-    """With a zero table z[k/128][n], W = s * (q - z); q == z gives 0 and q = z + 1 gives s."""
+@pytest.mark.parametrize("G", [128, 32])
+def test_zero_table(oracle_mod, G):
+    """With a zero table z[k/G][n], W = s * (q - z); q == z gives 0 and q = z + 1 gives s."""
     M, N, K = 2, 8, 256
     rng = np.random.default_rng(4)
     z = rng.integers(0, 15, size=(K // G, N), dtype=np.uint8)
     q = np.repeat(z, G, axis=0).T.copy()               # q[n][k] = z[k/G][n]
     s = np.full((K // G, N), 0.5, np.float16)
     A = rng.standard_normal((M, K)).astype(np.float16)
-    assert np.all(oracle_mod.w4a16_gemm(A, q, s, zeros=z) == 0.0)
+    assert np.all(oracle_mod.w4a16_gemm(A, q, s, zeros=z, group=G) == 0.0)
     A1 = np.ones((M, K), np.float16)
-    C = oracle_mod.w4a16_gemm(A1, q + 1, s, zeros=z)
+    C = oracle_mod.w4a16_gemm(A1, q + 1, s, zeros=z, group=G)
     assert np.all(C == 0.5 * K)
 
 
