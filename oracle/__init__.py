@@ -60,6 +60,7 @@ def _load():
             lib.oracle_argmax_f64.argtypes = [P, I, I, P]
             lib.oracle_argmax_f32.argtypes = [P, I, I, P]
             lib.oracle_spec_accept.argtypes = [P, P, I, I, P, P]
+            lib.oracle_ngram_draft.argtypes = [P, P, I, I, I, I, I, P, P]
             lib.oracle_num_threads.restype = I
             lib.oracle_set_num_threads.argtypes = [I]
             _lib = lib
@@ -215,3 +216,19 @@ def spec_accept(target, draft):
     tok = np.empty((B, K + 1), np.int32)
     _load().oracle_spec_accept(_ptr(t), _ptr(d), B, K, _ptr(n), _ptr(tok))
     return n, tok
+
+
+def ngram_draft(context, lengths, n_min, n_max, K):
+    """Prompt-lookup drafts for each row of context int32 [B][ld] (row b holds
+    lengths[b] tokens): (drafts int32 [B][K] with -1 padding, match length [B])."""
+    c = _c(context, np.int32)
+    if c.ndim == 1:
+        d, m = ngram_draft(c[None, :], [c.shape[0]], n_min, n_max, K)
+        return d[0], int(m[0])
+    B, ld = c.shape
+    ln = _c(lengths, np.int32).reshape(B)
+    assert np.all((ln >= 0) & (ln <= ld)) and 1 <= n_min <= n_max and K >= 0
+    d = np.empty((B, K), np.int32)
+    m = np.empty(B, np.int32)
+    _load().oracle_ngram_draft(_ptr(c), _ptr(ln), B, ld, int(n_min), int(n_max), int(K), _ptr(d), _ptr(m))
+    return d, m

@@ -22,6 +22,8 @@
  *     common, but not the deciding lever": the target is 4-bit W4A16 GPTQ
  *     with group size 128, fp16 activations, and an untied lm_head quantized
  *     to 8 bits.
+ *   - Same page, section 3, table of drafting methods: n-gram /
+ *     prompt-lookup drafting copies spans from the prompt.
  * Readings where the pages are silent (zero point 8, scales laid out
  * [K/G][N], int8 symmetric per-vocab-row lm_head scale, lowest-index argmax
  * tie-break, NaN counted as -inf) are the plainest ones the rest supports;
@@ -232,6 +234,48 @@ void oracle_spec_accept(const int32_t *t, const int32_t *d, int B, int K,
             int32_t *ob = tok_out + (size_t)b * (K + 1);
             for (int j = 0; j <= K; ++j) ob[j] = (j < n) ? db[j] : (j == n ? tb[n] : -1);
         }
+    }
+}
+
+/* ------------------------------------------------------- n-gram drafting --
+ * Model-free drafting by prompt lookup ("Efficient LLM Challenge Results",
+ * section 3, the table of drafting methods: n-gram / prompt-lookup drafting
+ * copies spans from the prompt; it needs no auxiliary model).  For a context
+ * c[0..L-1], with n running from n_max down to n_min:
+ *   the n-gram is the last n tokens c[L-n..L-1];
+ *   an occurrence is a start p with p + n <= L - 1 (it starts before the
+ *   n-gram itself, so at least one token follows it) and c[p+i] == c[L-n+i]
+ *   for every i < n; the latest such p is taken;
+ *   the drafts are the tokens that followed it: d[i] = c[p+n+i] while
+ *   p+n+i < L, then the -1 sentinel up to K (the constant-K padding of the
+ *   runner-up paragraph of the same section).
+ * The first n (the longest) with an occurrence decides; match_len is that n.
+ * With no occurrence for any n >= n_min (or L < 2) every draft is -1 and
+ * match_len is 0.  Contexts are rows of a [B][ld] array, row b of length
+ * len[b] (0 <= len[b] <= ld).                                               */
+void oracle_ngram_draft(const int32_t *ctx, const int32_t *len, int B, int ld, int n_min, int n_max, int K,
+                        int32_t *d_out, int32_t *match_out)
+{
+    for (int b = 0; b < B; ++b) {
+        const int32_t *c = ctx + (size_t)b * ld;
+        const int L = len[b];
+        int32_t *d = d_out + (size_t)b * K;
+        for (int i = 0; i < K; ++i) d[i] = -1;
+        int found_n = 0;
+        for (int n = n_max; n >= n_min && found_n == 0; --n) {
+            if (n > L - 1) continue;                /* no start p >= 0 with p + n <= L - 1 */
+            for (int p = L - n - 1; p >= 0; --p) {
+                int same = 1;
+                for (int i = 0; i < n; ++i)
+                    if (c[p + i] != c[L - n + i]) { same = 0; break; }
+                if (same) {
+                    for (int i = 0; i < K && p + n + i < L; ++i) d[i] = c[p + n + i];
+                    found_n = n;
+                    break;
+                }
+            }
+        }
+        if (match_out) match_out[b] = found_n;
     }
 }
 

@@ -4,12 +4,14 @@
 speculative decoding leaves the output unchanged, whatever the drafts; drafts
 padded with -1 sentinels stay lossless.  On a toy W4A16 target with an int8
 lm_head (oracle/toy_model.py), speculative decoding with random, perfect,
-perfect-then-wrong, all-sentinel, K=0, K=15 and K=20 drafters must emit the
-same tokens as plain greedy decoding, token for token.
+perfect-then-wrong, all-sentinel, prompt-lookup (n-gram), K=0, K=15, K=20
+and K=23 drafters must emit the same tokens as plain greedy decoding, token
+for token.
 """
 import numpy as np
 import pytest
 
+import oracle
 from oracle.toy_model import ToyWeights, greedy_decode, spec_decode
 from speculative_decoding_verify_w4a16_gb300 import inputs
 
@@ -42,12 +44,17 @@ def _drafters(w, seed):
         L = int(rng.integers(0, K + 1))
         return greedy_decode(w, ctx, L) + [-1] * (K - L)
 
+    def ngram(ctx, K):
+        # prompt lookup over the context so far (the oracle's n-gram drafter)
+        d, _ = oracle.ngram_draft(np.array(ctx, np.int32), None, 1, 3, K)
+        return [int(x) for x in d]
+
     return dict(random=random, perfect=perfect, perfect_then_wrong=perfect_then_wrong,
-                sentinel=sentinel, padded=padded)
+                sentinel=sentinel, padded=padded, ngram=ngram)
 
 
 CASES = (("random", 15), ("perfect", 15), ("perfect_then_wrong", 15),
-         ("sentinel", 20), ("padded", 20), ("random", 0), ("perfect", 4))
+         ("sentinel", 20), ("padded", 20), ("random", 0), ("perfect", 4), ("ngram", 15), ("ngram", 23))
 
 
 @pytest.mark.parametrize("V", [64, 1024])
