@@ -329,6 +329,7 @@ def run_gpu(args, rank, world):
     if args.prefill:
         result["prefill"] = run_prefill(dev, w4v, torch, peaks)
         result["lmhead_batched"] = run_lmhead_batched(dev, w4v, torch, peaks)
+    result["ngram_draft"] = run_ngram(dev, w4v, torch)
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(step)
     return result
@@ -586,6 +587,24 @@ def run_lmhead_batched(dev, w4v, torch, peaks):
         out["M=%d" % M] = {"ms": round(ms, 5), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
                            "TFLOP/s": round(2.0 * M * V * H / (ms * 1e-3) / 1e12, 1),
                            "workload": "%d sequences x %d positions + acceptance" % (B, K1)}
+    return out
+
+
+def run_ngram(dev, w4v, torch):
+    """Prompt-lookup drafting of K = 23 tokens (the n-gram entry's K) for 8
+    prompt-like contexts of 4096 tokens, and for one 64K-token context."""
+    out = {}
+    for (B, ld) in ((8, 4096), (1, 65536)):
+        ctx, lens = inputs.ngram_contexts(SEED, B, ld, inputs.V_4B, "bench", ragged=False)
+        c = torch.from_numpy(ctx).to(dev)
+        l = torch.from_numpy(lens).to(dev)
+        d = torch.empty((B, 23), dtype=torch.int32, device=dev)
+        m = torch.empty(B, dtype=torch.int32, device=dev)
+        ws = w4v.workspace(w4v.load().ngram_draft_workspace_bytes(B), dev)
+        ms = time_graph(torch, lambda: [w4v.ngram_draft(c, l, 1, 4, 23, out=d, match=m, ws=ws)
+                                        for _ in range(20)]) / 20
+        out["B=%d,L=%d" % (B, ld)] = {"us": round(ms * 1e3, 2), "n_min": 1, "n_max": 4, "K": 23,
+                                      "GB/s": round(B * ld * 4 / (ms * 1e-3) / 1e9, 1)}
     return out
 
 

@@ -216,6 +216,29 @@ w4v_status w8_lmhead_argmax_accept(const uint16_t *X, const int8_t *W, const uin
                                    float *maxlogit, void *workspace, size_t workspace_bytes,
                                    w4v_stream_t stream);
 
+/* ------------------------------------------------------------ ngram_draft
+ * Model-free drafts by prompt lookup ("Efficient LLM Challenge Results",
+ * section 3, table of drafting methods: n-gram / prompt-lookup drafting
+ * copies spans from the prompt; the runner-up pads drafts to a constant K
+ * with -1).  For row b of `context`, c[0..L-1] with L = lengths[b] (values
+ * outside [0, ld] are clamped to it): for n from n_max down to n_min, the
+ * n-gram is c[L-n..L-1]; its latest earlier occurrence is the largest p with
+ * p + n <= L - 1 and c[p+i] == c[L-n+i] for i < n.  The first n with an
+ * occurrence gives drafts[b][i] = c[p+n+i] while p+n+i < L, else -1, and
+ * match_len[b] = n; with none, every draft is -1 and match_len[b] = 0.
+ *   context    device, int32 [B][ld] (tokens past a row's length are ignored)
+ *   lengths    device, int32 [B]
+ *   drafts     device, int32 [B][K] (may be NULL when K == 0)
+ *   match_len  device, int32 [B] or NULL
+ * Sizes: 0 <= B <= 65535 (0 is a no-op), ld >= 1, 1 <= n_min <= n_max <= 64,
+ * 0 <= K <= 1024.  Workspace: ngram_draft_workspace_bytes(B) bytes,
+ * zero-filled before first use (one best key and one arrival counter per
+ * row). */
+size_t ngram_draft_workspace_bytes(int B);
+w4v_status ngram_draft(const int32_t *context, const int32_t *lengths, int B, int ld, int n_min,
+                       int n_max, int K, int32_t *drafts, int32_t *match_len,
+                       void *workspace, size_t workspace_bytes, w4v_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -166,6 +166,26 @@ w4v_status w8_lmhead_argmax_accept(const uint16_t *X, const int8_t *W, const uin
                                         reinterpret_cast<cudaStream_t>(stream), &acc);
 }
 
+size_t ngram_draft_workspace_bytes(int B) {
+    if (B < 0 || B > 65535) return 0;
+    return w4v::ngram_ws_bytes(B);
+}
+
+w4v_status ngram_draft(const int32_t *context, const int32_t *lengths, int B, int ld, int n_min, int n_max, int K,
+                       int32_t *drafts, int32_t *match_len, void *ws, size_t ws_bytes, w4v_stream_t stream) {
+    if (B < 0 || B > 65535 || ld < 1 || n_min < 1 || n_max < n_min || n_max > w4v::kNgramMax || K < 0 || K > 1024)
+        return W4V_ERR_SHAPE;
+    if (B == 0) return W4V_OK;
+    if (context == nullptr || lengths == nullptr || (K > 0 && drafts == nullptr)) return W4V_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(context) & 3u) || (reinterpret_cast<uintptr_t>(lengths) & 3u) ||
+        (reinterpret_cast<uintptr_t>(drafts) & 3u) || (reinterpret_cast<uintptr_t>(match_len) & 3u))
+        return W4V_ERR_ALIGN;
+    if (ws == nullptr || ws_bytes < w4v::ngram_ws_bytes(B)) return W4V_ERR_WORKSPACE;
+    if (!w4v::aligned16(ws)) return W4V_ERR_ALIGN;
+    return w4v::launch_ngram_draft(context, lengths, B, ld, n_min, n_max, K, drafts, match_len, ws,
+                                   reinterpret_cast<cudaStream_t>(stream));
+}
+
 w4v_status spec_accept(const int32_t *target, const int32_t *draft, int B, int K, int32_t *n_accepted,
                        int32_t *out_tokens, w4v_stream_t stream) {
     if (B < 0 || K < 0 || K > 1024) return W4V_ERR_SHAPE;

@@ -98,6 +98,12 @@ w4v_status launch_w4a16_prefill(const uint16_t *A, const void *Bq, const uint16_
 // Rows up to which the verify-sized (HBM-bound) kernel is used.
 constexpr int kDecodeMaxRows = 32;
 
+// Prompt-lookup drafting: longest suffix n-gram searched, n <= kNgramMax.
+constexpr int kNgramMax = 64;
+size_t ngram_ws_bytes(int B);
+w4v_status launch_ngram_draft(const int32_t *context, const int32_t *lengths, int B, long long ld, int n_min,
+                              int n_max, int K, int32_t *draft, int32_t *match, void *ws, cudaStream_t stream);
+
 // Greedy acceptance fused into the lm_head's last CTA: the M = B*(n_draft+1)
 // rows are B verify blocks of n_draft+1 positions each.
 struct LmAccept {

@@ -164,3 +164,30 @@ def toy_model_arrays(seed: int, V: int = 64, H: int = 256, layers: int = 2):
 
 def random_tokens(seed: int, n: int, V: int, *tags) -> List[int]:
     return [int(x) for x in rng(seed, "tok", n, V, *tags).integers(0, V, size=n)]
+
+
+def ngram_contexts(seed: int, B: int, ld: int, V: int, *tags, copy_prob: float = 0.5,
+                   ragged: bool = True) -> Tuple[np.ndarray, np.ndarray]:
+    """Prompt-like token contexts for prompt-lookup drafting: int32 [B][ld] and
+    lengths [B].  Each row grows by spans of 4..32 tokens that are, with
+    probability copy_prob, copies of an earlier span of the same row (the
+    repeated passages prompt lookup feeds on), else fresh uniform tokens.
+    Ragged lengths are uniform in [ld/2, ld]; tokens past a row's length are
+    uniform filler."""
+    r = rng(seed, "ngctx", B, ld, V, *tags)
+    ctx = r.integers(0, V, size=(B, ld), dtype=np.int64).astype(np.int32)
+    if ragged:
+        lens = r.integers(ld // 2, ld + 1, size=B).astype(np.int32)
+    else:
+        lens = np.full(B, ld, np.int32)
+    for b in range(B):
+        L = int(lens[b])
+        pos = min(L, int(r.integers(4, 33)))
+        while pos < L:
+            n = min(L - pos, int(r.integers(4, 33)))
+            if pos >= 8 and r.random() < copy_prob:
+                src = int(r.integers(0, pos - 4))
+                for i in range(n):           # may overlap its own output, like a repeat
+                    ctx[b, pos + i] = ctx[b, src + i]
+            pos += n
+    return ctx, lens

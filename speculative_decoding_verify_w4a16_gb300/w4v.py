@@ -66,6 +66,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.spec_accept.restype = I
             lib.w8_lmhead_argmax_accept.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, S, P]
             lib.w8_lmhead_argmax_accept.restype = I
+            lib.ngram_draft_workspace_bytes.argtypes = [I]
+            lib.ngram_draft_workspace_bytes.restype = S
+            lib.ngram_draft.argtypes = [P, P, I, I, I, I, I, P, P, P, S, P]
+            lib.ngram_draft.restype = I
             _lib = lib
     return _lib
 
@@ -222,3 +226,20 @@ def w8_lmhead_argmax_accept(X, W, scale, draft, out=None, n_out=None, tok_out=No
                                           _ptr(tok_out), _ptr(maxlogit), _ptr(ws), ws.numel(), _stream(stream))
     _check(code, "w8_lmhead_argmax_accept")
     return out, n_out, tok_out
+
+
+def ngram_draft(context, lengths, n_min: int, n_max: int, K: int, out=None, match=None, ws=None, stream=None):
+    """Prompt-lookup drafts on the GPU: context int32 [B][ld], lengths int32 [B] (cuda).
+    Returns (drafts int32 [B][K], match length int32 [B])."""
+    import torch
+    B, ld = context.shape
+    if out is None:
+        out = torch.empty((B, K), dtype=torch.int32, device=context.device)
+    if match is None:
+        match = torch.empty(B, dtype=torch.int32, device=context.device)
+    if ws is None:
+        ws = workspace(load().ngram_draft_workspace_bytes(B), context.device)
+    code = load().ngram_draft(_ptr(context), _ptr(lengths), B, ld, int(n_min), int(n_max), int(K),
+                              _ptr(out) if K > 0 else None, _ptr(match), _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "ngram_draft")
+    return out, match

@@ -14,7 +14,7 @@ FAKE = 0x10000          # an aligned, never-dereferenced stand-in pointer
 def test_exports_every_header_function(w4v_mod):
     names = w4v_mod.header_functions()
     for required in ("w4v_init", "w4v_get_status", "w4v_pack_int4", "w4a16_gemm",
-                     "w8_lmhead_argmax", "spec_accept", "w8_lmhead_argmax_accept"):
+                     "w8_lmhead_argmax", "spec_accept", "w8_lmhead_argmax_accept", "ngram_draft"):
         assert required in names
     lib = w4v_mod.load()
     for name in names:
@@ -121,6 +121,20 @@ def test_argument_validation_before_launch(w4v_mod):
     assert acc(FAKE, FAKE, FAKE, 1, 15, 256, 1024, FAKE + 2, FAKE, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_ALIGN
     assert acc(FAKE, FAKE, FAKE, 1, 15, 256, 1024, FAKE, FAKE, FAKE, None, None, FAKE, ws_small, None) == w4v_mod.ERR_WORKSPACE
     assert acc(None, None, None, 0, 15, 256, 1024, None, None, None, None, None, None, 0, None) == w4v_mod.OK
+    # ngram_draft
+    ng = lib.ngram_draft
+    assert ng(FAKE, FAKE, 4, 100, 0, 3, 8, FAKE, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE   # n_min 0
+    assert ng(FAKE, FAKE, 4, 100, 3, 2, 8, FAKE, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE   # n_max < n_min
+    assert ng(FAKE, FAKE, 4, 100, 1, 65, 8, FAKE, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert ng(FAKE, FAKE, 4, 100, 1, 3, 1025, FAKE, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert ng(FAKE, FAKE, 4, 0, 1, 3, 8, FAKE, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE     # ld 0
+    assert ng(FAKE, FAKE, 65536, 100, 1, 3, 8, FAKE, None, FAKE, 1 << 30, None) == w4v_mod.ERR_SHAPE
+    assert ng(None, FAKE, 4, 100, 1, 3, 8, FAKE, None, FAKE, 1 << 30, None) == w4v_mod.ERR_ARG
+    assert ng(FAKE, FAKE, 4, 100, 1, 3, 8, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_ARG
+    assert ng(FAKE, FAKE + 2, 4, 100, 1, 3, 8, FAKE, None, FAKE, 1 << 30, None) == w4v_mod.ERR_ALIGN
+    assert ng(FAKE, FAKE, 4, 100, 1, 3, 8, FAKE, None, FAKE, 16, None) == w4v_mod.ERR_WORKSPACE
+    assert ng(None, None, 0, 100, 1, 3, 8, None, None, None, 0, None) == w4v_mod.OK
+    assert w4v_mod.load().ngram_draft_workspace_bytes(8) >= 8 * 12
     # packer
     assert lib.w4v_pack_int4(None, 128, 128, FAKE) == w4v_mod.ERR_ARG
     buf = ctypes.create_string_buffer(16)
