@@ -61,6 +61,7 @@ def _load():
             lib.oracle_argmax_f32.argtypes = [P, I, I, P]
             lib.oracle_spec_accept.argtypes = [P, P, I, I, P, P]
             lib.oracle_ngram_draft.argtypes = [P, P, I, I, I, I, I, P, P]
+            lib.oracle_gdn_recurrence.argtypes = [P, P, P, P, P, P, I, I, I, P, P]
             lib.oracle_num_threads.restype = I
             lib.oracle_set_num_threads.argtypes = [I]
             _lib = lib
@@ -232,3 +233,33 @@ def ngram_draft(context, lengths, n_min, n_max, K):
     m = np.empty(B, np.int32)
     _load().oracle_ngram_draft(_ptr(c), _ptr(ln), B, ld, int(n_min), int(n_max), int(K), _ptr(d), _ptr(m))
     return d, m
+
+
+def gdn_recurrence(S0, q, k, v, alpha, beta):
+    """Gated delta recurrence per head, in double:
+    S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,  o_t = S_t q_t.
+    S0 [H][dv][dk]; q, k [T][H][dk]; v [T][H][dv]; alpha, beta [T][H] (any float dtype,
+    converted exactly to double).  Returns (o [T][H][dv], S_T [H][dv][dk])."""
+    S0 = _c(S0, np.float64)
+    q = _c(q, np.float64)
+    k = _c(k, np.float64)
+    v = _c(v, np.float64)
+    alpha = _c(alpha, np.float64)
+    beta = _c(beta, np.float64)
+    H, dv, dk = S0.shape
+    T = q.shape[0]
+    assert q.shape == (T, H, dk) and k.shape == (T, H, dk) and v.shape == (T, H, dv)
+    assert alpha.shape == (T, H) and beta.shape == (T, H)
+    o = np.empty((T, H, dv), np.float64)
+    S = np.empty((H, dv, dk), np.float64)
+    lib = _load()
+    for h in range(H):
+        qh, kh, vh = _c(q[:, h], np.float64), _c(k[:, h], np.float64), _c(v[:, h], np.float64)
+        ah, bh = _c(alpha[:, h], np.float64), _c(beta[:, h], np.float64)
+        oh = np.empty((T, dv), np.float64)
+        Sh = np.empty((dv, dk), np.float64)
+        lib.oracle_gdn_recurrence(_ptr(_c(S0[h], np.float64)), _ptr(qh), _ptr(kh), _ptr(vh), _ptr(ah), _ptr(bh),
+                                  T, dk, dv, _ptr(oh), _ptr(Sh))
+        o[:, h] = oh
+        S[h] = Sh
+    return o, S

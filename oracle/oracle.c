@@ -24,6 +24,10 @@
  *     to 8 bits.
  *   - Same page, section 3, table of drafting methods: n-gram /
  *     prompt-lookup drafting copies spans from the prompt.
+ *   - Same page, section 3 (runner-up paragraph), and "DFlash K=15 for
+ *     Qwen3.5-4B on a single A10G", section "What transfers": a rejected
+ *     draft must not leave its update in a Gated DeltaNet recurrent state;
+ *     the recurrence is that of the first page's reference [12].
  * Readings where the pages are silent (zero point 8, scales laid out
  * [K/G][N], int8 symmetric per-vocab-row lm_head scale, lowest-index argmax
  * tie-break, NaN counted as -inf) are the plainest ones the rest supports;
@@ -277,6 +281,56 @@ void oracle_ngram_draft(const int32_t *ctx, const int32_t *len, int B, int ld, i
         }
         if (match_out) match_out[b] = found_n;
     }
+}
+
+/* ------------------------------------------------ gated delta recurrence --
+ * The recurrent state of a Gated DeltaNet layer, which the pages name as most
+ * of the target's layers and whose state a rejected draft corrupted
+ * ("Efficient LLM Challenge Results", section 3, runner-up paragraph; "DFlash
+ * K=15 for Qwen3.5-4B on a single A10G", section "What transfers": rejected
+ * drafts can corrupt a recurrent state).  The recurrence is the one of Yang
+ * et al., "Gated Delta Networks: Improving Mamba2 with Delta Rule", the first
+ * page's reference [12].  One head, state S
+ * [dv][dk], per position t with key k_t [dk], value v_t [dv], query q_t
+ * [dk], decay alpha_t and write strength beta_t:
+ *     S_t = alpha_t * S_{t-1} * (I - beta_t k_t k_t^T) + beta_t * v_t k_t^T
+ *     o_t = S_t q_t
+ * written as the matrix products they are (O(dv dk^2) per step, no
+ * shortcut).  S_out is the state after the T positions.                    */
+void oracle_gdn_recurrence(const double *S0, const double *q, const double *k, const double *v,
+                           const double *alpha, const double *beta, int T, int dk, int dv,
+                           double *o, double *S_out)
+{
+    double *S = (double *)malloc(sizeof(double) * (size_t)dv * dk);
+    double *P = (double *)malloc(sizeof(double) * (size_t)dv * dk);
+    double *G = (double *)malloc(sizeof(double) * (size_t)dk * dk);
+    for (size_t i = 0; i < (size_t)dv * dk; ++i) S[i] = S0[i];
+    for (int t = 0; t < T; ++t) {
+        const double *kt = k + (size_t)t * dk, *vt = v + (size_t)t * dv, *qt = q + (size_t)t * dk;
+        /* G = I - beta k k^T */
+        for (int m = 0; m < dk; ++m)
+            for (int j = 0; j < dk; ++j) G[(size_t)m * dk + j] = (m == j ? 1.0 : 0.0) - beta[t] * kt[m] * kt[j];
+        /* P = S G */
+        for (int i = 0; i < dv; ++i)
+            for (int j = 0; j < dk; ++j) {
+                double acc = 0.0;
+                for (int m = 0; m < dk; ++m) acc += S[(size_t)i * dk + m] * G[(size_t)m * dk + j];
+                P[(size_t)i * dk + j] = acc;
+            }
+        /* S = alpha P + beta v k^T */
+        for (int i = 0; i < dv; ++i)
+            for (int j = 0; j < dk; ++j) S[(size_t)i * dk + j] = alpha[t] * P[(size_t)i * dk + j] + beta[t] * vt[i] * kt[j];
+        /* o = S q */
+        for (int i = 0; i < dv; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * qt[j];
+            o[(size_t)t * dv + i] = acc;
+        }
+    }
+    for (size_t i = 0; i < (size_t)dv * dk; ++i) S_out[i] = S[i];
+    free(S);
+    free(P);
+    free(G);
 }
 
 /* Number of OpenMP threads the parallel loops above may use (1 without OpenMP). */

@@ -191,3 +191,17 @@ def ngram_contexts(seed: int, B: int, ld: int, V: int, *tags, copy_prob: float =
                     ctx[b, pos + i] = ctx[b, src + i]
             pos += n
     return ctx, lens
+
+
+def toy_gdn_arrays(seed: int, H: int = 256, heads: int = 2):
+    """Weights of the toy model's gated-delta layer: a fused W4A16 q|k|v
+    projection H -> 3H, a W4A16 output projection H -> H, and fp16 gate
+    vectors [heads][H] for the decay (alpha) and the write strength (beta)."""
+    q_qkv = w4_codes(seed, 3 * H, H, "toy-gdn", "qkv")
+    s_qkv = w4_scales(seed, 3 * H, H, "toy-gdn", "qkv")
+    q_o = w4_codes(seed, H, H, "toy-gdn", "o")
+    s_o = w4_scales(seed, H, H, "toy-gdn", "o")
+    r = rng(seed, "toy-gdn-gates", heads, H)
+    wa = (r.standard_normal(size=(heads, H)) / np.sqrt(H)).astype(np.float16)
+    wb = (r.standard_normal(size=(heads, H)) / np.sqrt(H)).astype(np.float16)
+    return q_qkv, s_qkv, q_o, s_o, wa, wb

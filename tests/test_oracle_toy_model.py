@@ -96,3 +96,62 @@ def test_toy_model_is_context_dependent():
     assert len(outs) >= 4
     seq = greedy_decode(w, [1, 2, 3], 24)
     assert len(set(seq)) >= 3
+
+
+# ------------------------------------------------- recurrent (gated-delta) state
+def _weights_gdn(seed, V):
+    E, layers, W8, s8 = inputs.toy_model_arrays(seed, V=V, H=256, layers=2)
+    return ToyWeights(E, layers, W8, s8, gdn=inputs.toy_gdn_arrays(seed, H=256, heads=2))
+
+
+GDN_CASES = (("random", 15), ("perfect_then_wrong", 15), ("padded", 20), ("sentinel", 20),
+             ("ngram", 15), ("perfect", 4), ("random", 0))
+
+
+def test_spec_decode_equals_greedy_with_recurrent_state():
+    """With a gated-delta layer, speculative decoding commits only the accepted
+    prefix of each verify block and still emits exactly the greedy tokens
+    (greedy recomputes the state from the first token at every step)."""
+    w = _weights_gdn(21, 64)
+    n_new = 16
+    for p in range(3):
+        prompt = inputs.random_tokens(300 + p, 2 + p, 64)
+        want = greedy_decode(w, prompt, n_new)
+        drafters = _drafters(w, 3000 + p)
+        for name, K in GDN_CASES:
+            stats = {}
+            got = spec_decode(w, prompt, n_new, K, drafters[name], stats)
+            assert got == want, (p, name, K)
+            if name == "perfect":
+                assert stats["steps"] == -(-n_new // (K + 1))
+
+
+def test_invariant_catches_a_corrupted_recurrent_state():
+    """The two failures the pages describe, planted in the oracle on the CPU:
+    committing the rejected positions' updates, or never advancing the state
+    (a stale state), each change the emitted tokens for some prompt."""
+    w = _weights_gdn(22, 64)
+    n_new = 16
+    caught = {"all": False, "none": False}
+    for p in range(4):
+        prompt = inputs.random_tokens(400 + p, 3, 64)
+        want = greedy_decode(w, prompt, n_new)
+        for mode in caught:
+            rng = np.random.default_rng(4000 + p)
+            drafter = lambda ctx, K: [int(x) for x in rng.integers(0, 64, K)]
+            if spec_decode(w, prompt, n_new, 15, drafter, commit=mode) != want:
+                caught[mode] = True
+        if all(caught.values()):
+            break
+    assert caught == {"all": True, "none": True}
+
+
+def test_recurrent_state_matters():
+    """The layer's state changes the tokens: the same context with the state
+    reset to zero before the last position gives different logits."""
+    from oracle.toy_model import logits_at
+    w = _weights_gdn(23, 64)
+    toks = inputs.random_tokens(500, 12, 64)
+    L1 = logits_at(w, toks, [11])
+    L0 = logits_at(w, toks, [11], state=w.zero_state())
+    assert not np.allclose(L1, L0)
