@@ -169,7 +169,10 @@ def capture(torch, fn):
     return g
 
 
-LM_HEAD_SOURCES = ("w8_lmhead_argmax.cu", "sm103_ptx.cuh", "runtime.h")
+# The lm_head kernel's device code: its source and the PTX helpers it inlines
+# (runtime.h, also included, holds host-side launch declarations of every
+# kernel family and changes whenever one is added).
+LM_HEAD_SOURCES = ("w8_lmhead_argmax.cu", "sm103_ptx.cuh")
 LM_HEAD_PROFILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "w8_lmhead_argmax_m16.md")
 
 
@@ -330,6 +333,7 @@ def run_gpu(args, rank, world):
         result["prefill"] = run_prefill(dev, w4v, torch, peaks)
         result["lmhead_batched"] = run_lmhead_batched(dev, w4v, torch, peaks)
     result["ngram_draft"] = run_ngram(dev, w4v, torch)
+    result["gdn_state"] = run_gdn(dev, w4v, torch)
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(step)
     return result
@@ -605,6 +609,36 @@ def run_ngram(dev, w4v, torch):
                                         for _ in range(20)]) / 20
         out["B=%d,L=%d" % (B, ld)] = {"us": round(ms * 1e3, 2), "n_min": 1, "n_max": 4, "K": 23,
                                       "GB/s": round(B * ld * 4 / (ms * 1e-3) / 1e9, 1)}
+    return out
+
+
+def run_gdn(dev, w4v, torch):
+    """Recurrent-state handling of one Gated DeltaNet layer across a verify
+    block of 16 positions: gdn_verify (outputs, state read) then gdn_commit
+    (replay of the accepted prefix, state written), assumed head shape
+    32 heads x 128 x 128, for 1 and 8 sequences."""
+    out = {}
+    H, d, T = 32, 128, 16
+    g = torch.Generator(device=dev)
+    g.manual_seed(SEED)
+    for B in (1, 8):
+        S = torch.randn((B, H, d, d), generator=g, device=dev)
+        q = torch.nn.functional.normalize(torch.randn((B, T, H, d), generator=g, device=dev), dim=-1).half()
+        k = torch.nn.functional.normalize(torch.randn((B, T, H, d), generator=g, device=dev), dim=-1).half()
+        v = torch.randn((B, T, H, d), generator=g, device=dev).half()
+        a = torch.rand((B, T, H), generator=g, device=dev) * 0.5 + 0.5
+        be = torch.rand((B, T, H), generator=g, device=dev)
+        n = torch.full((B,), T - 1, dtype=torch.int32, device=dev)
+        o = torch.empty((B, T, H, d), dtype=torch.float16, device=dev)
+
+        def step():
+            w4v.gdn_verify(S, q, k, v, a, be, out=o)
+            w4v.gdn_commit(S, k, v, a, be, n)
+
+        ms = time_graph(torch, lambda: [step() for _ in range(20)]) / 20
+        state_bytes = 3 * B * H * d * d * 4          # verify read, commit read + write
+        out["B=%d" % B] = {"us": round(ms * 1e3, 2), "T": T, "heads": H, "dk": d, "dv": d,
+                           "state_GB/s": round(state_bytes / (ms * 1e-3) / 1e9, 1)}
     return out
 
 

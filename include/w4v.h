@@ -239,6 +239,39 @@ w4v_status ngram_draft(const int32_t *context, const int32_t *lengths, int B, in
                        int n_max, int K, int32_t *drafts, int32_t *match_len,
                        void *workspace, size_t workspace_bytes, w4v_stream_t stream);
 
+/* --------------------------------------------------- gdn_verify / gdn_commit
+ * The Gated DeltaNet recurrent state across a verify block, rolled back
+ * under rejection.  Most of the target's layers are Gated DeltaNet, and a
+ * rejected draft must not leave its update in their state ("Efficient LLM
+ * Challenge Results", section 3, runner-up paragraph; "DFlash K=15 for
+ * Qwen3.5-4B on a single A10G", "What transfers").  Per sequence b and head
+ * h, with the recurrence of the first page's reference [12]:
+ *     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *     o_t = S_t q_t,
+ * S the state [dv][dk] (row i = value index, column j = key index).
+ * gdn_verify runs the T positions of a verify block from the committed state
+ * and writes o_t for every t; it never writes the state.  gdn_commit then
+ * advances the committed state in place by positions 0..n_accepted[b] of the
+ * block (the last context token and the accepted drafts; n is clamped to
+ * [0, T-1]), so the rejected positions leave no trace.  Keys and queries are
+ * used as given (Gated DeltaNet normalises them to unit length upstream).
+ *   state       device, fp32 [B][H][dv][dk] (read by gdn_verify, read and
+ *               written by gdn_commit)
+ *   q, k        device, fp16 [B][T][H][dk]  (gdn_commit takes no q)
+ *   v           device, fp16 [B][T][H][dv]
+ *   alpha, beta device, fp32 [B][T][H]
+ *   o           device, fp16 [B][T][H][dv] (written; fp32 arithmetic inside)
+ *   n_accepted  device, int32 [B] (as written by spec_accept or
+ *               w8_lmhead_argmax_accept)
+ * Sizes: 0 <= B <= 65535 (0 is a no-op), 1 <= T <= 64, 1 <= H <= 65535,
+ * dk == 128, dv a multiple of 32 up to 4096.  No workspace. */
+w4v_status gdn_verify(const float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const float *alpha, const float *beta, int B, int T, int H, int dk, int dv,
+                      uint16_t *o, w4v_stream_t stream);
+w4v_status gdn_commit(float *state, const uint16_t *k, const uint16_t *v, const float *alpha,
+                      const float *beta, const int32_t *n_accepted, int B, int T, int H, int dk,
+                      int dv, w4v_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,7 @@ LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "libw4v.so")
 SOURCES = ("runtime.cu", "api.cpp", "spec_accept.cu", "w4a16_gemm.cu", "w4a16_prefill.cu",
            "w8_lmhead_argmax.cu", "lmhead_noalloc.cu",
-           "ngram_draft.cu")
+           "ngram_draft.cu", "gdn_state.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]

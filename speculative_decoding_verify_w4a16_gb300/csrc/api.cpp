@@ -186,6 +186,42 @@ w4v_status ngram_draft(const int32_t *context, const int32_t *lengths, int B, in
                                    reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+w4v_status gdn_check(const float *state, const uint16_t *k, const uint16_t *v, const float *alpha,
+                     const float *beta, int B, int T, int H, int dk, int dv) {
+    if (B < 0 || B > 65535 || T < 1 || T > w4v::kGdnMaxT || H < 1 || H > 65535 || dk != w4v::kGdnDk || dv < 32 ||
+        dv % 32 != 0 || dv > 4096)
+        return W4V_ERR_SHAPE;
+    if (B == 0) return W4V_OK;
+    if (state == nullptr || k == nullptr || v == nullptr || alpha == nullptr || beta == nullptr) return W4V_ERR_ARG;
+    if (!w4v::aligned16(state) || !w4v::aligned16(k) || !w4v::aligned16(v) ||
+        (reinterpret_cast<uintptr_t>(alpha) & 3u) || (reinterpret_cast<uintptr_t>(beta) & 3u))
+        return W4V_ERR_ALIGN;
+    return W4V_OK;
+}
+}  // namespace
+
+w4v_status gdn_verify(const float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const float *alpha, const float *beta, int B, int T, int H, int dk, int dv, uint16_t *o,
+                      w4v_stream_t stream) {
+    w4v_status st = gdn_check(state, k, v, alpha, beta, B, T, H, dk, dv);
+    if (st != W4V_OK || B == 0) return st;
+    if (q == nullptr || o == nullptr) return W4V_ERR_ARG;
+    if (!w4v::aligned16(q) || !w4v::aligned16(o)) return W4V_ERR_ALIGN;
+    return w4v::launch_gdn(false, const_cast<float *>(state), q, k, v, alpha, beta, nullptr, o, B, T, H, dv,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+w4v_status gdn_commit(float *state, const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta,
+                      const int32_t *n_accepted, int B, int T, int H, int dk, int dv, w4v_stream_t stream) {
+    w4v_status st = gdn_check(state, k, v, alpha, beta, B, T, H, dk, dv);
+    if (st != W4V_OK || B == 0) return st;
+    if (n_accepted == nullptr) return W4V_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(n_accepted) & 3u) return W4V_ERR_ALIGN;
+    return w4v::launch_gdn(true, state, nullptr, k, v, alpha, beta, n_accepted, nullptr, B, T, H, dv,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
 w4v_status spec_accept(const int32_t *target, const int32_t *draft, int B, int K, int32_t *n_accepted,
                        int32_t *out_tokens, w4v_stream_t stream) {
     if (B < 0 || K < 0 || K > 1024) return W4V_ERR_SHAPE;

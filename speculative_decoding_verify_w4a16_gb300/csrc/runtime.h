@@ -104,6 +104,13 @@ size_t ngram_ws_bytes(int B);
 w4v_status launch_ngram_draft(const int32_t *context, const int32_t *lengths, int B, long long ld, int n_min,
                               int n_max, int K, int32_t *draft, int32_t *match, void *ws, cudaStream_t stream);
 
+// Gated DeltaNet state over a verify block: key width and longest block.
+constexpr int kGdnDk = 128;
+constexpr int kGdnMaxT = 64;
+w4v_status launch_gdn(bool commit, float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const float *alpha, const float *beta, const int32_t *n_accepted, uint16_t *o, int B, int T,
+                      int H, int dv, cudaStream_t stream);
+
 // Greedy acceptance fused into the lm_head's last CTA: the M = B*(n_draft+1)
 // rows are B verify blocks of n_draft+1 positions each.
 struct LmAccept {

@@ -70,6 +70,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.ngram_draft_workspace_bytes.restype = S
             lib.ngram_draft.argtypes = [P, P, I, I, I, I, I, P, P, P, S, P]
             lib.ngram_draft.restype = I
+            lib.gdn_verify.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P]
+            lib.gdn_verify.restype = I
+            lib.gdn_commit.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P]
+            lib.gdn_commit.restype = I
             _lib = lib
     return _lib
 
@@ -243,3 +247,27 @@ def ngram_draft(context, lengths, n_min: int, n_max: int, K: int, out=None, matc
                               _ptr(out) if K > 0 else None, _ptr(match), _ptr(ws), ws.numel(), _stream(stream))
     _check(code, "ngram_draft")
     return out, match
+
+
+def gdn_verify(state, q, k, v, alpha, beta, out=None, stream=None):
+    """Outputs o [B][T][H][dv] (fp16) of the gated delta recurrence over a verify block,
+    from the committed fp32 state [B][H][dv][dk]; the state is not written."""
+    import torch
+    B, H, dv, dk = state.shape
+    T = q.shape[1]
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=torch.float16, device=state.device)
+    code = load().gdn_verify(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), B, T, H, dk, dv,
+                             _ptr(out), _stream(stream))
+    _check(code, "gdn_verify")
+    return out
+
+
+def gdn_commit(state, k, v, alpha, beta, n_accepted, stream=None):
+    """Advance the committed state in place by positions 0..n_accepted[b] of the block."""
+    B, H, dv, dk = state.shape
+    T = k.shape[1]
+    code = load().gdn_commit(_ptr(state), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(n_accepted), B, T, H,
+                             dk, dv, _stream(stream))
+    _check(code, "gdn_commit")
+    return state

@@ -14,7 +14,8 @@ FAKE = 0x10000          # an aligned, never-dereferenced stand-in pointer
 def test_exports_every_header_function(w4v_mod):
     names = w4v_mod.header_functions()
     for required in ("w4v_init", "w4v_get_status", "w4v_pack_int4", "w4a16_gemm",
-                     "w8_lmhead_argmax", "spec_accept", "w8_lmhead_argmax_accept", "ngram_draft"):
+                     "w8_lmhead_argmax", "spec_accept", "w8_lmhead_argmax_accept", "ngram_draft",
+                     "gdn_verify", "gdn_commit"):
         assert required in names
     lib = w4v_mod.load()
     for name in names:
@@ -135,6 +136,19 @@ def test_argument_validation_before_launch(w4v_mod):
     assert ng(FAKE, FAKE, 4, 100, 1, 3, 8, FAKE, None, FAKE, 16, None) == w4v_mod.ERR_WORKSPACE
     assert ng(None, None, 0, 100, 1, 3, 8, None, None, None, 0, None) == w4v_mod.OK
     assert w4v_mod.load().ngram_draft_workspace_bytes(8) >= 8 * 12
+    # gdn_verify / gdn_commit
+    gv, gc = lib.gdn_verify, lib.gdn_commit
+    assert gv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 16, 4, 64, 128, FAKE, None) == w4v_mod.ERR_SHAPE    # dk != 128
+    assert gv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 65, 4, 128, 128, FAKE, None) == w4v_mod.ERR_SHAPE   # T > 64
+    assert gv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 0, 4, 128, 128, FAKE, None) == w4v_mod.ERR_SHAPE
+    assert gv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 16, 4, 128, 100, FAKE, None) == w4v_mod.ERR_SHAPE   # dv % 32
+    assert gv(FAKE, None, FAKE, FAKE, FAKE, FAKE, 1, 16, 4, 128, 128, FAKE, None) == w4v_mod.ERR_ARG
+    assert gv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 16, 4, 128, 128, None, None) == w4v_mod.ERR_ARG
+    assert gv(FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 16, 4, 128, 128, FAKE, None) == w4v_mod.ERR_ALIGN
+    assert gv(None, None, None, None, None, None, 0, 16, 4, 128, 128, None, None) == w4v_mod.OK
+    assert gc(FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 16, 4, 128, 128, None) == w4v_mod.ERR_ARG
+    assert gc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, 1, 16, 4, 128, 128, None) == w4v_mod.ERR_ALIGN
+    assert gc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 16, 0, 128, 128, None) == w4v_mod.ERR_SHAPE
     # packer
     assert lib.w4v_pack_int4(None, 128, 128, FAKE) == w4v_mod.ERR_ARG
     buf = ctypes.create_string_buffer(16)
