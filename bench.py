@@ -131,22 +131,45 @@ class VerifyStep:
                     self.host[p.name] = (q, s)
                 layer.append((p, t(w4v.pack_int4(q)), t(s)))
             self.projs.append(layer)
-        self.acts = {p.name: t(inputs.activations(SEED, M, p.K, "bench", p.name)) for p in inputs.LAYER_PROJS}
+        # the step's inputs (every projection's activations, the lm_head rows,
+        # the drafts) live in one device buffer, so that the end-to-end run
+        # moves them with one host -> device copy; likewise the outputs read
+        # back (accepted length, emitted tokens) in one buffer
+        host_in = [(p.name, inputs.activations(SEED, M, p.K, "bench", p.name)) for p in inputs.LAYER_PROJS]
+        host_in.append(("X", inputs.activations(SEED, M, H, "bench", "lm")))
+        d = inputs.rng(SEED, "bench-drafts").integers(0, V, size=(1, K_DRAFT)).astype(np.int32)
+        host_in.append(("draft", d))
+        offs, off = {}, 0
+        for name, a in host_in:
+            offs[name] = off
+            off += (a.nbytes + 255) // 256 * 256
+        self.in_host = torch.empty(off, dtype=torch.uint8).pin_memory()
+        hv = self.in_host.numpy()
+        for name, a in host_in:
+            hv[offs[name]:offs[name] + a.nbytes] = np.ascontiguousarray(a).view(np.uint8).reshape(-1)
+        self.in_dev = self.in_host.to(dev)
+
+        def view(name, a):
+            dt = torch.float16 if a.dtype == np.float16 else torch.int32
+            return self.in_dev[offs[name]:offs[name] + a.nbytes].view(dt).view(*a.shape)
+
+        src = dict(host_in)
+        self.acts = {p.name: view(p.name, src[p.name]) for p in inputs.LAYER_PROJS}
         self.outs = {p.name: torch.empty((M, p.N), dtype=torch.float16, device=dev) for p in inputs.LAYER_PROJS}
         self.ws = {p.name: w4v.workspace(w4v.w4a16_workspace_bytes(M, p.N, p.K), dev) for p in inputs.LAYER_PROJS}
         W8, s8 = inputs.lmhead_weights(SEED, V, H, "bench")
         self.host["lm"] = (W8, s8)
         self.W8, self.s8 = t(W8), t(s8)
-        self.X = t(inputs.activations(SEED, M, H, "bench", "lm"))
+        self.X = view("X", src["X"])
         self.host["acts"] = {k: v.cpu().numpy() for k, v in self.acts.items()}
         self.host["X"] = self.X.cpu().numpy()
         self.tok = torch.empty(M, dtype=torch.int32, device=dev)
         self.ws_lm = w4v.workspace(w4v.w8_lmhead_argmax_workspace_bytes(M, V), dev)
         # drafts: fixed from the seed (the synthetic verify rows do not depend on them)
-        d = inputs.rng(SEED, "bench-drafts").integers(0, V, size=(1, K_DRAFT)).astype(np.int32)
-        self.draft = t(d)
-        self.n_acc = torch.empty(1, dtype=torch.int32, device=dev)
-        self.out_tok = torch.empty((1, K_DRAFT + 1), dtype=torch.int32, device=dev)
+        self.draft = view("draft", src["draft"])
+        self.out_dev = torch.empty(2 + K_DRAFT + 1, dtype=torch.int32, device=dev)
+        self.n_acc = self.out_dev[0:1]
+        self.out_tok = self.out_dev[2:].view(1, K_DRAFT + 1)
         self.launches_per_step = len(inputs.LAYER_PROJS) + 1
 
     def enqueue(self, copy):
@@ -341,21 +364,13 @@ def run_gpu(args, rank, world):
 
 def run_e2e(args, step, torch, total_bytes, world):
     """Host buffers in, accepted tokens out, through the same calls, one graph per step."""
-    names = [p.name for p in inputs.LAYER_PROJS]
-    h_acts = {n: torch.from_numpy(step.host["acts"][n]).pin_memory() for n in names}
-    h_X = torch.from_numpy(step.host["X"]).pin_memory()
-    h_d = step.draft.cpu().pin_memory()
-    h_n = torch.empty(1, dtype=torch.int32).pin_memory()
-    h_tok = torch.empty((1, K_DRAFT + 1), dtype=torch.int32).pin_memory()
+    h_out = torch.empty(step.out_dev.numel(), dtype=torch.int32).pin_memory()
+    h_n = h_out[0:1]
 
     def body(c):
-        for n in names:
-            step.acts[n].copy_(h_acts[n], non_blocking=True)
-        step.X.copy_(h_X, non_blocking=True)
-        step.draft.copy_(h_d, non_blocking=True)
+        step.in_dev.copy_(step.in_host, non_blocking=True)     # all of the step's inputs
         step.enqueue(c)
-        h_n.copy_(step.n_acc, non_blocking=True)
-        h_tok.copy_(step.out_tok, non_blocking=True)
+        h_out.copy_(step.out_dev, non_blocking=True)           # accepted length + emitted tokens
 
     for c in range(COPIES):
         body(c)
@@ -373,12 +388,13 @@ def run_e2e(args, step, torch, total_bytes, world):
         torch.cuda.current_stream().synchronize()     # the host reads the accepted tokens every step
         _ = int(h_n[0])
     ms = reduce_step_time((time.perf_counter() - t0) / steps * 1e3, world, step.draft.device)
-    h2d = sum(v.numel() * v.element_size() for v in h_acts.values()) + h_X.numel() * 2 + h_d.numel() * 4
-    d2h = h_n.numel() * 4 + h_tok.numel() * 4
+    h2d = step.in_host.numel()
+    d2h = h_out.numel() * 4
     return {"value": round(job_value(total_bytes, ms, world), 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "how": "pinned host -> device activations and drafts, one CUDA graph of the step, "
-                   "device -> host accepted tokens, host synchronize each step (wall clock)"}
+            "how": "one pinned host -> device copy of all activations and drafts, one CUDA graph of the step, "
+                   "one device -> host copy of the accepted length and tokens, host synchronize each step "
+                   "(wall clock)"}
 
 
 def time_graph(torch, fn, reps=3):
