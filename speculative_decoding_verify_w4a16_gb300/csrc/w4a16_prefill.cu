@@ -16,15 +16,17 @@
 // relative, which keeps the output within the 2e-3 relative bound.
 //
 // Design:
-//   * Two CTAs per SM (each one copy per ~650 cycles, so two double the copy
-//     rate; one CTA's epilogue overlaps the other's MMAs).  A CTA computes
-//     128 weight rows x 128 activation rows over the whole K, tile after tile.
-//   * Per 128-k group: one 8 KB bulk copy of packed int4 and one 32 KB 3-D
-//     TMA of the activation slice (128-byte swizzle), double-buffered.
+//   * One CTA per SM computes 128 weight rows x 256 activation rows over the
+//     whole K, tile after tile.  An M128 N256 K16 MMA takes ~136 cycles to
+//     issue against ~96 for N = 128, so the wide tile lets one issuing
+//     thread keep the tensor cores ~90% busy (two CTAs per SM with N = 128
+//     tiles reached ~50%).
+//   * Per 128-k group: one 8 KB bulk copy of packed int4 and one 64 KB 3-D
+//     TMA of the activation slice (128-byte swizzle), three stages.
 //   * Four dequant warps turn a group into fp16 s * (q - z) and write it into
 //     tensor memory (64-column tcgen05.st); one thread issues eight
 //     tcgen05.mma.kind::f16 per group with A = weights from TMEM (M = 128),
-//     B = activations from shared memory (N = 128), D in TMEM.
+//     B = activations from shared memory (N = 256), D in TMEM.
 //   * Four epilogue warps read the finished tile (32-column tcgen05.ld),
 //     round to fp16 and store C.
 #include "runtime.h"
@@ -34,15 +36,15 @@ namespace w4v {
 namespace {
 
 constexpr int kTileN = 128;                       // weight rows per tile (MMA M)
-constexpr int kTileM = 128;                       // activation rows per tile (MMA N)
+constexpr int kTileM = 256;                       // activation rows per tile (MMA N)
 constexpr int kGroup = 128;
 constexpr int kBlockBytes = kTileN * kGroup / 2;  // 8 KB packed per (tile, group)
-constexpr int kActBox = kTileM * 128;             // one 64-k block of activations, 16 KB
-constexpr int kAct = 2 * kActBox;                 // one group, 32 KB
-constexpr int kStage = kAct + kBlockBytes;        // 40 KB, 1024-aligned
-constexpr int kStages = 2;
+constexpr int kActBox = kTileM * 128;             // one 64-k block of activations, 32 KB
+constexpr int kAct = 2 * kActBox;                 // one group, 64 KB
+constexpr int kStage = kAct + kBlockBytes;        // 72 KB, 1024-aligned
+constexpr int kStages = 3;
 constexpr int kASlots = 2;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAcol0 = 0;
 constexpr uint32_t kDcol0 = kASlots * 64;
 constexpr int kWarpProd = 0;
@@ -56,6 +58,7 @@ constexpr int kNumBars = 2 * kStages + 2 * kASlots + 2 + 1;
 constexpr int kMisc = kBar + 8 * kNumBars;
 constexpr int kBytes = kMisc + 64 + 1024;
 static_assert(kStage % 1024 == 0, "stage alignment");
+static_assert(kBytes <= 227 * 1024, "shared memory plan");
 static_assert(kDcol0 + kTileM <= kTmemCols, "tensor memory plan");
 
 struct Args {
@@ -71,7 +74,7 @@ struct Args {
 // kG32: group size 32, so each 32-k chunk of a 128-k block has its own
 // scale and zero point (four per block instead of one).
 template <bool kG32>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -333,7 +336,7 @@ w4v_status launch_w4a16_prefill(const uint16_t *A, const void *Bq, const uint16_
                              CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != W4V_OK) return st;
     const long long tiles = (long long)a.n_tiles_n * a.n_tiles_m;
-    const int grid = static_cast<int>(std::min<long long>(2LL * info->sm_count, tiles));
+    const int grid = static_cast<int>(std::min<long long>(info->sm_count, tiles));
     return group == 32 ? launch<true>(xmap, a, grid, stream) : launch<false>(xmap, a, grid, stream);
 }
 
