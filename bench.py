@@ -559,15 +559,17 @@ def run_prefill(dev, w4v, torch, peaks):
             sc = (torch.rand(((p.K // 128), p.N), generator=g, device=dev) * 0.015 + 0.005).half()
             A = torch.randn((M, p.K), generator=g, device=dev).half()
             C = torch.empty((M, p.N), device=dev, dtype=torch.float16)
-            projs.append((p, packed, sc, A, C))
+            ws = w4v.workspace(w4v.w4a16_workspace_bytes(M, p.N, p.K), dev)
+            projs.append((p, packed, sc, A, C, ws))
 
         def run():
-            for (p, packed, sc, A, C) in projs:
-                w4v.w4a16_gemm(A, packed, sc, p.N, out=C)
+            for (p, packed, sc, A, C, ws) in projs:
+                w4v.w4a16_gemm(A, packed, sc, p.N, out=C, ws=ws)
 
         per = {}
-        for (p, packed, sc, A, C) in projs:
-            ms = time_graph(torch, lambda p=p, packed=packed, sc=sc, A=A, C=C: w4v.w4a16_gemm(A, packed, sc, p.N, out=C))
+        for (p, packed, sc, A, C, ws) in projs:
+            ms = time_graph(torch, lambda p=p, packed=packed, sc=sc, A=A, C=C, ws=ws:
+                            w4v.w4a16_gemm(A, packed, sc, p.N, out=C, ws=ws))
             per[p.name] = round(2.0 * M * p.N * p.K / (ms * 1e-3) / 1e12, 1)
         ms = time_graph(torch, run)
         flop = sum(2.0 * M * p.N * p.K for p in inputs.LAYER_PROJS)

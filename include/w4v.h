@@ -111,8 +111,11 @@ w4v_status w4v_unpack_int4(const void *packed_host, int N, int K, uint8_t *q_hos
  *   C        device, fp16 [M][N] (written, never read)
  * Sizes: M >= 0 (M == 0 is a no-op), N % 8 == 0, K % 128 == 0.
  * Workspace: w4a16_workspace_bytes(M, N, K) bytes, zero-filled before first
- * use (split-K partial sums and per-tile arrival counters; M > 32 uses
- * none and may pass NULL). */
+ * use: fp32 partial sums of output tiles whose k range is split between
+ * CTAs, and one arrival counter per tile.  About 1 MB for M <= 32; for
+ * M > 32, 256 KB per 128 x 256 output tile when there are at most 1024
+ * tiles (the kernel may then split tiles in two k halves), plus 4 bytes per
+ * tile. */
 size_t w4a16_workspace_bytes(int M, int N, int K);
 w4v_status w4a16_gemm(const uint16_t *A, const void *Bq, const uint16_t *scales,
                       const uint8_t *zeros, int group, uint16_t *C, int M, int N, int K,

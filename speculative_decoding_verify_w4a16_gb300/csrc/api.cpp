@@ -91,7 +91,7 @@ w4v_status w4v_unpack_int4(const void *packed, int N, int K, uint8_t *q) {
 
 size_t w4a16_workspace_bytes(int M, int N, int K) {
     if (M < 0 || !pack_shape_ok(N, K)) return 0;
-    if (M > w4v::kDecodeMaxRows) return 256;     // the prefill kernel needs no workspace
+    if (M > w4v::kDecodeMaxRows) return w4v::w4a16_prefill_ws_bytes(M, N, K);
     return w4v::w4a16_decode_ws_bytes(M, N, K);
 }
 
@@ -113,11 +113,11 @@ w4v_status w4a16_gemm_ex(const uint16_t *A, const void *Bq, const uint16_t *scal
     if (!w4v::aligned16(A) || !w4v::aligned16(Bq) || !w4v::aligned16(scales) ||
         (zeros != nullptr && !w4v::aligned16(zeros)))
         return W4V_ERR_ALIGN;
-    if (M > w4v::kDecodeMaxRows)
-        return w4v::launch_w4a16_prefill(A, Bq, scales, zeros, group, C, M, N, K,
-                                         reinterpret_cast<cudaStream_t>(stream));
-    if (ws == nullptr || ws_bytes < w4v::w4a16_decode_ws_bytes(M, N, K)) return W4V_ERR_WORKSPACE;
+    if (ws == nullptr || ws_bytes < w4a16_workspace_bytes(M, N, K)) return W4V_ERR_WORKSPACE;
     if (!w4v::aligned16(ws)) return W4V_ERR_ALIGN;
+    if (M > w4v::kDecodeMaxRows)
+        return w4v::launch_w4a16_prefill(A, Bq, scales, zeros, group, C, M, N, K, ws,
+                                         reinterpret_cast<cudaStream_t>(stream));
     return w4v::launch_w4a16_decode(A, Bq, scales, zeros, group, C, M, N, K, ws, (flags & W4V_STATIC_WEIGHTS) != 0u,
                                     reinterpret_cast<cudaStream_t>(stream));
 }

@@ -93,8 +93,9 @@ w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t
                                const uint8_t *zeros, int group, uint16_t *C, int M, int N, int K,
                                void *ws, bool static_weights, cudaStream_t stream);
 size_t w4a16_decode_ws_bytes(int M, int N, int K);
+size_t w4a16_prefill_ws_bytes(int M, int N, int K);
 w4v_status launch_w4a16_prefill(const uint16_t *A, const void *Bq, const uint16_t *scales, const uint8_t *zeros,
-                                int group, uint16_t *C, int M, int N, int K, cudaStream_t stream);
+                                int group, uint16_t *C, int M, int N, int K, void *ws, cudaStream_t stream);
 // Rows up to which the verify-sized (HBM-bound) kernel is used.
 constexpr int kDecodeMaxRows = 32;
 

@@ -29,6 +29,12 @@
 //     B = activations from shared memory (N = 256), D in TMEM.
 //   * Four epilogue warps read the finished tile (32-column tcgen05.ld),
 //     round to fp16 and store C.
+//   * When the last wave of tiles would leave most SMs idle and K is long
+//     enough to pay for it (down at 2048 and 8192 rows), each tile's k range
+//     is split in two halves done by two CTAs at the same time: each writes
+//     its fp32 partial tile to the workspace, and the second to arrive
+//     (acquire-release counter, no waiting) adds half 0 and half 1 in that
+//     order and writes C, so the result does not depend on timing.
 #include "runtime.h"
 #include "sm103_ptx.cuh"
 
@@ -54,7 +60,11 @@ constexpr int kWarpEp0 = 6;                       // 6..9
 constexpr int kWarps = 10;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kBar = kStages * kStage;
-constexpr int kNumBars = 2 * kStages + 2 * kASlots + 2 + 1;
+constexpr int kNumBars = 2 * kStages + 2 * kASlots + 2 + 2;
+constexpr int kPart = kTileM * kTileN;             // floats of one output tile
+// Tiles are split in two k halves only for launches of at most this many
+// tiles (the workspace holds both halves' fp32 partials of every tile).
+constexpr int kSplitMaxTiles = 1024;
 constexpr int kMisc = kBar + 8 * kNumBars;
 constexpr int kBytes = kMisc + 64 + 1024;
 static_assert(kStage % 1024 == 0, "stage alignment");
@@ -66,9 +76,23 @@ struct Args {
     const __half *scales;
     const uint8_t *zeros;
     __half *C;
+    float *partial;          // [tiles][2][kTileM][kTileN] fp32 (halves == 2)
+    uint32_t *tile_cnt;      // [tiles] arrivals, zero between calls (halves == 2)
     uint32_t *status;
     int M, N, K;
     int n_tiles_n, n_tiles_m, n_groups;
+    int halves;              // 1, or 2: each tile's k range done by two CTAs
+};
+
+// Work item i: tile i / halves, k groups [g0, g1) of half i % halves.
+struct Item {
+    int tile, half, g0, g1;
+    __device__ Item(int i, int halves, int G) {
+        tile = halves == 2 ? i >> 1 : i;
+        half = halves == 2 ? i & 1 : 0;
+        g0 = half ? G / 2 : 0;
+        g1 = (halves == 2 && !half) ? G / 2 : G;
+    }
 };
 
 // kG32: group size 32, so each 32-k chunk of a 128-k block has its own
@@ -88,11 +112,13 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     const uint32_t dfull = bar0 + 8u * (2 * kStages + 2 * kASlots);
     const uint32_t dempty = dfull + 8u;
     const uint32_t done_bar = dempty + 8u;
-    uint32_t *misc = reinterpret_cast<uint32_t *>(base + kMisc);     // [0] tmem, [1] abort
+    const uint32_t ep_bar = done_bar + 8u;                            // epilogue warps' sync
+    uint32_t *misc = reinterpret_cast<uint32_t *>(base + kMisc);     // [0] tmem, [1] abort, [2] last
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int tiles = p.n_tiles_n * p.n_tiles_m;
+    const int items = p.n_tiles_n * p.n_tiles_m * p.halves;
+    const int G = p.n_groups;
     AbortState ab{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.status};
 
     if (threadIdx.x == 0) {
@@ -107,7 +133,9 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         mbar_init(dfull, 1);
         mbar_init(dempty, 4);
         mbar_init(done_bar, 1);
+        mbar_init(ep_bar, 4);
         misc[1] = 0;
+        misc[2] = 0;
         fence_barrier_init();
     }
     if (warp == kWarpMma) {
@@ -129,10 +157,11 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             const uint64_t pol_w = l2_policy_evict_last();
             const uint64_t pol_x = l2_policy_evict_last();
             int it = 0;
-            for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-                const int tn = tile % p.n_tiles_n, tm = tile / p.n_tiles_n;
+            for (int i = blockIdx.x; i < items; i += gridDim.x) {
+                const Item w(i, p.halves, G);
+                const int tn = w.tile % p.n_tiles_n, tm = w.tile / p.n_tiles_n;
                 bool ok = true;
-                for (int g = 0; g < p.n_groups; ++g, ++it) {
+                for (int g = w.g0; g < w.g1; ++g, ++it) {
                     const int s = it % kStages;
                     if (it >= kStages && !mbar_wait(empty(s), ((it / kStages) - 1) & 1, ab)) {
                         ok = false;
@@ -155,9 +184,10 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             constexpr uint32_t idesc = idesc_f16_f32(128, kTileM);
             int it = 0, nt = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++nt) {
+            for (int i = blockIdx.x; i < items && ok; i += gridDim.x, ++nt) {
+                const Item w(i, p.halves, G);
                 if (nt > 0 && !mbar_wait(dempty, (nt - 1) & 1, ab)) break;
-                for (int g = 0; g < p.n_groups; ++g, ++it) {
+                for (int g = w.g0; g < w.g1; ++g, ++it) {
                     const int s = it % kStages;
                     const int slot = it % kASlots;
                     if (!mbar_wait(full(s), (it / kStages) & 1, ab) ||
@@ -171,7 +201,7 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                     for (int j = 0; j < kGroup / 16; ++j) {
                         const uint32_t baddr = act + (j >> 2) * kActBox + (j & 3) * 32;
                         mma_f16_ts(tmem + kDcol0, tmem + kAcol0 + slot * 64 + 8 * j, sdesc_sw128(baddr), idesc,
-                                   (g > 0 || j > 0) ? 1u : 0u);
+                                   (g > w.g0 || j > 0) ? 1u : 0u);
                     }
                     mma_commit(empty(s));
                     mma_commit(aempty(slot));
@@ -188,16 +218,18 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         const __half2 sixteenth = __float2half2_rn(0.0625f);
         int it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-            const int tn = tile % p.n_tiles_n;
+        for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
+            const Item w(i, p.halves, G);
+            const int tn = w.tile % p.n_tiles_n;
             const int n = tn * kTileN + r;
             const bool valid = n < p.N;
             // scale rows per 128-k block: 1, or 4 with group size 32
             constexpr int kSub = kG32 ? 4 : 1;
             float s_next[kSub];
 #pragma unroll
-            for (int c = 0; c < kSub; ++c) s_next[c] = valid ? __half2float(__ldg(p.scales + size_t(c) * p.N + n)) : 0.f;
-            for (int g = 0; g < p.n_groups; ++g, ++it) {
+            for (int c = 0; c < kSub; ++c)
+                s_next[c] = valid ? __half2float(__ldg(p.scales + size_t(kSub * w.g0 + c) * p.N + n)) : 0.f;
+            for (int g = w.g0; g < w.g1; ++g, ++it) {
                 const int s = it % kStages;
                 const int slot = it % kASlots;
                 float sc[kSub];
@@ -205,7 +237,7 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
 #pragma unroll
                 for (int c = 0; c < kSub; ++c) {
                     sc[c] = s_next[c];
-                    if (g + 1 < p.n_groups)
+                    if (g + 1 < w.g1)
                         s_next[c] = valid ? __half2float(__ldg(p.scales + size_t(kSub * (g + 1) + c) * p.N + n)) : 0.f;
                     z[c] = 8;
                     if (p.zeros != nullptr && valid) z[c] = __ldg(p.zeros + size_t(kSub * g + c) * p.N + n);
@@ -256,11 +288,20 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     } else if (warp >= kWarpEp0 && warp < kWarpEp0 + 4) {
         const int q = warp & 3;
         const int r = 32 * q + lane;
+        const int ep = warp - kWarpEp0;
         const uint32_t lane_base = uint32_t(32 * q) << 16;
+        uint32_t syncs = 0;
+        auto ep_sync = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ep_bar);
+            return warp_wait(ep_bar, (syncs++) & 1, ab);
+        };
         int nt = 0;
-        for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++nt) {
-            const int tn = tile % p.n_tiles_n, tm = tile / p.n_tiles_n;
+        for (int i = blockIdx.x; i < items; i += gridDim.x, ++nt) {
+            const Item w(i, p.halves, G);
+            const int tn = w.tile % p.n_tiles_n, tm = w.tile / p.n_tiles_n;
             const int n = tn * kTileN + r;
+            float *part = p.partial + (size_t(w.tile) * 2 + w.half) * kPart;
             if (!warp_wait(dfull, nt & 1, ab)) break;
             tc_fence_after();
 #pragma unroll 1
@@ -273,11 +314,50 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(dempty);
                 }
-                if (n < p.N) {
+                if (p.halves == 1) {
+                    if (n < p.N) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int m = tm * kTileM + c + j;
-                        if (m < p.M) p.C[size_t(m) * p.N + n] = __float2half_rn(__uint_as_float(d[j]));
+                        for (int j = 0; j < 32; ++j) {
+                            const int m = tm * kTileM + c + j;
+                            if (m < p.M) p.C[size_t(m) * p.N + n] = __float2half_rn(__uint_as_float(d[j]));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) __stcg(part + (c + j) * kTileN + r, __uint_as_float(d[j]));
+                }
+            }
+            if (p.halves == 1) continue;
+            // Split tile: the second half to arrive adds the two fp32 partials,
+            // half 0 first (a fixed order, so the result is deterministic).
+            if (!ep_sync()) break;
+            if (ep == 0 && lane == 0) {
+                const uint32_t prev = atom_add_acq_rel_gpu(p.tile_cnt + w.tile, 1u);
+                const bool last = prev == 1u;
+                if (last) p.tile_cnt[w.tile] = 0u;
+                misc[2] = last ? 1u : 0u;
+            }
+            if (!ep_sync()) break;
+            if (!misc[2]) continue;
+            const float4 *p0 = reinterpret_cast<const float4 *>(p.partial + size_t(w.tile) * 2 * kPart);
+            const float4 *p1 = p0 + kPart / 4;
+            constexpr int kB = 8;                     // float4s per thread in flight
+            for (int e0 = ep * 32 + lane; e0 < kPart / 4; e0 += 128 * kB) {
+                float4 a[kB], b[kB];
+#pragma unroll
+                for (int k = 0; k < kB; ++k) {
+                    a[k] = __ldcg(p0 + e0 + k * 128);
+                    b[k] = __ldcg(p1 + e0 + k * 128);
+                }
+#pragma unroll
+                for (int k = 0; k < kB; ++k) {
+                    const int e = 4 * (e0 + k * 128);      // [m][n] element, consecutive threads: consecutive n
+                    const int gm = tm * kTileM + e / kTileN, gn = tn * kTileN + e % kTileN;
+                    if (gm < p.M && gn < p.N) {             // N % 8 == 0: four n are all in or all out
+                        uint2 h;
+                        h.x = h2_as_u32(__floats2half2_rn(a[k].x + b[k].x, a[k].y + b[k].y));
+                        h.y = h2_as_u32(__floats2half2_rn(a[k].z + b[k].z, a[k].w + b[k].w));
+                        *reinterpret_cast<uint2 *>(p.C + size_t(gm) * p.N + gn) = h;
                     }
                 }
             }
@@ -314,8 +394,15 @@ w4v_status launch(const CUtensorMap &xmap, const Args &a, int grid, cudaStream_t
 
 }  // namespace
 
+size_t w4a16_prefill_ws_bytes(int M, int N, int K) {
+    (void)K;
+    const size_t tiles = ((size_t(N) + kTileN - 1) / kTileN) * ((size_t(M) + kTileM - 1) / kTileM);
+    const size_t partials = tiles <= size_t(kSplitMaxTiles) ? tiles * 2 * kPart * sizeof(float) : 0;
+    return partials + ((tiles * sizeof(uint32_t) + 255) & ~size_t(255));
+}
+
 w4v_status launch_w4a16_prefill(const uint16_t *A, const void *Bq, const uint16_t *scales, const uint8_t *zeros,
-                                int group, uint16_t *C, int M, int N, int K, cudaStream_t stream) {
+                                int group, uint16_t *C, int M, int N, int K, void *ws, cudaStream_t stream) {
     const DeviceInfo *info = nullptr;
     w4v_status st = device_info(&info);
     if (st != W4V_OK) return st;
@@ -336,7 +423,19 @@ w4v_status launch_w4a16_prefill(const uint16_t *A, const void *Bq, const uint16_
                              CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != W4V_OK) return st;
     const long long tiles = (long long)a.n_tiles_n * a.n_tiles_m;
-    const int grid = static_cast<int>(std::min<long long>(info->sm_count, tiles));
+    // Split each tile's k range in two when that shortens the launch: a
+    // whole tile costs G groups plus about 2 groups' time of epilogue, a half
+    // G/2 plus about 4 (its fp32 partial out, and for the second half the
+    // sum of both in).  E.g. down (G = 76) at 2048 rows: 160 tiles on 152
+    // SMs are two waves of whole tiles, or three of halves.
+    const long long sms = info->sm_count;
+    const long long G = a.n_groups;
+    const long long waves1 = (tiles + sms - 1) / sms, waves2 = (2 * tiles + sms - 1) / sms;
+    a.halves = (G >= 2 && tiles <= kSplitMaxTiles && waves2 * (G / 2 + 4) < waves1 * (G + 2)) ? 2 : 1;
+    const size_t part_bytes = tiles <= kSplitMaxTiles ? size_t(tiles) * 2 * kPart * sizeof(float) : 0;
+    a.partial = static_cast<float *>(ws);
+    a.tile_cnt = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + part_bytes);
+    const int grid = static_cast<int>(std::min<long long>(sms, tiles * a.halves));
     return group == 32 ? launch<true>(xmap, a, grid, stream) : launch<false>(xmap, a, grid, stream);
 }
 

@@ -68,7 +68,7 @@ def test_pack_pads_tail_rows_with_zero_point(w4v_mod):
 
 def test_workspace_sizes(w4v_mod):
     assert w4v_mod.w4a16_workspace_bytes(16, 7680, 2560) > 0
-    assert w4v_mod.w4a16_workspace_bytes(33, 512, 256) == 256       # prefill path: no workspace
+    assert w4v_mod.w4a16_workspace_bytes(33, 512, 256) >= 256 * 128 * 4   # prefill: split-tile partials
     assert w4v_mod.w4a16_workspace_bytes(-1, 512, 256) == 0
     assert w4v_mod.w4a16_workspace_bytes(16, 100, 256) == 0       # N % 8 != 0
     assert w4v_mod.w8_lmhead_argmax_workspace_bytes(128, 151936) > 0
