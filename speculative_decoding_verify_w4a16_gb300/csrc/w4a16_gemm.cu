@@ -302,9 +302,6 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    // every CTA of the cluster has initialised its barriers before any
-    // member arrives on the leader's
-    if (CL > 1) cluster_sync_all();
     grid_dep_launch();
 
     if (warp == kWarpProd) {
@@ -869,7 +866,9 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 }
             }
         }
-        cluster_sync_all();                       // nobody leaves while another CTA reads its partial
+        // nobody leaves while another CTA reads its partial (nothing to
+        // publish: a relaxed arrive, no memory barrier)
+        asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
     }
 
     // ----------------------------- stream-K split-tile fix-up (all threads)
