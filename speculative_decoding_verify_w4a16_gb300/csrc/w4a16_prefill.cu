@@ -18,9 +18,9 @@
 // Design:
 //   * One CTA per SM computes 128 weight rows x 256 activation rows over the
 //     whole K, tile after tile.  An M128 N256 K16 MMA takes ~136 cycles to
-//     issue against ~96 for N = 128, so the wide tile lets one issuing
-//     thread keep the tensor cores ~90% busy (two CTAs per SM with N = 128
-//     tiles reached ~50%).
+//     issue against ~96 for N = 128 (twice the work in 1.4x the issue
+//     time), so one issuing thread keeps the tensor pipe ~64% busy, where
+//     two CTAs per SM with N = 128 tiles reached ~50%.
 //   * Per 128-k group: one 8 KB bulk copy of packed int4 and one 64 KB 3-D
 //     TMA of the activation slice (128-byte swizzle), three stages.
 //   * Four dequant warps turn a group into fp16 s * (q - z) and write it into
