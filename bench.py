@@ -715,13 +715,37 @@ def oracle_step(host, frac=1.0):
 def cpu_baseline(step):
     import oracle
     oracle.build()
+    threads = oracle.num_threads()
     t0 = time.perf_counter()
     nbytes = oracle_step(step.host, 1.0)
     dt = time.perf_counter() - t0
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+    # the same oracle on one thread, on 1/16 of every matrix's output rows
+    oracle.set_num_threads(1)
+    try:
+        t1 = time.perf_counter()
+        nb1 = oracle_step(step.host, 1.0 / 16)
+        dt1 = time.perf_counter() - t1
+    finally:
+        oracle.set_num_threads(threads)
+    # the projections' dequantization and GEMM timed apart (all threads)
+    t_deq = t_mm = 0.0
+    for p in inputs.LAYER_PROJS:
+        q, sc = step.host[p.name]
+        t2 = time.perf_counter()
+        w = oracle.dequant_w4(q, sc)
+        t3 = time.perf_counter()
+        oracle.matmul_dequantized(step.host["acts"][p.name], w)
+        t4 = time.perf_counter()
+        t_deq += t3 - t2
+        t_mm += t4 - t3
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle", "seconds": round(dt, 2),
             "sample": "one full cfg1 verify step (4 projections + lm_head + argmax + accept), M=16, "
-                      "double precision, OpenMP over output rows"}
+                      "double precision, OpenMP over output rows",
+            "affinity_cores": _cores(), "nproc": os.cpu_count(),
+            "single_thread": {"GB/s": round(nb1 / dt1 / 1e9, 4), "seconds": round(dt1, 2),
+                              "sample": "1/16 of every matrix's output rows, one thread"},
+            "projections_split_s": {"dequant": round(t_deq, 3), "gemm": round(t_mm, 3)}}
 
 
 def host_inputs():
