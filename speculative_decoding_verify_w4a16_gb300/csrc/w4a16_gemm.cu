@@ -363,7 +363,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         // (shared and tensor memory only: ordered by the stage barriers)
         if (lane == 0) {
             const int me = warp - kWarpIss0;
-            constexpr uint32_t idesc = idesc_f16_f32(128, 16);
+            constexpr uint32_t idesc = idesc_f16_f32(128, 16 * NBLK);
             StageWalk sw(ub, nP, G, nunits);
             bool ok = true;
             int f0 = 0;                          // first unit of the stage
@@ -397,12 +397,10 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                         const uint32_t act = base_s + s * L::kStage + 2 * (kUnitGroups * jj + gg) * L::kActBox;
 #pragma unroll
                         for (int j = 0; j < kGroup / 16; ++j) {
-#pragma unroll
-                            for (int b = 0; b < NBLK; ++b) {
-                                const uint32_t baddr = act + (j >> 2) * L::kActBox + b * 2048 + (j & 3) * 32;
-                                mma_f16_ts(dset + (gg * NBLK + b) * 16, tmem + slot * kASlotCols + gg * 64 + 8 * j,
-                                           sdesc_sw128(baddr), idesc, j > 0 ? 1u : 0u);
-                            }
+                            // all 16 NBLK activation rows in one MMA (N = 16 NBLK)
+                            const uint32_t baddr = act + (j >> 2) * L::kActBox + (j & 3) * 32;
+                            mma_f16_ts(dset + gg * NBLK * 16, tmem + slot * kASlotCols + gg * 64 + 8 * j,
+                                       sdesc_sw128(baddr), idesc, j > 0 ? 1u : 0u);
                         }
                     }
                     const int commits = (mine0 ? 1 : 0) + (mine1 ? 1 : 0) + (ng == 1 ? 1 : 0);

@@ -76,8 +76,15 @@ struct Layout {
     static constexpr int kStages = (196 * 1024) / kStage > 6 ? 6 : (196 * 1024) / kStage;
     // Independent accumulators per tile: the same count for every M <= 32,
     // so the per-logit arithmetic does not depend on M there.
+    // (M = 128 keeps one accumulator and two D sets: two accumulators in a
+    // single set ran 19% slower, the tile's drain then stalling the MMAs.)
     static constexpr int kAcc = NBLK <= 2 ? 3 : 8 / NBLK;
-    static constexpr uint32_t kDSet = kAcc * 16 * NBLK;  // laid out [block][acc][16]
+    static constexpr int kDSets = 2;
+    // M <= 16: one M128 N16 MMA per k-step.  M > 16: one MMA of N = 16 NBLK
+    // per k-step (an MMA costs about the same to issue up to N = 128), D laid
+    // out [acc][block][16].
+    static constexpr bool kWide = NBLK >= 2;
+    static constexpr uint32_t kDSet = kAcc * 16 * NBLK;
     // A slots: as many 128-column units as fit beside two accumulator sets
     static constexpr int kASlots = NBLK == 1 ? 3 : 2;
     static constexpr uint32_t kDcol0 = kASlots * kASlotCols;
@@ -87,7 +94,7 @@ struct Layout {
     static constexpr int kMisc = kBest + 8 * kMaxRows;
     static constexpr int kBytes = kMisc + 64 + 1024;
     static_assert(kStage % 1024 == 0, "stage alignment");
-    static_assert(kDcol0 + 2 * kDSet <= kTmemCols, "tensor memory plan");
+    static_assert(kDcol0 + kDSets * kDSet <= kTmemCols, "tensor memory plan");
     static_assert(kBytes <= 227 * 1024, "shared memory plan");
 };
 
@@ -241,6 +248,7 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
         if (lane == 0) {
             const int me = warp - kWarpIss0;
             constexpr uint32_t idesc = idesc_f16_f32(128, 16);
+            constexpr uint32_t idesc_wide = idesc_f16_f32(128, 16 * NBLK);
             ChunkWalk cw(p.n_chunks, ntiles);
             bool ok = true;
             for (int st = 0; cw.more() && ok; ++st) {      // unit st = stage st
@@ -248,9 +256,9 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
                 const int s = st % S;
                 const int j = cw.j;
                 const int slot = st % kASlots;
-                const int buf = j & 1;
+                const int buf = j % L::kDSets, use = j / L::kDSets;   // D set and its use count
                 if (!mbar_wait(full(s), (st / S) & 1, ab) || !mbar_wait(afull(slot), (st / kASlots) & 1, ab) ||
-                    (cw.c == 0 && j >= 2 && !mbar_wait(dempty(buf), ((j >> 1) - 1) & 1, ab))) {
+                    (cw.c == 0 && use >= 1 && !mbar_wait(dempty(buf), (use - 1) & 1, ab))) {
                     ok = false;
                     break;
                 }
@@ -261,14 +269,22 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
                     const uint32_t act = base_s + s * L::kStage + 2 * jj * L::kActBox;
 #pragma unroll
                     for (int kk = 0; kk < kChunk / 16; ++kk) {
+                        const int a = kk % L::kAcc;
+                        if constexpr (L::kWide) {
+                            // accumulator a belongs to issuer a: all NBLK blocks in one MMA
+                            if (a % kIssuers != me) continue;
+                            const uint32_t baddr = act + (kk >> 2) * L::kActBox + (kk & 3) * 32;
+                            mma_f16_ts(dset + a * (16 * NBLK), tmem + kAcol0 + slot * kASlotCols + jj * 64 + 8 * kk,
+                                       sdesc_sw128(baddr), idesc_wide, (c > 0 || kk >= L::kAcc) ? 1u : 0u);
+                        } else {
 #pragma unroll
-                        for (int b = 0; b < NBLK; ++b) {
-                            const int a = kk % L::kAcc;
-                            if ((a * NBLK + b) % kIssuers != me) continue;
-                            const uint32_t baddr = act + (kk >> 2) * L::kActBox + b * 2048 + (kk & 3) * 32;
-                            mma_f16_ts(dset + (b * L::kAcc + a) * 16,
-                                       tmem + kAcol0 + slot * kASlotCols + jj * 64 + 8 * kk, sdesc_sw128(baddr),
-                                       idesc, (c > 0 || kk >= L::kAcc) ? 1u : 0u);
+                            for (int b = 0; b < NBLK; ++b) {
+                                if ((a * NBLK + b) % kIssuers != me) continue;
+                                const uint32_t baddr = act + (kk >> 2) * L::kActBox + b * 2048 + (kk & 3) * 32;
+                                mma_f16_ts(dset + (b * L::kAcc + a) * 16,
+                                           tmem + kAcol0 + slot * kASlotCols + jj * 64 + 8 * kk, sdesc_sw128(baddr),
+                                           idesc, (c > 0 || kk >= L::kAcc) ? 1u : 0u);
+                            }
                         }
                     }
                 }
@@ -375,12 +391,12 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
 
         bool ok = true;
         for (int j = 0; j < ntiles && ok; ++j) {
-            const int buf = j & 1;
+            const int buf = j % L::kDSets, use = j / L::kDSets;
             const int t = tb + j;
             const int v = t * kTileV + r;
             const bool valid = v < p.V;
             const float sc = valid ? __half2float(__ldg(p.scale + v)) : 0.f;
-            if (!warp_wait(dfull(buf), (j >> 1) & 1, ab)) {
+            if (!warp_wait(dfull(buf), use & 1, ab)) {
                 ok = false;
                 break;
             }
@@ -390,7 +406,7 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
             for (int b = 0; b < NBLK; ++b) {
                 // the block's accumulators, added in a fixed order
                 float g[16];
-                if constexpr (L::kAcc == 3) {
+                if constexpr (L::kAcc == 3 && NBLK == 1) {
                     uint32_t d01[32], d2[16];
                     tmem_ld_32x32b_x32(dset + (b * 3) * 16, d01);
                     tmem_ld_32x32b_x16(dset + (b * 3 + 2) * 16, d2);
@@ -399,12 +415,27 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj)
                         g[jj] = (__uint_as_float(d01[jj]) + __uint_as_float(d01[16 + jj])) + __uint_as_float(d2[jj]);
-                } else if constexpr (L::kAcc == 2) {
-                    uint32_t d[32];
-                    tmem_ld_32x32b_x32(dset + (b * 2) * 16, d);
-                    tc_wait_ld_keep<32>(d);
+                } else if constexpr (L::kAcc == 3) {
+                    // wide layout [acc][block][16], accumulators added in order
+                    uint32_t d0[16], d1[16], d2[16];
+                    tmem_ld_32x32b_x16(dset + b * 16, d0);
+                    tmem_ld_32x32b_x16(dset + 16 * NBLK + b * 16, d1);
+                    tmem_ld_32x32b_x16(dset + 32 * NBLK + b * 16, d2);
+                    tc_wait_ld_keep<16>(d0);
+                    tc_wait_ld_keep<16>(d1);
+                    tc_wait_ld_keep<16>(d2);
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) g[jj] = __uint_as_float(d[jj]) + __uint_as_float(d[16 + jj]);
+                    for (int jj = 0; jj < 16; ++jj)
+                        g[jj] = (__uint_as_float(d0[jj]) + __uint_as_float(d1[jj])) + __uint_as_float(d2[jj]);
+                } else if constexpr (L::kAcc == 2) {
+                    // wide layout [acc][block][16]
+                    uint32_t d0[16], d1[16];
+                    tmem_ld_32x32b_x16(dset + b * 16, d0);
+                    tmem_ld_32x32b_x16(dset + 16 * NBLK + b * 16, d1);
+                    tc_wait_ld_keep<16>(d0);
+                    tc_wait_ld_keep<16>(d1);
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) g[jj] = __uint_as_float(d0[jj]) + __uint_as_float(d1[jj]);
                 } else {
                     uint32_t d[16];
                     tmem_ld_32x32b_x16(dset + b * 16, d);

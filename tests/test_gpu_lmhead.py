@@ -127,3 +127,17 @@ def test_full_vocab_cfg1(w4v_mod, gpu, oracle_mod):
     for m in range(M):
         if tok[m] != t_o[m]:
             assert best[m] - second[m] <= 1e-3 * abs(best[m]), m
+
+
+def test_batch_invariance(w4v_mod, gpu):
+    """For M <= 32 every logit comes from the same arithmetic whatever M is:
+    the rows of a small call equal the same rows of a 32-row call bit for
+    bit (logits and tokens)."""
+    K, V = 512, 4096
+    X = inputs.activations(77, 32, K, "inv")
+    W, s = inputs.lmhead_weights(77, V, K, "inv")
+    tok32, _, L32 = _run(w4v_mod, gpu, X, W, s)
+    for m in (1, 7, 16, 17, 21):
+        tok, _, L = _run(w4v_mod, gpu, X[:m], W, s)
+        assert np.array_equal(L, L32[:m]), m
+        assert np.array_equal(tok, tok32[:m]), m
