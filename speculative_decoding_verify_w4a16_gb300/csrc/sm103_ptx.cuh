@@ -248,6 +248,31 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         : "memory");
 }
 
+// The same, executed by a whole converged warp with lane 0 alone issuing:
+// every operand is then warp-uniform (the issue loop runs in all lanes), so
+// it can live in uniform registers instead of being moved there per MMA.
+__device__ __forceinline__ void mma_f16_ts_lane0(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "mov.u32 l, %%laneid;\n\t"
+        "setp.eq.u32 e, l, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// mma_commit by lane 0 of a converged warp (the lane that issued the MMAs).
+__device__ __forceinline__ void mma_commit_lane0(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\t"
+        "mov.u32 l, %%laneid;\n\t"
+        "setp.eq.u32 e, l, 0;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
 // Arrive on `bar` once every tcgen05.mma this thread issued so far completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)

@@ -360,8 +360,10 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         }
     } else if (warp >= kWarpIss0 && warp < kWarpIss0 + kIssuers) {
         // ------------------------------------------------------ MMA issuers
-        // (shared and tensor memory only: ordered by the stage barriers)
-        if (lane == 0) {
+        // (shared and tensor memory only: ordered by the stage barriers).
+        // The whole warp runs the loop and lane 0 alone issues, so the
+        // operands stay warp-uniform.
+        {
             const int me = warp - kWarpIss0;
             constexpr uint32_t idesc = idesc_f16_f32(128, 16 * NBLK);
             StageWalk sw(ub, nP, G, nunits);
@@ -373,7 +375,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 const int s = rg.s;
                 // Every issuer waits for every stage, so its once-per-stage
                 // release below always lands in the phase of this stage.
-                if (!mbar_wait(xfull(s), rg.ph, ab)) break;
+                if (!warp_wait(xfull(s), rg.ph, ab)) break;
                 for (int jj = 0; jj < n; ++jj) {
                     const int f = f0 + jj;
                     // group gg of unit f belongs to issuer (2f + gg) % 3; a
@@ -385,8 +387,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                     if (!mine0 && !mine1) continue;
                     const int slot = f % kASlots;
                     const int set = f % DS;
-                    if (!mbar_wait(afull(slot), (f / kASlots) & 1, ab) ||
-                        (f >= DS && !mbar_wait(dempty(set), ((f / DS) - 1) & 1, ab))) {
+                    if (!warp_wait(afull(slot), (f / kASlots) & 1, ab) ||
+                        (f >= DS && !warp_wait(dempty(set), ((f / DS) - 1) & 1, ab))) {
                         ok = false;
                         break;
                     }
@@ -399,23 +401,24 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                         for (int j = 0; j < kGroup / 16; ++j) {
                             // all 16 NBLK activation rows in one MMA (N = 16 NBLK)
                             const uint32_t baddr = act + (j >> 2) * L::kActBox + (j & 3) * 32;
-                            mma_f16_ts(dset + gg * NBLK * 16, tmem + slot * kASlotCols + gg * 64 + 8 * j,
+                            mma_f16_ts_lane0(dset + gg * NBLK * 16, tmem + slot * kASlotCols + gg * 64 + 8 * j,
                                        sdesc_sw128(baddr), idesc, j > 0 ? 1u : 0u);
                         }
                     }
                     const int commits = (mine0 ? 1 : 0) + (mine1 ? 1 : 0) + (ng == 1 ? 1 : 0);
                     for (int c = 0; c < commits; ++c) {
-                        mma_commit(aempty(slot));
-                        mma_commit(dfull(set));
+                        mma_commit_lane0(aempty(slot));
+                        mma_commit_lane0(dfull(set));
                     }
                 }
-                mma_commit(empty(s));
+                mma_commit_lane0(empty(s));
                 f0 += n;
                 sw.next(n);
             }
             // Every MMA of this issuer has finished once this arrives.
-            mma_commit(done_bar);
+            mma_commit_lane0(done_bar);
             mbar_wait_bounded(done_bar, 0);
+            __syncwarp();
         }
     } else if (warp >= kWarpDq0) {
         // --------------------------------------------------------- dequant

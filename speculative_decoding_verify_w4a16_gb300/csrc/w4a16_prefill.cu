@@ -180,18 +180,20 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             }
         }
     } else if (warp == kWarpMma) {
-        if (lane == 0) {
+        // The whole warp runs the loop and lane 0 alone issues, so the
+        // operands stay warp-uniform.
+        {
             constexpr uint32_t idesc = idesc_f16_f32(128, kTileM);
             int it = 0, nt = 0;
             bool ok = true;
             for (int i = blockIdx.x; i < items && ok; i += gridDim.x, ++nt) {
                 const Item w(i, p.halves, G);
-                if (nt > 0 && !mbar_wait(dempty, (nt - 1) & 1, ab)) break;
+                if (nt > 0 && !warp_wait(dempty, (nt - 1) & 1, ab)) break;
                 for (int g = w.g0; g < w.g1; ++g, ++it) {
                     const int s = it % kStages;
                     const int slot = it % kASlots;
-                    if (!mbar_wait(full(s), (it / kStages) & 1, ab) ||
-                        !mbar_wait(afull(slot), (it / kASlots) & 1, ab)) {
+                    if (!warp_wait(full(s), (it / kStages) & 1, ab) ||
+                        !warp_wait(afull(slot), (it / kASlots) & 1, ab)) {
                         ok = false;
                         break;
                     }
@@ -200,16 +202,17 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
 #pragma unroll
                     for (int j = 0; j < kGroup / 16; ++j) {
                         const uint32_t baddr = act + (j >> 2) * kActBox + (j & 3) * 32;
-                        mma_f16_ts(tmem + kDcol0, tmem + kAcol0 + slot * 64 + 8 * j, sdesc_sw128(baddr), idesc,
+                        mma_f16_ts_lane0(tmem + kDcol0, tmem + kAcol0 + slot * 64 + 8 * j, sdesc_sw128(baddr), idesc,
                                    (g > w.g0 || j > 0) ? 1u : 0u);
                     }
-                    mma_commit(empty(s));
-                    mma_commit(aempty(slot));
+                    mma_commit_lane0(empty(s));
+                    mma_commit_lane0(aempty(slot));
                 }
-                if (ok) mma_commit(dfull);
+                if (ok) mma_commit_lane0(dfull);
             }
-            mma_commit(done_bar);
+            mma_commit_lane0(done_bar);
             mbar_wait_bounded(done_bar, 0);
+            __syncwarp();
         }
     } else if (warp >= kWarpDq0 && warp < kWarpDq0 + 4) {
         const int q = warp & 3;

@@ -244,8 +244,10 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
         }
     } else if (warp >= kWarpIss0 && warp < kWarpIss0 + kIssuers) {
         // ------------------------------------------------------ MMA issuers
+        // The whole warp runs the loop and lane 0 alone issues, so the
+        // operands stay warp-uniform.
         grid_dep_wait();
-        if (lane == 0) {
+        {
             const int me = warp - kWarpIss0;
             constexpr uint32_t idesc = idesc_f16_f32(128, 16);
             constexpr uint32_t idesc_wide = idesc_f16_f32(128, 16 * NBLK);
@@ -257,8 +259,8 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
                 const int j = cw.j;
                 const int slot = st % kASlots;
                 const int buf = j % L::kDSets, use = j / L::kDSets;   // D set and its use count
-                if (!mbar_wait(full(s), (st / S) & 1, ab) || !mbar_wait(afull(slot), (st / kASlots) & 1, ab) ||
-                    (cw.c == 0 && use >= 1 && !mbar_wait(dempty(buf), (use - 1) & 1, ab))) {
+                if (!warp_wait(full(s), (st / S) & 1, ab) || !warp_wait(afull(slot), (st / kASlots) & 1, ab) ||
+                    (cw.c == 0 && use >= 1 && !warp_wait(dempty(buf), (use - 1) & 1, ab))) {
                     ok = false;
                     break;
                 }
@@ -274,27 +276,28 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
                             // accumulator a belongs to issuer a: all NBLK blocks in one MMA
                             if (a % kIssuers != me) continue;
                             const uint32_t baddr = act + (kk >> 2) * L::kActBox + (kk & 3) * 32;
-                            mma_f16_ts(dset + a * (16 * NBLK), tmem + kAcol0 + slot * kASlotCols + jj * 64 + 8 * kk,
+                            mma_f16_ts_lane0(dset + a * (16 * NBLK), tmem + kAcol0 + slot * kASlotCols + jj * 64 + 8 * kk,
                                        sdesc_sw128(baddr), idesc_wide, (c > 0 || kk >= L::kAcc) ? 1u : 0u);
                         } else {
 #pragma unroll
                             for (int b = 0; b < NBLK; ++b) {
                                 if ((a * NBLK + b) % kIssuers != me) continue;
                                 const uint32_t baddr = act + (kk >> 2) * L::kActBox + b * 2048 + (kk & 3) * 32;
-                                mma_f16_ts(dset + (b * L::kAcc + a) * 16,
+                                mma_f16_ts_lane0(dset + (b * L::kAcc + a) * 16,
                                            tmem + kAcol0 + slot * kASlotCols + jj * 64 + 8 * kk, sdesc_sw128(baddr),
                                            idesc, (c > 0 || kk >= L::kAcc) ? 1u : 0u);
                             }
                         }
                     }
                 }
-                mma_commit(aempty(slot));
-                if (cw.c + ng == p.n_chunks) mma_commit(dfull(buf));
-                mma_commit(empty(s));
+                mma_commit_lane0(aempty(slot));
+                if (cw.c + ng == p.n_chunks) mma_commit_lane0(dfull(buf));
+                mma_commit_lane0(empty(s));
                 cw.next(ng);
             }
-            mma_commit(done_bar);
+            mma_commit_lane0(done_bar);
             mbar_wait_bounded(done_bar, 0);
+            __syncwarp();
         }
     } else if (warp >= kWarpDq0) {
         grid_dep_wait();
