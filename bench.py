@@ -794,6 +794,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-prefill", dest="prefill", action="store_false")
     ap.add_argument("--prefill-only", action="store_true", help="run only the prefill leg (profiling aid)")
+    ap.add_argument("--gdn-only", action="store_true", help="run only the gated-delta state leg (profiling aid)")
     ap.add_argument("--ref-frac", type=float, default=1.0 / 16)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -808,14 +809,17 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
-    if args.prefill_only:
+    if args.prefill_only or args.gdn_only:
         import torch
         from speculative_decoding_verify_w4a16_gb300 import _build, w4v
         _build.build()
         w4v.load()
         w4v.init()
         dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
-        print(json.dumps({"prefill": run_prefill(dev, w4v, torch, load_peaks())}), flush=True)
+        if args.prefill_only:
+            print(json.dumps({"prefill": run_prefill(dev, w4v, torch, load_peaks())}), flush=True)
+        else:
+            print(json.dumps({"gdn_state": run_gdn(dev, w4v, torch)}), flush=True)
         return
     res = run_gpu(args, rank, world)
     if rank == 0:
