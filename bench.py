@@ -362,7 +362,16 @@ def run_gpu(args, rank, world):
     result["gdn_state"] = run_gdn(dev, w4v, torch)
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(step)
+    check_device_status(w4v)
     return result
+
+
+def check_device_status(w4v):
+    """A kernel that gave up a bounded wait leaves its status word set and its
+    outputs and timings meaningless: fail loudly instead of printing them."""
+    st = w4v.get_status()
+    if st != 0:
+        raise RuntimeError("device status %d: a kernel gave up a bounded wait; the measurements are invalid" % st)
 
 
 def run_e2e(args, step, torch, total_bytes, world):
@@ -817,9 +826,11 @@ def main():
         w4v.init()
         dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
         if args.prefill_only:
-            print(json.dumps({"prefill": run_prefill(dev, w4v, torch, load_peaks())}), flush=True)
+            out = {"prefill": run_prefill(dev, w4v, torch, load_peaks())}
         else:
-            print(json.dumps({"gdn_state": run_gdn(dev, w4v, torch)}), flush=True)
+            out = {"gdn_state": run_gdn(dev, w4v, torch)}
+        check_device_status(w4v)
+        print(json.dumps(out), flush=True)
         return
     res = run_gpu(args, rank, world)
     if rank == 0:
