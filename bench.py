@@ -306,8 +306,11 @@ def run_gpu(args, rank, world):
     gemm_ms = sum(kern[p.name]["ms"] for p in inputs.LAYER_PROJS)
     gemm_gbs = proj_bytes / (gemm_ms * 1e-3) / 1e9
 
+    check_device_status(w4v, "verify step and per-kernel graphs")
+
     # ---- end to end through the public API with host buffers -----------------
     e2e = run_e2e(args, step, torch, total_bytes, world)
+    check_device_status(w4v, "end to end")
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -341,37 +344,46 @@ def run_gpu(args, rank, world):
     }
     if args.sweep:
         result["sweep"] = stack.sweep(peaks)
+        check_device_status(w4v, "36-layer sweep")
         result["verify_36_layers"] = stack.full_verify(step.W8, step.s8, peaks)
+        check_device_status(w4v, "36-layer verify")
         # a 4-bit g128 drafter of the pages' size (277 MB): five layer sets, 263 MB
         drafter = Stack(dev, w4v, torch, group=128, layers=5)
         result["drafter_5_layers"] = drafter.stack_graph(peaks)
+        check_device_status(w4v, "drafter stack")
         del drafter
         # the same kernel's streaming rate: one 200 MB projection (N = 155648,
         # K = 2560) at M = 16, where the launch's ramp and tail are amortised
         result["gemm_m16_streaming"] = run_streaming(dev, w4v, torch, peaks)
+        check_device_status(w4v, "streaming")
         # the group-size-32 W4A16 target (compressed-tensors format), same shapes
         g32 = Stack(dev, w4v, torch, group=32)
         result["gemm_m16_g32"] = g32.layer_set(peaks)
+        check_device_status(w4v, "group-32 layer set")
         del g32
     del stack
     torch.cuda.empty_cache()
     if args.prefill:
         result["prefill"] = run_prefill(dev, w4v, torch, peaks)
+        check_device_status(w4v, "prefill")
         result["lmhead_batched"] = run_lmhead_batched(dev, w4v, torch, peaks)
+        check_device_status(w4v, "batched lm_head")
     result["ngram_draft"] = run_ngram(dev, w4v, torch)
     result["gdn_state"] = run_gdn(dev, w4v, torch)
+    check_device_status(w4v, "drafter and recurrent state")
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(step)
-    check_device_status(w4v)
     return result
 
 
-def check_device_status(w4v):
-    """A kernel that gave up a bounded wait leaves its status word set and its
-    outputs and timings meaningless: fail loudly instead of printing them."""
+def check_device_status(w4v, leg="bench"):
+    """A kernel that gave up a bounded wait leaves its status word set (read and
+    cleared here) and its outputs and timings meaningless: fail loudly instead
+    of printing them."""
     st = w4v.get_status()
     if st != 0:
-        raise RuntimeError("device status %d: a kernel gave up a bounded wait; the measurements are invalid" % st)
+        raise RuntimeError("device status %d after the %s leg: a kernel gave up a bounded wait; "
+                           "the measurements are invalid" % (st, leg))
 
 
 def run_e2e(args, step, torch, total_bytes, world):
@@ -829,7 +841,7 @@ def main():
             out = {"prefill": run_prefill(dev, w4v, torch, load_peaks())}
         else:
             out = {"gdn_state": run_gdn(dev, w4v, torch)}
-        check_device_status(w4v)
+        check_device_status(w4v, "prefill" if args.prefill_only else "recurrent state")
         print(json.dumps(out), flush=True)
         return
     res = run_gpu(args, rank, world)

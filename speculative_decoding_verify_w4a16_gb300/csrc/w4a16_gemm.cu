@@ -29,14 +29,12 @@
 //     sharing a scheduler work on different units and so fall naturally out
 //     of phase.  The dequantized operand never touches shared memory.
 //   * tcgen05.mma (A from TMEM, B = activations from shared memory, D in
-//     TMEM) is issued by three warps, unit f wholly by warp f % 3 (which so
-//     owns A slot f % 3): each of its waits and commits costs a couple of
-//     hundred cycles, so a unit takes one of each per barrier, and three
-//     units are in flight.  In steady state the tensor pipe is the limit:
-//     an M128 N16 K16 MMA occupies it ~97 cycles, so a 16 KB unit (16 MMAs)
-//     takes ~1550 cycles per SM whatever the issue order.  Each group
-//     accumulates its 8 k-steps into its own accumulator block, so every
-//     output element is the same chain of MMAs whatever the timing or M.
+//     TMEM) is issued by three threads in three warps; one thread alone
+//     issues at most one MMA per ~90 cycles, so the two groups of a unit go
+//     to two different issuers (group g of unit f to issuer (2f + g) % 3) and
+//     run side by side.  Each group accumulates its 8 k-steps into its own
+//     accumulator block, so every output element is the same chain of MMAs
+//     whatever the timing or M.
 //   * Four drain warps read a unit's accumulators (one tcgen05.ld for both
 //     groups) and apply the group scales in fp32, groups in ascending order.
 //     Scales (and zero points) are tiny but each group needs a fresh row of
@@ -90,8 +88,6 @@ constexpr int kWarpDq0 = 8;                        // 8..15 dequant
 constexpr int kWarps = kWarpDq0 + kDqWarps;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kASlots = 3;                         // unit f uses A slot f % 3
-static_assert(kASlots == kIssuers && kStageUnits <= kIssuers,
-              "issuer f % 3 owns A slot f % 3 and at most one unit of a stage");
 constexpr uint32_t kASlotCols = kUnitGroups * 64;  // fp16 pairs of 128 rows x 256 k
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDcol0 = kASlots * kASlotCols;
@@ -283,14 +279,14 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         for (int s = 0; s < S; ++s) {
             mbar_init(wfull(s), 1);
             mbar_init(xfull(s), 1);
-            mbar_init(empty(s), kDqWarps + kStageUnits);   // dequant warps + one per unit's issuer
+            mbar_init(empty(s), kDqWarps + kIssuers);
         }
         for (int a = 0; a < kASlots; ++a) {
             mbar_init(afull(a), kDqWarps / 2);     // the four quarter warps of the unit's parity
-            mbar_init(aempty(a), 1);               // the unit's issuer
+            mbar_init(aempty(a), kUnitGroups);     // one commit per group issuer
         }
         for (int b = 0; b < DS; ++b) {
-            mbar_init(dfull(b), 1);
+            mbar_init(dfull(b), kUnitGroups);
             mbar_init(dempty(b), kDrWarps);
         }
         mbar_init(done_bar, kIssuers);
@@ -365,49 +361,57 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     } else if (warp >= kWarpIss0 && warp < kWarpIss0 + kIssuers) {
         // ------------------------------------------------------ MMA issuers
         // (shared and tensor memory only: ordered by the stage barriers).
-        // Issuer me owns every unit f with f % 3 == me -- both of its groups,
-        // so one wait per barrier and one commit per consumer a unit -- and
-        // with it A slot me.  The whole warp runs the loop and lane 0 alone
-        // issues, so the operands stay warp-uniform.
+        // The whole warp runs the loop and lane 0 alone issues, so the
+        // operands stay warp-uniform.
         {
             const int me = warp - kWarpIss0;
             constexpr uint32_t idesc = idesc_f16_f32(128, 16 * NBLK);
             StageWalk sw(ub, nP, G, nunits);
+            bool ok = true;
             int f0 = 0;                          // first unit of the stage
             StageRing rg(S);
-            for (; sw.left > 0; rg.next()) {
+            for (; sw.left > 0 && ok; rg.next()) {
                 const int n = sw.size();
                 const int s = rg.s;
-                const int jj = (me - f0 % kIssuers + kIssuers) % kIssuers;   // my unit in the stage, if any
-                if (jj < n) {
+                // Every issuer waits for every stage, so its once-per-stage
+                // release below always lands in the phase of this stage.
+                if (!warp_wait(xfull(s), rg.ph, ab)) break;
+                for (int jj = 0; jj < n; ++jj) {
                     const int f = f0 + jj;
+                    // group gg of unit f belongs to issuer (2f + gg) % 3; a
+                    // unit with one group gets both of its commits from that
+                    // group's issuer
                     const int ng = min(kUnitGroups, G - 2 * (sw.p + jj));
+                    const int i0 = (2 * f) % kIssuers, i1 = (2 * f + 1) % kIssuers;
+                    const bool mine0 = i0 == me, mine1 = ng > 1 ? i1 == me : false;
+                    if (!mine0 && !mine1) continue;
                     const int slot = f % kASlots;
                     const int set = f % DS;
-                    // afull first: the unit's weights were dequantized, so this
-                    // stage's previous use is complete and the parity of xfull
-                    // names this use (an issuer skips the stages it has no unit in)
-                    if (!warp_wait(afull(slot), (f / kASlots) & 1, ab) || !warp_wait(xfull(s), rg.ph, ab) ||
-                        (f >= DS && !warp_wait(dempty(set), ((f / DS) - 1) & 1, ab)))
+                    if (!warp_wait(afull(slot), (f / kASlots) & 1, ab) ||
+                        (f >= DS && !warp_wait(dempty(set), ((f / DS) - 1) & 1, ab))) {
+                        ok = false;
                         break;
+                    }
                     tc_fence_after();
                     const uint32_t dset = tmem + kDcol0 + set * L::kDUnit;
                     for (int gg = 0; gg < ng; ++gg) {
+                        if (!(gg == 0 ? mine0 : mine1)) continue;
                         const uint32_t act = base_s + s * L::kStage + 2 * (kUnitGroups * jj + gg) * L::kActBox;
 #pragma unroll
                         for (int j = 0; j < kGroup / 16; ++j) {
                             // all 16 NBLK activation rows in one MMA (N = 16 NBLK)
                             const uint32_t baddr = act + (j >> 2) * L::kActBox + (j & 3) * 32;
                             mma_f16_ts_lane0(dset + gg * NBLK * 16, tmem + slot * kASlotCols + gg * 64 + 8 * j,
-                                             sdesc_sw128(baddr), idesc, j > 0 ? 1u : 0u);
+                                       sdesc_sw128(baddr), idesc, j > 0 ? 1u : 0u);
                         }
                     }
-                    mma_commit_lane0(aempty(slot));
-                    mma_commit_lane0(dfull(set));
-                    // one release of the stage per unit (a one-unit stage counts twice)
-                    mma_commit_lane0(empty(s));
-                    if (n == 1) mma_commit_lane0(empty(s));
+                    const int commits = (mine0 ? 1 : 0) + (mine1 ? 1 : 0) + (ng == 1 ? 1 : 0);
+                    for (int c = 0; c < commits; ++c) {
+                        mma_commit_lane0(aempty(slot));
+                        mma_commit_lane0(dfull(set));
+                    }
                 }
+                mma_commit_lane0(empty(s));
                 f0 += n;
                 sw.next(n);
             }
