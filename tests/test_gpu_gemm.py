@@ -192,3 +192,35 @@ def test_prefill_split_tiles_deterministic_and_clean(w4v_mod, gpu, oracle_mod, M
     R = oracle_mod.w4a16_gemm_sampled(A, q, s, rows, cols)
     assert gemm_rel_err(a[rows, cols], R) <= GEMM_TOL
     assert w4v_mod.get_status() == 0
+
+
+@pytest.mark.parametrize("M", [16, 21, 32])
+def test_back_to_back_layer_launches_clean_and_deterministic(w4v_mod, gpu, M):
+    """The 4B layer's projections launched back to back many times with
+    static weights (each launch's set-up overlapping the previous one, as in
+    the verify step): no kernel may give up a bounded wait (device status
+    stays clear) and every launch must reproduce the first one's outputs bit
+    for bit.  A barrier whose phases a waiter can skip shows up here as a
+    timeout or as a changed output; M = 21 and 32 run two accumulator sets
+    per tile, M = 16 four."""
+    g = torch.Generator(device=gpu)
+    g.manual_seed(71 + M)
+    projs = []
+    for p in inputs.LAYER_PROJS:
+        packed = torch.randint(0, 256, (w4v_mod.packed_bytes(p.N, p.K),), generator=g, device=gpu,
+                               dtype=torch.uint8)
+        sc = (torch.rand((p.K // 128, p.N), generator=g, device=gpu) * 0.015 + 0.005).half()
+        A = torch.randn((M, p.K), generator=g, device=gpu).half()
+        ws = w4v_mod.workspace(w4v_mod.w4a16_workspace_bytes(M, p.N, p.K), gpu)
+        projs.append((p, packed, sc, A, ws))
+    assert w4v_mod.get_status() == 0
+    ref = [w4v_mod.w4a16_gemm(A, packed, sc, p.N, ws=ws, static_weights=True).clone()
+           for (p, packed, sc, A, ws) in projs]
+    outs = [torch.empty_like(r) for r in ref]
+    for _ in range(100):
+        for (p, packed, sc, A, ws), C in zip(projs, outs):
+            w4v_mod.w4a16_gemm(A, packed, sc, p.N, out=C, ws=ws, static_weights=True)
+    torch.cuda.synchronize()
+    assert w4v_mod.get_status() == 0
+    for r, C in zip(ref, outs):
+        assert torch.equal(r, C)
