@@ -100,6 +100,12 @@ constexpr int kFAhead = 3;
 constexpr int kFRing = 4;
 constexpr int kFEntry = 4 * 32 * 2 + 4 * 32;       // 256 B scales + 128 B zeros
 
+// Group size 128: the producer copies each stage's scales (its four groups'
+// rows of one tile) into a ring of kSclSlots slots with one 2-D TMA, and the
+// drain warps read them from there.
+constexpr int kSclSlots = 8;
+constexpr int kSclSlotBytes = kStageGroups * kTileN * 2;
+
 constexpr int kMaxStages = 4;
 constexpr int kMaxSmem = 227 * 1024;
 // Largest cluster (portable size).  Measured on the 4B shapes at M = 16, each
@@ -120,14 +126,15 @@ struct Layout {
     static constexpr uint32_t kDUnit = kUnitGroups * 16 * NBLK;   // accumulator columns per unit
     static constexpr int kDSets = int((kTmemCols - kDcol0) / kDUnit);
     // wfull, xfull, empty per stage (room for kMaxStages); afull, aempty per A slot;
-    // dfull, dempty per set; done; drain sync
-    static constexpr int kNumBars = 3 * kMaxStages + 2 * kASlots + 2 * kDSets + 2;
+    // dfull, dempty per set; done; drain sync; sfull, sempty per scale slot
+    static constexpr int kNumBars = 3 * kMaxStages + 2 * kASlots + 2 * kDSets + 2 + 2 * kSclSlots;
     static constexpr int kBarBytes = (8 * kNumBars + 127) & ~127;
     static constexpr int kScl = kBarBytes;                         // offsets inside the fixed block
     static constexpr int kZro = kScl + kDrWarps * kRing * 64;      // 32 fp16 scales per entry
     static constexpr int kMisc = kZro + kDqWarps * kRing * 32;     // 32 uint8 zeros per entry
     static_assert(kDqWarps * kFRing * kFEntry <= kMisc - kScl, "group-32 ring fits the rings' space");
-    static constexpr int kFixed = kMisc + 128;
+    static constexpr int kSst = kMisc + 128;                        // stage scale ring (128-byte aligned)
+    static constexpr int kFixed = kSst + kSclSlots * kSclSlotBytes;
     static constexpr int kPart = 16 * NBLK * kTileN;               // floats of one partial tile
     __host__ __device__ static constexpr int bytes(int stages) { return stages * kStage + kFixed + 1024; }
     static_assert(kStage % 1024 == 0, "stage alignment");
@@ -154,6 +161,7 @@ struct Args {
     int stages;                       // pipeline stages in shared memory
     int cluster;                      // CTAs per tile (cluster size); 0 = stream-K
     int static_w;                     // weights, scales, zeros not written by earlier work in flight
+    int sbox_w, sbox_h;               // scale box of one stage: min(128, N) x min(4, K / 128)
 };
 
 // A unit: tile t, pair p (groups 2p and, if it exists, 2p + 1).
@@ -231,7 +239,8 @@ struct GroupWalk {
 // group's fp32 sum instead.
 template <int NBLK, bool kFold>
 __global__ void __launch_bounds__(kThreads, 1)
-w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
+w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap,
+                    const Args p) {
     using L = Layout<NBLK>;
     constexpr int DS = L::kDSets;
     constexpr int MS = kMaxStages;
@@ -252,6 +261,9 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     auto dempty = [&](int b) { return bar0 + 8u * (3 * MS + 2 * kASlots + DS + b); };
     const uint32_t done_bar = bar0 + 8u * (3 * MS + 2 * kASlots + 2 * DS);
     const uint32_t drain_bar = done_bar + 8u;
+    auto sfull = [&](int b) { return drain_bar + 8u * (1 + b); };               // a stage's scales landed
+    auto sempty = [&](int b) { return drain_bar + 8u * (1 + kSclSlots + b); };  // the drain has read them
+    const uint32_t sst = base_s + fixed_off + L::kSst;
     // [0] tmem base, [1] abort flag, [2..3] pending tile + 1 per slot, [4..5] last-arriver flags
     uint32_t *misc = reinterpret_cast<uint32_t *>(base + fixed_off + L::kMisc);
 
@@ -291,6 +303,10 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         }
         mbar_init(done_bar, kIssuers);
         mbar_init(drain_bar, kDrWarps);
+        for (int b = 0; b < kSclSlots; ++b) {
+            mbar_init(sfull(b), 1);
+            mbar_init(sempty(b), kDrWarps);
+        }
         for (int k = 1; k < 16; ++k) misc[k] = 0;
         fence_barrier_init();
     }
@@ -315,14 +331,23 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             bulk_load(base_s + s * L::kStage + L::kW, p.wq + (size_t(w.t) * G + g0) * kGroupBytes, wbytes, wfull(s),
                       pol_w);
         };
+        // stage use u's scales into slot u % kSclSlots (rows past N or K land as zero)
+        auto load_scales = [&](const StageWalk &w, int u) {
+            if (kFold) return;
+            const int b = u % kSclSlots;
+            mbar_arrive_expect_tx(sfull(b), uint32_t(p.sbox_w * p.sbox_h * 2));
+            tma_load_2d(sst + uint32_t(b * kSclSlotBytes), &smap, w.t * kTileN, w.gbeg(), sfull(b), pol_w);
+        };
         int w_early = 0;                         // stages whose weights went out before the wait
         if (lane == 0) {
             prefetch_tensormap(&xmap);
+            if (!kFold) prefetch_tensormap(&smap);
             StageWalk pw(ub, nP, G, nunits);
             for (int st = 0; st < S && pw.left > 0; ++st) {
                 const int n = pw.size();
                 if (p.static_w) {
                     load_weights(pw, n, st);
+                    load_scales(pw, st);         // st < S <= kSclSlots: the slot is fresh
                     ++w_early;
                 } else {
                     // Only L2 is warmed before the dependency wait: L2 is the
@@ -343,7 +368,14 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                 const int n = sw.size();
                 const int s = rg.s;
                 if (rg.wrapped && !mbar_wait(empty(s), rg.ph ^ 1u, ab)) break;
-                if (issued >= w_early) load_weights(sw, n, s);
+                if (issued >= w_early) {
+                    // the slot's previous stage must have been read by the drain
+                    if (!kFold && issued >= kSclSlots &&
+                        !mbar_wait(sempty(issued % kSclSlots), uint32_t(issued / kSclSlots - 1) & 1u, ab))
+                        break;
+                    load_weights(sw, n, s);
+                    load_scales(sw, issued);
+                }
                 mbar_arrive_expect_tx(xfull(s), L::kAct);
                 tma_load_3d(base_s + s * L::kStage, &xmap, 0, 0, 2 * sw.gbeg(), xfull(s), pol_x);
                 ++issued;
@@ -356,6 +388,9 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                     mbar_wait_bounded(wfull(i % S), uint32_t(i / S) & 1u);
                 for (int i = max(0, issued - S); i < issued; ++i)
                     mbar_wait_bounded(xfull(i % S), uint32_t(i / S) & 1u);
+                if (!kFold)
+                    for (int i = max(0, w_issued - kSclSlots); i < w_issued; ++i)
+                        mbar_wait_bounded(sfull(i % kSclSlots), uint32_t(i / kSclSlots) & 1u);
             }
         }
     } else if (warp >= kWarpIss0 && warp < kWarpIss0 + kIssuers) {
@@ -659,36 +694,12 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         };
         if (!p.static_w) grid_dep_wait();
 
-        // Group scales of this warp's 32 rows, kAhead groups ahead (rows past
-        // N read as 0 and are never stored).
-        const __half *sring = reinterpret_cast<const __half *>(base + fixed_off + L::kScl) + dr * kRing * 32;
-        GroupWalk sgw(ub, 0, 1, nunits, nP, G);
-        int sissued = 0, sused = 0;
-        auto scale_issue = [&]() {
-            if (sgw.more()) {
-                if (lane < 4) {
-                    const int n0 = sgw.t() * kTileN + 32 * q + 8 * lane;
-                    const bool in = n0 < p.N;
-                    cp_async<16>(smem_u32(sring + (sissued % kRing) * 32 + 8 * lane),
-                                 in ? static_cast<const void *>(p.scales + size_t(sgw.g()) * p.N + n0) : p.scales,
-                                 in ? 16u : 0u);
-                }
-                sgw.next();
-            }
-            ++sissued;
-            cp_async_commit();
-        };
-        auto scale_take = [&]() -> float {
-            cp_async_wait<kAhead - 1>();
-            __syncwarp();
-            const float v = __half2float(__ushort_as_half(lds_u16(smem_u32(sring + (sused % kRing) * 32 + lane))));
-            ++sused;
-            __syncwarp();
-            scale_issue();
-            return v;
-        };
-        if (!kFold)
-            for (int k = 0; k < kAhead; ++k) scale_issue();
+        // The unit's group scales come from the stage scale ring (rows past
+        // N read as 0 and are never stored): dw walks the stages as the
+        // producer does, du is the stage use, dj the unit within the stage.
+        StageWalk dw(ub, nP, G, nunits);
+        int du = 0, dj = 0;
+        const uint32_t srow = uint32_t(2 * r);
         if (p.static_w) grid_dep_wait();     // before any write of C or the workspace
 
         // Tile finished by this CTA alone: write C.  Otherwise publish the fp32
@@ -801,17 +812,34 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             if (lane == 0) mbar_arrive(dempty(set));
             // groups in ascending order, each scaled in fp32 (group size 32:
             // the weights carry their scales, the sums are added as they are)
-            const float s0 = kFold ? 1.f : scale_take();
+            float s0 = 1.f, s1 = 1.f;
+            if (!kFold) {
+                const int b = du % kSclSlots;
+                // once per stage (on an abort the values are never stored)
+                if (dj == 0) warp_wait(sfull(b), uint32_t(du / kSclSlots) & 1u, ab);
+                const uint32_t row0 = sst + uint32_t(b * kSclSlotBytes) + srow;
+                const uint32_t pitch = uint32_t(p.sbox_w * 2);
+                s0 = __half2float(__ushort_as_half(lds_u16(row0 + uint32_t(2 * dj) * pitch)));
+                if (ng > 1) s1 = __half2float(__ushort_as_half(lds_u16(row0 + uint32_t(2 * dj + 1) * pitch)));
+            }
 #pragma unroll
             for (int b = 0; b < NBLK; ++b)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) acc[b][j] = fmaf(s0, __uint_as_float(d[b][j]), acc[b][j]);
             if (ng > 1) {
-                const float s1 = kFold ? 1.f : scale_take();
 #pragma unroll
                 for (int b = 0; b < NBLK; ++b)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) acc[b][j] = fmaf(s1, __uint_as_float(d[NBLK + b][j]), acc[b][j]);
+            }
+            if (++dj == dw.size()) {             // the stage's last unit: its scales are read
+                if (!kFold) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sempty(du % kSclSlots));
+                }
+                dw.next(dj);
+                ++du;
+                dj = 0;
             }
             const int t = wd.t;
             const bool tile_end = wd.tile_last();
@@ -828,7 +856,6 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             }
         }
         if (ok) mark_last();
-        cp_async_wait<0>();
     }
 
     __syncthreads();
@@ -988,7 +1015,7 @@ w4v_status configure() {
 }
 
 template <int NBLK, bool kFold>
-w4v_status launch(const CUtensorMap &xmap, Args &a, int cluster, cudaStream_t stream) {
+w4v_status launch(const CUtensorMap &xmap, const CUtensorMap &smap, Args &a, int cluster, cudaStream_t stream) {
     using L = Layout<NBLK>;
     w4v_status st = configure<NBLK, kFold>();
     if (st != W4V_OK) return st;
@@ -997,7 +1024,7 @@ w4v_status launch(const CUtensorMap &xmap, Args &a, int cluster, cudaStream_t st
     if (cluster > 0) a.P = a.n_tiles * cluster;
     const size_t smem = size_t(L::bytes(a.stages));
     if (launch_pdl_cluster(w4a16_decode_kernel<NBLK, kFold>, dim3(a.P), dim3(kThreads), smem, stream, cluster, xmap,
-                           a) !=
+                           smap, a) !=
         cudaSuccess) {
         cudaGetLastError();
         return W4V_ERR_CUDA;
@@ -1062,9 +1089,18 @@ w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t
     st = encode_tmap_kblocks(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, uint64_t(K), uint64_t(M), 64, 16 * nblk,
                              2 * kStageGroups, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != W4V_OK) return st;
+    // scales [K/group][N]: one stage's rows (up to 4 groups) of one tile (up to 128 columns)
+    a.sbox_w = std::min(kTileN, N);
+    a.sbox_h = std::min(kStageGroups, K / group);
+    CUtensorMap smap;
+    st = encode_tmap_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, scales, uint64_t(N), uint64_t(K / group),
+                        uint64_t(N) * 2, uint32_t(a.sbox_w), uint32_t(a.sbox_h), CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != W4V_OK) return st;
     const int cluster = cluster_for(a.n_tiles, a.n_pairs, info->sm_count);
-    if (group == 32) return nblk == 1 ? launch<1, true>(xmap, a, cluster, stream) : launch<2, true>(xmap, a, cluster, stream);
-    return nblk == 1 ? launch<1, false>(xmap, a, cluster, stream) : launch<2, false>(xmap, a, cluster, stream);
+    if (group == 32)
+        return nblk == 1 ? launch<1, true>(xmap, smap, a, cluster, stream)
+                         : launch<2, true>(xmap, smap, a, cluster, stream);
+    return nblk == 1 ? launch<1, false>(xmap, smap, a, cluster, stream) : launch<2, false>(xmap, smap, a, cluster, stream);
 }
 
 }  // namespace w4v
