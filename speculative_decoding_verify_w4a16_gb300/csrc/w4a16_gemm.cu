@@ -37,10 +37,13 @@
 //     whatever the timing or M.
 //   * Four drain warps read a unit's accumulators (one tcgen05.ld for both
 //     groups) and apply the group scales in fp32, groups in ascending order.
-//     Scales (and zero points) are tiny but each group needs a fresh row of
-//     them, and a global load takes over a microsecond when HBM is busy:
-//     each warp keeps the next 16 groups' values in flight with cp.async
-//     into a shared-memory ring.
+//     The drain warps pace the pipeline (the accumulator sets they free gate
+//     the issuers), so they issue no global loads: the producer copies each
+//     stage's scales (four groups of one tile) with one 2-D TMA into a ring
+//     of eight slots, which the drain frees stage by stage.  A load issued
+//     by a drain warp stalls behind the weight stream's queued requests.
+//     Zero points (and the group-32 scales) are read by the dequant warps,
+//     which keep them 16 (3) groups ahead with cp.async into rings.
 //   * Work split.  With few 128-row tiles, each tile belongs to a
 //     thread-block cluster of C CTAs (C about the square root of the units
 //     per tile, at most 8, all clusters in one wave)
