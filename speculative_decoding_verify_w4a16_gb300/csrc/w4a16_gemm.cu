@@ -128,9 +128,10 @@ struct Layout {
     static constexpr int kStage = kW + kStageGroups * kGroupBytes;
     static constexpr uint32_t kDUnit = kUnitGroups * 16 * NBLK;   // accumulator columns per unit
     static constexpr int kDSets = int((kTmemCols - kDcol0) / kDUnit);
-    // wfull, xfull, empty per stage (room for kMaxStages); afull, aempty per A slot;
+    // wfull, xfull, empty per stage (room for kMaxStages); afull per A slot, aempty
+    // per A slot and dequant parity;
     // dfull, dempty per set; done; drain sync; sfull, sempty per scale slot
-    static constexpr int kNumBars = 3 * kMaxStages + 2 * kASlots + 2 * kDSets + 2 + 2 * kSclSlots;
+    static constexpr int kNumBars = 3 * kMaxStages + 3 * kASlots + 2 * kDSets + 2 + 2 * kSclSlots;
     static constexpr int kBarBytes = (8 * kNumBars + 127) & ~127;
     static constexpr int kScl = kBarBytes;                         // offsets inside the fixed block
     static constexpr int kZro = kScl + kDrWarps * kRing * 64;      // 32 fp16 scales per entry
@@ -259,10 +260,14 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
     auto xfull = [&](int s) { return bar0 + 8u * (MS + s); };   // stage's activations landed
     auto empty = [&](int s) { return bar0 + 8u * (2 * MS + s); };
     auto afull = [&](int a) { return bar0 + 8u * (3 * MS + a); };
-    auto aempty = [&](int a) { return bar0 + 8u * (3 * MS + kASlots + a); };
-    auto dfull = [&](int b) { return bar0 + 8u * (3 * MS + 2 * kASlots + b); };
-    auto dempty = [&](int b) { return bar0 + 8u * (3 * MS + 2 * kASlots + DS + b); };
-    const uint32_t done_bar = bar0 + 8u * (3 * MS + 2 * kASlots + 2 * DS);
+    // A slot a freed for the dequant warps of parity par: unit u's MMAs release
+    // slot u % 3 to its next user u + 3, of parity (u + 1) % 2.  Each waiter
+    // so sees every phase of its barrier in turn (one barrier per slot would
+    // let a parity skip a phase).
+    auto aempty = [&](int a, int par) { return bar0 + 8u * (3 * MS + kASlots + 2 * a + par); };
+    auto dfull = [&](int b) { return bar0 + 8u * (3 * MS + 3 * kASlots + b); };
+    auto dempty = [&](int b) { return bar0 + 8u * (3 * MS + 3 * kASlots + DS + b); };
+    const uint32_t done_bar = bar0 + 8u * (3 * MS + 3 * kASlots + 2 * DS);
     const uint32_t drain_bar = done_bar + 8u;
     auto sfull = [&](int b) { return drain_bar + 8u * (1 + b); };               // a stage's scales landed
     auto sempty = [&](int b) { return drain_bar + 8u * (1 + kSclSlots + b); };  // the drain has read them
@@ -298,7 +303,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         }
         for (int a = 0; a < kASlots; ++a) {
             mbar_init(afull(a), kDqWarps / 2);     // the four quarter warps of the unit's parity
-            mbar_init(aempty(a), kUnitGroups);     // one commit per group issuer
+            mbar_init(aempty(a, 0), kUnitGroups);  // one commit per group issuer
+            mbar_init(aempty(a, 1), kUnitGroups);
         }
         for (int b = 0; b < DS; ++b) {
             mbar_init(dfull(b), kUnitGroups);
@@ -445,7 +451,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                     }
                     const int commits = (mine0 ? 1 : 0) + (mine1 ? 1 : 0) + (ng == 1 ? 1 : 0);
                     for (int c = 0; c < commits; ++c) {
-                        mma_commit_lane0(aempty(slot));
+                        mma_commit_lane0(aempty(slot, (f + 1) & 1));
                         mma_commit_lane0(dfull(set));
                     }
                 }
@@ -644,7 +650,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                         dequant(gp, 0, z, ra);
                     }
                     if (gg == 0) {
-                        if (f >= kASlots && !warp_wait(aempty(slot), ((f / kASlots) - 1) & 1, ab)) {
+                        // the release by unit f - 3: this parity's ((f - 3) / 6)-th on the barrier
+                        if (f >= kASlots && !warp_wait(aempty(slot, f & 1), uint32_t((f - kASlots) / 6) & 1u, ab)) {
                             aborted = true;
                             break;
                         }
