@@ -91,6 +91,8 @@ constexpr int kWarpDq0 = 8;                        // 8..15 dequant
 constexpr int kWarps = kWarpDq0 + kDqWarps;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kASlots = 3;                         // unit f uses A slot f % 3
+static_assert(kASlots == kIssuers && kStageUnits <= kIssuers,
+              "issuer f % 3 owns A slot f % 3 and at most one unit of a stage");
 constexpr uint32_t kASlotCols = kUnitGroups * 64;  // fp16 pairs of 128 rows x 256 k
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDcol0 = kASlots * kASlotCols;
@@ -131,7 +133,7 @@ struct Layout {
     // wfull, xfull, empty per stage (room for kMaxStages); afull per A slot, aempty
     // per A slot and dequant parity;
     // dfull, dempty per set; done; drain sync; sfull, sempty per scale slot
-    static constexpr int kNumBars = 3 * kMaxStages + 3 * kASlots + 2 * kDSets + 2 + 2 * kSclSlots;
+    static constexpr int kNumBars = 3 * kMaxStages + 3 * kASlots + (1 + kIssuers) * kDSets + 2 + 2 * kSclSlots;
     static constexpr int kBarBytes = (8 * kNumBars + 127) & ~127;
     static constexpr int kScl = kBarBytes;                         // offsets inside the fixed block
     static constexpr int kZro = kScl + kDrWarps * kRing * 64;      // 32 fp16 scales per entry
@@ -266,8 +268,11 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
     // let a parity skip a phase).
     auto aempty = [&](int a, int par) { return bar0 + 8u * (3 * MS + kASlots + 2 * a + par); };
     auto dfull = [&](int b) { return bar0 + 8u * (3 * MS + 3 * kASlots + b); };
-    auto dempty = [&](int b) { return bar0 + 8u * (3 * MS + 3 * kASlots + DS + b); };
-    const uint32_t done_bar = bar0 + 8u * (3 * MS + 3 * kASlots + 2 * DS);
+    // accumulator set b freed for issuer i: the drain of unit u releases set
+    // u % DS to its next user u + DS, issued by (u + DS) % 3, so each issuer
+    // sees every phase of its own barriers
+    auto dempty = [&](int b, int i) { return bar0 + 8u * (3 * MS + 3 * kASlots + DS + b * kIssuers + i); };
+    const uint32_t done_bar = bar0 + 8u * (3 * MS + 3 * kASlots + (1 + kIssuers) * DS);
     const uint32_t drain_bar = done_bar + 8u;
     auto sfull = [&](int b) { return drain_bar + 8u * (1 + b); };               // a stage's scales landed
     auto sempty = [&](int b) { return drain_bar + 8u * (1 + kSclSlots + b); };  // the drain has read them
@@ -299,16 +304,16 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         for (int s = 0; s < S; ++s) {
             mbar_init(wfull(s), 1);
             mbar_init(xfull(s), 1);
-            mbar_init(empty(s), kDqWarps + kIssuers);
+            mbar_init(empty(s), kDqWarps + kStageUnits);   // dequant warps + one per unit's issuer
         }
         for (int a = 0; a < kASlots; ++a) {
             mbar_init(afull(a), kDqWarps / 2);     // the four quarter warps of the unit's parity
-            mbar_init(aempty(a, 0), kUnitGroups);  // one commit per group issuer
-            mbar_init(aempty(a, 1), kUnitGroups);
+            mbar_init(aempty(a, 0), 1);            // the unit's issuer
+            mbar_init(aempty(a, 1), 1);
         }
         for (int b = 0; b < DS; ++b) {
-            mbar_init(dfull(b), kUnitGroups);
-            mbar_init(dempty(b), kDrWarps);
+            mbar_init(dfull(b), 1);
+            for (int i = 0; i < kIssuers; ++i) mbar_init(dempty(b, i), kDrWarps);
         }
         mbar_init(done_bar, kIssuers);
         mbar_init(drain_bar, kDrWarps);
@@ -405,57 +410,50 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
     } else if (warp >= kWarpIss0 && warp < kWarpIss0 + kIssuers) {
         // ------------------------------------------------------ MMA issuers
         // (shared and tensor memory only: ordered by the stage barriers).
-        // The whole warp runs the loop and lane 0 alone issues, so the
-        // operands stay warp-uniform.
+        // Issuer me owns every unit f with f % 3 == me -- both of its groups,
+        // so one wait per barrier and one commit per consumer a unit -- and
+        // with it A slot me.  The whole warp runs the loop and lane 0 alone
+        // issues, so the operands stay warp-uniform.
         {
             const int me = warp - kWarpIss0;
             constexpr uint32_t idesc = idesc_f16_f32(128, 16 * NBLK);
+            constexpr int kSetPeriod = DS * kIssuers;       // units between uses of one dempty barrier
             StageWalk sw(ub, nP, G, nunits);
-            bool ok = true;
             int f0 = 0;                          // first unit of the stage
             StageRing rg(S);
-            for (; sw.left > 0 && ok; rg.next()) {
+            for (; sw.left > 0; rg.next()) {
                 const int n = sw.size();
                 const int s = rg.s;
-                // Every issuer waits for every stage, so its once-per-stage
-                // release below always lands in the phase of this stage.
-                if (!warp_wait(xfull(s), rg.ph, ab)) break;
-                for (int jj = 0; jj < n; ++jj) {
+                const int jj = (me - f0 % kIssuers + kIssuers) % kIssuers;   // my unit in the stage, if any
+                if (jj < n) {
                     const int f = f0 + jj;
-                    // group gg of unit f belongs to issuer (2f + gg) % 3; a
-                    // unit with one group gets both of its commits from that
-                    // group's issuer
                     const int ng = min(kUnitGroups, G - 2 * (sw.p + jj));
-                    const int i0 = (2 * f) % kIssuers, i1 = (2 * f + 1) % kIssuers;
-                    const bool mine0 = i0 == me, mine1 = ng > 1 ? i1 == me : false;
-                    if (!mine0 && !mine1) continue;
                     const int slot = f % kASlots;
                     const int set = f % DS;
-                    if (!warp_wait(afull(slot), (f / kASlots) & 1, ab) ||
-                        (f >= DS && !warp_wait(dempty(set), ((f / DS) - 1) & 1, ab))) {
-                        ok = false;
+                    // afull first: the unit's weights were dequantized, so this
+                    // stage's previous use is complete and the parity of xfull
+                    // names this use (an issuer skips the stages it has no unit in)
+                    if (!warp_wait(afull(slot), (f / kASlots) & 1, ab) || !warp_wait(xfull(s), rg.ph, ab) ||
+                        (f >= DS && !warp_wait(dempty(set, me), uint32_t((f - DS) / kSetPeriod) & 1u, ab)))
                         break;
-                    }
                     tc_fence_after();
                     const uint32_t dset = tmem + kDcol0 + set * L::kDUnit;
                     for (int gg = 0; gg < ng; ++gg) {
-                        if (!(gg == 0 ? mine0 : mine1)) continue;
                         const uint32_t act = base_s + s * L::kStage + 2 * (kUnitGroups * jj + gg) * L::kActBox;
 #pragma unroll
                         for (int j = 0; j < kGroup / 16; ++j) {
                             // all 16 NBLK activation rows in one MMA (N = 16 NBLK)
                             const uint32_t baddr = act + (j >> 2) * L::kActBox + (j & 3) * 32;
                             mma_f16_ts_lane0(dset + gg * NBLK * 16, tmem + slot * kASlotCols + gg * 64 + 8 * j,
-                                       sdesc_sw128(baddr), idesc, j > 0 ? 1u : 0u);
+                                             sdesc_sw128(baddr), idesc, j > 0 ? 1u : 0u);
                         }
                     }
-                    const int commits = (mine0 ? 1 : 0) + (mine1 ? 1 : 0) + (ng == 1 ? 1 : 0);
-                    for (int c = 0; c < commits; ++c) {
-                        mma_commit_lane0(aempty(slot, (f + 1) & 1));
-                        mma_commit_lane0(dfull(set));
-                    }
+                    mma_commit_lane0(aempty(slot, (f + 1) & 1));
+                    mma_commit_lane0(dfull(set));
+                    // one release of the stage per unit (a one-unit stage counts twice)
+                    mma_commit_lane0(empty(s));
+                    if (n == 1) mma_commit_lane0(empty(s));
                 }
-                mma_commit_lane0(empty(s));
                 f0 += n;
                 sw.next(n);
             }
@@ -819,7 +817,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(dempty(set));
+            if (lane == 0) mbar_arrive(dempty(set, (f + DS) % kIssuers));
             // groups in ascending order, each scaled in fp32 (group size 32:
             // the weights carry their scales, the sums are added as they are)
             float s0 = 1.f, s1 = 1.f;
