@@ -29,12 +29,18 @@
 //     sharing a scheduler work on different units and so fall naturally out
 //     of phase.  The dequantized operand never touches shared memory.
 //   * tcgen05.mma (A from TMEM, B = activations from shared memory, D in
-//     TMEM) is issued by three threads in three warps; one thread alone
-//     issues at most one MMA per ~90 cycles, so the two groups of a unit go
-//     to two different issuers (group g of unit f to issuer (2f + g) % 3) and
-//     run side by side.  Each group accumulates its 8 k-steps into its own
-//     accumulator block, so every output element is the same chain of MMAs
-//     whatever the timing or M.
+//     TMEM) is issued by three warps, unit f wholly by warp f % 3 (which so
+//     owns A slot f % 3), the loop run by the whole warp with lane 0 issuing
+//     so the operands stay warp-uniform.  Each wait on a completed barrier
+//     and each commit costs a couple of hundred cycles, so a unit takes one
+//     of each per barrier, and three units are in flight.  Each group
+//     accumulates its 8 k-steps into its own accumulator block, so every
+//     output element is the same chain of MMAs whatever the timing or M.
+//   * Every wait is on an mbarrier phase parity, which names the phase only
+//     if the barrier is neither a phase behind nor two ahead.  A waiter that
+//     sees only some uses of a resource therefore gets a barrier of its own:
+//     the A slot a unit frees is released to the dequant warps of the next
+//     user's parity, the accumulator set to the issuer of its next user.
 //   * Four drain warps read a unit's accumulators (one tcgen05.ld for both
 //     groups) and apply the group scales in fp32, groups in ascending order.
 //     The drain warps pace the pipeline (the accumulator sets they free gate
