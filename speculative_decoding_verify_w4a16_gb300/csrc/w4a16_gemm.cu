@@ -436,11 +436,16 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                     const int ng = min(kUnitGroups, G - 2 * (sw.p + jj));
                     const int slot = f % kASlots;
                     const int set = f % DS;
-                    // afull first: the unit's weights were dequantized, so this
-                    // stage's previous use is complete and the parity of xfull
-                    // names this use (an issuer skips the stages it has no unit in)
-                    if (!warp_wait(afull(slot), (f / kASlots) & 1, ab) || !warp_wait(xfull(s), rg.ph, ab) ||
-                        (f >= DS && !warp_wait(dempty(set, me), uint32_t((f - DS) / kSetPeriod) & 1u, ab)))
+                    // afull before xfull: the unit's weights were dequantized, so
+                    // this stage's previous use is complete and the parity of
+                    // xfull names this use (an issuer skips the stages it has no
+                    // unit in).  The free accumulator set is waited for first
+                    // with four sets (M <= 16), last with two (measured).
+                    const bool set_ok = f < DS || NBLK != 1 ||
+                                        warp_wait(dempty(set, me), uint32_t((f - DS) / kSetPeriod) & 1u, ab);
+                    if (!set_ok || !warp_wait(afull(slot), (f / kASlots) & 1, ab) || !warp_wait(xfull(s), rg.ph, ab) ||
+                        (NBLK != 1 && f >= DS &&
+                         !warp_wait(dempty(set, me), uint32_t((f - DS) / kSetPeriod) & 1u, ab)))
                         break;
                     tc_fence_after();
                     const uint32_t dset = tmem + kDcol0 + set * L::kDUnit;
