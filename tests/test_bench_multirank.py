@@ -69,3 +69,22 @@ def test_profiled_traffic_needs_matching_sources(tmp_path):
     stale.write_text("source_sha256: 0000000000000000\ndram_bytes_read: 1\ndram_bytes_write: 2\n")
     assert bench.profiled_traffic(str(stale), bench.LM_HEAD_SOURCES) is None
     assert bench.profiled_traffic(str(tmp_path / "missing.md"), bench.LM_HEAD_SOURCES) is None
+
+
+def test_device_status_fails_the_bench_leg():
+    """A kernel that gave up a bounded wait leaves the device status word set:
+    the bench then refuses to print its timings and names the leg."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class FakeLib:
+        def __init__(self, status):
+            self.status = status
+
+        def get_status(self):
+            st, self.status = self.status, 0     # read and cleared, like w4v_get_status
+            return st
+
+    bench.check_device_status(FakeLib(0), "clean leg")
+    with pytest.raises(RuntimeError, match="36-layer sweep"):
+        bench.check_device_status(FakeLib(7), "36-layer sweep")
