@@ -275,6 +275,21 @@ w4v_status gdn_commit(float *state, const uint16_t *k, const uint16_t *v, const 
                       const float *beta, const int32_t *n_accepted, int B, int T, int H, int dk,
                       int dv, w4v_stream_t stream);
 
+/* gdn_step: the commit of the previous block and the verify of the next one
+ * in one launch, reading and writing the state once: the state is advanced
+ * by positions 0..n_prev[b] of the previous block (k_prev, v_prev,
+ * alpha_prev, beta_prev over T_prev positions; n clamped as in gdn_commit)
+ * and written back, then o_t of the current block is produced from it, with
+ * the same arithmetic as gdn_commit followed by gdn_verify (bit for bit).
+ * T_prev = 0 means no previous block (the *_prev pointers and n_prev are
+ * then ignored and the state is not written).  Arrays, layouts and limits as
+ * above, 0 <= T_prev <= 64. */
+w4v_status gdn_step(float *state, const uint16_t *k_prev, const uint16_t *v_prev,
+                    const float *alpha_prev, const float *beta_prev, const int32_t *n_prev, int T_prev,
+                    const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *alpha,
+                    const float *beta, int B, int T, int H, int dk, int dv, uint16_t *o,
+                    w4v_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

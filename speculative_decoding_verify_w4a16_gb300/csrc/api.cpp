@@ -222,6 +222,26 @@ w4v_status gdn_commit(float *state, const uint16_t *k, const uint16_t *v, const 
                            reinterpret_cast<cudaStream_t>(stream));
 }
 
+w4v_status gdn_step(float *state, const uint16_t *k_prev, const uint16_t *v_prev, const float *alpha_prev,
+                    const float *beta_prev, const int32_t *n_prev, int T_prev, const uint16_t *q, const uint16_t *k,
+                    const uint16_t *v, const float *alpha, const float *beta, int B, int T, int H, int dk, int dv,
+                    uint16_t *o, w4v_stream_t stream) {
+    w4v_status st = gdn_check(state, k, v, alpha, beta, B, T, H, dk, dv);
+    if (st != W4V_OK) return st;
+    if (T_prev < 0 || T_prev > w4v::kGdnMaxT) return W4V_ERR_SHAPE;
+    if (B == 0) return W4V_OK;
+    if (q == nullptr || o == nullptr) return W4V_ERR_ARG;
+    if (!w4v::aligned16(q) || !w4v::aligned16(o)) return W4V_ERR_ALIGN;
+    if (T_prev > 0) {
+        st = gdn_check(state, k_prev, v_prev, alpha_prev, beta_prev, B, T_prev, H, dk, dv);
+        if (st != W4V_OK) return st;
+        if (n_prev == nullptr) return W4V_ERR_ARG;
+        if (reinterpret_cast<uintptr_t>(n_prev) & 3u) return W4V_ERR_ALIGN;
+    }
+    return w4v::launch_gdn_step(state, k_prev, v_prev, alpha_prev, beta_prev, n_prev, T_prev, q, k, v, alpha, beta,
+                                o, B, T, H, dv, reinterpret_cast<cudaStream_t>(stream));
+}
+
 w4v_status spec_accept(const int32_t *target, const int32_t *draft, int B, int K, int32_t *n_accepted,
                        int32_t *out_tokens, w4v_stream_t stream) {
     if (B < 0 || K < 0 || K > 1024) return W4V_ERR_SHAPE;

@@ -34,6 +34,10 @@
 // CTA's v, alpha, beta for the whole block are staged in shared memory first.
 // Verify and commit run the same update, so the committed state is bit for
 // bit the state verify ran through.
+// gdn_step runs the commit of one block and the verify of the next in one
+// launch (the state read once and written once); the same update code.
+#include <algorithm>
+
 #include "runtime.h"
 #include "sm103_ptx.cuh"
 
@@ -226,6 +230,138 @@ w4v_status launch(const Args &a, cudaStream_t stream) {
     return W4V_OK;
 }
 
+
+// One verify block's inputs (and outputs).
+struct Block {
+    const __half *q, *k, *v;      // [B][T][H][dk|dk|dv] (q: verify only)
+    const float *alpha, *beta;    // [B][T][H]
+    __half *o;                    // verify: [B][T][H][dv]
+    int T;                        // positions in the block (its arrays' T)
+};
+
+struct StepArgs {
+    float *state;                 // [B][H][dv][dk]
+    Block cur;                    // the block verified
+    Block prev;                   // the previous block, committed first (T = 0: none)
+    const int32_t *n_accepted;    // accepted drafts of the previous block [B]
+    int B, H, dv;
+};
+
+// Runs positions 0..T-1 of block `blk` on the lane's rows s (8 rows, columns
+// 4 lane..4 lane+3).  kCommit = false: writes o_t; kCommit = true: only
+// advances s.  Every thread of the CTA calls it (it stages through shared
+// memory and synchronises).
+template <bool kCommit>
+__device__ __forceinline__ void run_block(const Block &blk, int T, float4 (&s)[kRowsPerWarp], float *smem, int b,
+                                          int h, int H, int dv, int row0) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rw = warp * kRowsPerWarp + (lane >> 2);   // the row whose sums this lane ends with
+    const int BT = blk.T;
+    float *ks = smem;
+    float *qs = ks + size_t(BT) * kDk;
+    float *vs = qs + (kCommit ? 0 : size_t(BT) * kDk);
+    float *as = vs + size_t(BT) * kRows;
+    float *bs = as + BT;
+    float *kq = bs + BT;
+    __half *kr = reinterpret_cast<__half *>(reinterpret_cast<uint8_t *>(smem) +
+                                            ((smem_f32(kCommit, BT) + 15) & ~size_t(15)));
+    __half *qr = kr + size_t(BT) * kDk;
+    __half *vr = qr + (kCommit ? 0 : size_t(BT) * kDk);
+    // every copy of the block's keys, queries, this CTA's values and the
+    // gates issued at once (16-byte pieces; 4 bytes for the gates)
+    for (int i = threadIdx.x; i < T * (kDk / 8); i += 32 * kWarps) {
+        const int t = i / (kDk / 8), c = 8 * (i % (kDk / 8));
+        const size_t base = ((size_t(b) * BT + t) * H + h) * kDk + c;
+        cp_async<16>(smem_u32(kr + t * kDk + c), blk.k + base, 16u);
+        if (!kCommit) cp_async<16>(smem_u32(qr + t * kDk + c), blk.q + base, 16u);
+    }
+    for (int i = threadIdx.x; i < T * (kRows / 8); i += 32 * kWarps) {
+        const int t = i / (kRows / 8), c = 8 * (i % (kRows / 8));
+        cp_async<16>(smem_u32(vr + t * kRows + c), blk.v + ((size_t(b) * BT + t) * H + h) * dv + row0 + c, 16u);
+    }
+    for (int t = threadIdx.x; t < T; t += 32 * kWarps) {
+        cp_async<4>(smem_u32(as + t), blk.alpha + (size_t(b) * BT + t) * H + h, 4u);
+        cp_async<4>(smem_u32(bs + t), blk.beta + (size_t(b) * BT + t) * H + h, 4u);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    // to fp32: one warp per position for k and q (and k_t . q_t: lane l adds
+    // columns 4l..4l+3, then a fixed tree), all threads for v
+    for (int t = warp; t < T; t += kWarps) {
+        const uint2 kw = *reinterpret_cast<const uint2 *>(kr + t * kDk + 4 * lane);
+        const float2 k01 = __half22float2(u32_as_h2(kw.x)), k23 = __half22float2(u32_as_h2(kw.y));
+        *reinterpret_cast<float4 *>(ks + t * kDk + 4 * lane) = make_float4(k01.x, k01.y, k23.x, k23.y);
+        if (!kCommit) {
+            const uint2 qw = *reinterpret_cast<const uint2 *>(qr + t * kDk + 4 * lane);
+            const float2 q01 = __half22float2(u32_as_h2(qw.x)), q23 = __half22float2(u32_as_h2(qw.y));
+            *reinterpret_cast<float4 *>(qs + t * kDk + 4 * lane) = make_float4(q01.x, q01.y, q23.x, q23.y);
+            float d = (k01.x * q01.x + k01.y * q01.y) + (k23.x * q23.x + k23.y * q23.y);
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, m);
+            if (lane == 0) kq[t] = d;
+        }
+    }
+    for (int i = threadIdx.x; i < T * kRows; i += 32 * kWarps) vs[i] = __half2float(vr[i]);
+    __syncthreads();
+
+    for (int t = 0; t < T; ++t) {
+        const float4 kv = *reinterpret_cast<const float4 *>(ks + t * kDk + 4 * lane);
+        const float a = as[t], be = bs[t];
+        // the 8 rows' parts of u = S_{t-1} k_t and w = S_{t-1} q_t
+        float pu[kRowsPerWarp], pw[kRowsPerWarp];
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) pu[r] = dot4(s[r], kv);
+        if (!kCommit) {
+            const float4 qv = *reinterpret_cast<const float4 *>(qs + t * kDk + 4 * lane);
+#pragma unroll
+            for (int r = 0; r < kRowsPerWarp; ++r) pw[r] = dot4(s[r], qv);
+        }
+        const float u = warp_rows_sum(pu, lane);                          // row rw
+        const float coef = be * (vs[t * kRows + rw] - a * u);
+        if (!kCommit) {
+            const float w = warp_rows_sum(pw, lane);
+            const float y = fmaf(a, w, coef * kq[t]);                     // (S_t q_t)[rw]
+            if ((lane & 3) == 0) blk.o[((size_t(b) * BT + t) * H + h) * dv + row0 + rw] = __float2half_rn(y);
+        }
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            const float cr = __shfl_sync(0xFFFFFFFFu, coef, 4 * r);       // row r's coefficient
+            update4(s[r], a, cr, kv);
+        }
+    }
+}
+
+__device__ __forceinline__ int accepted_positions(const int32_t *n_accepted, int b, int T) {
+    const int n = n_accepted[b];
+    return n < 0 ? 1 : (n + 1 > T ? T : n + 1);     // positions 0..n, n clamped to [0, T-1]
+}
+
+// Commit of the previous block, then verify of the current one from the
+// state just committed: one read and one write of the state for both.
+__global__ void __launch_bounds__(32 * kWarps)
+gdn_step_kernel(const StepArgs p) {
+    extern __shared__ __align__(16) float smem[];
+    grid_dep_wait();                         // inputs come from the previous kernels
+    grid_dep_launch();
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int row0 = blockIdx.x * kRows;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float *S = p.state + ((size_t(b) * p.H + h) * p.dv + row0 + warp * kRowsPerWarp) * kDk + 4 * lane;
+    float4 s[kRowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) s[r] = *reinterpret_cast<const float4 *>(S + r * kDk);
+    if (p.prev.T > 0) {
+        run_block<true>(p.prev, accepted_positions(p.n_accepted, b, p.prev.T), s, smem, b, h, p.H, p.dv, row0);
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) *reinterpret_cast<float4 *>(S + r * kDk) = s[r];
+        __syncthreads();                     // shared memory is staged again for the next block
+    }
+    run_block<false>(p.cur, p.cur.T, s, smem, b, h, p.H, p.dv, row0);
+}
+
+size_t step_smem(int T, int T_prev) { return std::max(smem_bytes(false, T), smem_bytes(true, T_prev)); }
+
 }  // namespace
 
 w4v_status launch_gdn(bool commit, float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -248,6 +384,42 @@ w4v_status launch_gdn(bool commit, float *state, const uint16_t *q, const uint16
     a.H = H;
     a.dv = dv;
     return commit ? launch<true>(a, stream) : launch<false>(a, stream);
+}
+
+w4v_status launch_gdn_step(float *state, const uint16_t *k_prev, const uint16_t *v_prev, const float *alpha_prev,
+                           const float *beta_prev, const int32_t *n_prev, int T_prev, const uint16_t *q,
+                           const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta, uint16_t *o,
+                           int B, int T, int H, int dv, cudaStream_t stream) {
+    const DeviceInfo *info = nullptr;
+    w4v_status st = device_info(&info);
+    if (st != W4V_OK) return st;
+    static int configured_for = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_for != dev) {
+        if (cudaFuncSetAttribute(gdn_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(step_smem(kMaxT, kMaxT))) != cudaSuccess) {
+            cudaGetLastError();
+            return W4V_ERR_CUDA;
+        }
+        configured_for = dev;
+    }
+    StepArgs a = {};
+    a.state = state;
+    a.cur = Block{reinterpret_cast<const __half *>(q), reinterpret_cast<const __half *>(k),
+                  reinterpret_cast<const __half *>(v), alpha, beta, reinterpret_cast<__half *>(o), T};
+    a.prev = Block{nullptr, reinterpret_cast<const __half *>(k_prev), reinterpret_cast<const __half *>(v_prev),
+                   alpha_prev, beta_prev, nullptr, T_prev};
+    a.n_accepted = n_prev;
+    a.B = B;
+    a.H = H;
+    a.dv = dv;
+    if (launch_pdl(gdn_step_kernel, dim3(dv / kRows, H, B), dim3(32 * kWarps), step_smem(T, T_prev), stream, a) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return W4V_ERR_CUDA;
+    }
+    return W4V_OK;
 }
 
 }  // namespace w4v

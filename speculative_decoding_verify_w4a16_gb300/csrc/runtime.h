@@ -111,6 +111,12 @@ constexpr int kGdnMaxT = 64;
 w4v_status launch_gdn(bool commit, float *state, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                       const float *alpha, const float *beta, const int32_t *n_accepted, uint16_t *o, int B, int T,
                       int H, int dv, cudaStream_t stream);
+// Commit of the previous block (T_prev positions, n_prev accepted; T_prev = 0:
+// none), then verify of the current one, in one launch.
+w4v_status launch_gdn_step(float *state, const uint16_t *k_prev, const uint16_t *v_prev, const float *alpha_prev,
+                           const float *beta_prev, const int32_t *n_prev, int T_prev, const uint16_t *q,
+                           const uint16_t *k, const uint16_t *v, const float *alpha, const float *beta, uint16_t *o,
+                           int B, int T, int H, int dv, cudaStream_t stream);
 
 // Greedy acceptance fused into the lm_head's last CTA: the M = B*(n_draft+1)
 // rows are B verify blocks of n_draft+1 positions each.

@@ -74,6 +74,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.gdn_verify.restype = I
             lib.gdn_commit.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P]
             lib.gdn_commit.restype = I
+            lib.gdn_step.argtypes = [P, P, P, P, P, P, I, P, P, P, P, P, I, I, I, I, I, P, P]
+            lib.gdn_step.restype = I
             _lib = lib
     return _lib
 
@@ -260,6 +262,27 @@ def gdn_verify(state, q, k, v, alpha, beta, out=None, stream=None):
     code = load().gdn_verify(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), B, T, H, dk, dv,
                              _ptr(out), _stream(stream))
     _check(code, "gdn_verify")
+    return out
+
+
+def gdn_step(state, prev, q, k, v, alpha, beta, out=None, stream=None):
+    """Commit the previous block into the fp32 state (prev = (k, v, alpha, beta,
+    n_accepted) of that block, or None) and return the outputs o [B][T][H][dv]
+    of the current block from the state just committed; one launch."""
+    import torch
+    B, H, dv, dk = state.shape
+    T = q.shape[1]
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=torch.float16, device=state.device)
+    if prev is None:
+        kp = vp = ap = bp = n = None
+        T_prev = 0
+    else:
+        kp, vp, ap, bp, n = prev
+        T_prev = kp.shape[1]
+    code = load().gdn_step(_ptr(state), _ptr(kp), _ptr(vp), _ptr(ap), _ptr(bp), _ptr(n), T_prev, _ptr(q), _ptr(k),
+                           _ptr(v), _ptr(alpha), _ptr(beta), B, T, H, dk, dv, _ptr(out), _stream(stream))
+    _check(code, "gdn_step")
     return out
 
 

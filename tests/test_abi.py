@@ -15,7 +15,7 @@ def test_exports_every_header_function(w4v_mod):
     names = w4v_mod.header_functions()
     for required in ("w4v_init", "w4v_get_status", "w4v_pack_int4", "w4a16_gemm",
                      "w8_lmhead_argmax", "spec_accept", "w8_lmhead_argmax_accept", "ngram_draft",
-                     "gdn_verify", "gdn_commit"):
+                     "gdn_verify", "gdn_commit", "gdn_step"):
         assert required in names
     lib = w4v_mod.load()
     for name in names:
@@ -149,6 +149,21 @@ def test_argument_validation_before_launch(w4v_mod):
     assert gc(FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 16, 4, 128, 128, None) == w4v_mod.ERR_ARG
     assert gc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, 1, 16, 4, 128, 128, None) == w4v_mod.ERR_ALIGN
     assert gc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 16, 0, 128, 128, None) == w4v_mod.ERR_SHAPE
+    # gdn_step(state, k_prev, v_prev, alpha_prev, beta_prev, n_prev, T_prev, q, k, v, alpha, beta,
+    #          B, T, H, dk, dv, o, stream)
+    gs = lib.gdn_step
+    F = FAKE
+    assert gs(F, F, F, F, F, F, 65, F, F, F, F, F, 1, 16, 4, 128, 128, F, None) == w4v_mod.ERR_SHAPE   # T_prev > 64
+    assert gs(F, F, F, F, F, F, -1, F, F, F, F, F, 1, 16, 4, 128, 128, F, None) == w4v_mod.ERR_SHAPE
+    assert gs(F, F, F, F, F, F, 16, F, F, F, F, F, 1, 65, 4, 128, 128, F, None) == w4v_mod.ERR_SHAPE   # T > 64
+    assert gs(F, F, F, F, F, None, 16, F, F, F, F, F, 1, 16, 4, 128, 128, F, None) == w4v_mod.ERR_ARG  # no n_prev
+    assert gs(F, None, F, F, F, F, 16, F, F, F, F, F, 1, 16, 4, 128, 128, F, None) == w4v_mod.ERR_ARG  # no k_prev
+    assert gs(F, F, F, F, F, F + 2, 16, F, F, F, F, F, 1, 16, 4, 128, 128, F, None) == w4v_mod.ERR_ALIGN
+    assert gs(F, F + 4, F, F, F, F, 16, F, F, F, F, F, 1, 16, 4, 128, 128, F, None) == w4v_mod.ERR_ALIGN
+    assert gs(F, F, F, F, F, F, 16, None, F, F, F, F, 1, 16, 4, 128, 128, F, None) == w4v_mod.ERR_ARG  # no q
+    assert gs(F, F, F, F, F, F, 16, F, F, F, F, F, 1, 16, 4, 128, 128, None, None) == w4v_mod.ERR_ARG  # no o
+    assert gs(None, None, None, None, None, None, 0, None, None, None, None, None, 0, 16, 4, 128, 128, None,
+              None) == w4v_mod.OK
     # packer
     assert lib.w4v_pack_int4(None, 128, 128, FAKE) == w4v_mod.ERR_ARG
     buf = ctypes.create_string_buffer(16)

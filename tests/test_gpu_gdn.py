@@ -125,3 +125,37 @@ def test_delta_rule_closed_form_gpu(w4v_mod, gpu):
     want[0, 0, :, j] = v[0, 0, 0].astype(np.float32)
     assert np.array_equal(Sd.cpu().numpy(), want)
     assert np.array_equal(o.cpu().numpy()[0, 0, 0], v[0, 0, 0])
+
+
+@pytest.mark.parametrize("B,T,T_prev,H,dv", [(2, 16, 16, 2, 128), (3, 21, 5, 3, 64), (1, 1, 1, 1, 32),
+                                             (2, 16, 0, 2, 64), (4, 8, 21, 2, 32)])
+def test_step_equals_commit_then_verify(w4v_mod, gpu, oracle_mod, B, T, T_prev, H, dv):
+    """gdn_step (commit of the previous block, verify of the next, one launch)
+    gives bit for bit the state and outputs of gdn_commit followed by
+    gdn_verify, and the oracle's within the recurrence's bounds; n spans none
+    accepted, some, all and out of range."""
+    d = lambda a: to_dev(a, gpu)
+    S0, q, k, v, alpha, beta = _block(300 + T, B, T, H, dv)
+    if T_prev > 0:
+        _, _, kp, vp, ap, bp = _block(400 + T_prev, B, T_prev, H, dv)
+        n = np.array([0, T_prev // 2, T_prev - 1, T_prev + 3][:B], np.int32)
+    Sa, Sb = d(S0), d(S0)
+    if T_prev > 0:
+        w4v_mod.gdn_commit(Sa, d(kp), d(vp), d(ap), d(bp), d(n))
+    o_ref = w4v_mod.gdn_verify(Sa, d(q), d(k), d(v), d(alpha), d(beta))
+    prev = (d(kp), d(vp), d(ap), d(bp), d(n)) if T_prev > 0 else None
+    o = w4v_mod.gdn_step(Sb, prev, d(q), d(k), d(v), d(alpha), d(beta))
+    torch.cuda.synchronize()
+    assert torch.equal(Sa, Sb)
+    assert torch.equal(o_ref, o)
+    if T_prev == 0:
+        assert np.array_equal(Sb.cpu().numpy(), S0)      # nothing to commit: state untouched
+    for b in range(B):
+        S_b = S0[b]
+        if T_prev > 0:
+            steps = min(int(n[b]), T_prev - 1) + 1
+            _, S_b = oracle_mod.gdn_recurrence(S0[b], np.zeros_like(kp[b, :steps]), kp[b, :steps], vp[b, :steps],
+                                               ap[b, :steps], bp[b, :steps])
+            assert _rel(Sb.cpu().numpy()[b], S_b) <= STATE_TOL, b
+        o_or, _ = oracle_mod.gdn_recurrence(S_b, q[b], k[b], v[b], alpha[b], beta[b])
+        assert _rel(o.cpu().numpy()[b], o_or) <= OUT_TOL + STATE_TOL, b

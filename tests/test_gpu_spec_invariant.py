@@ -74,12 +74,19 @@ class GpuToy:
         return (dev(q, np.float16), dev(k, np.float16), dev(v, np.float16),
                 dev(alpha, np.float32), dev(beta, np.float32))
 
-    def tokens_at(self, tokens, p0, T, S):
+    def tokens_at(self, tokens, p0, T, S, pending=None):
         """Greedy tokens after positions p0..p0+T-1 from committed state S (not
-        written); returns (tokens, the recurrence's inputs for a later commit)."""
+        written); returns (tokens, the recurrence's inputs for a later commit).
+        With `pending` = (inputs, n) of the previous block, that block's commit
+        runs first, in the same launch (gdn_step)."""
         h = self.inputs_at(tokens, p0, T)
         q, k, v, a, b = self.gdn_inputs(h)
-        o = self.w4v.gdn_verify(S, q, k, v, a, b)
+        if pending is None:
+            o = self.w4v.gdn_verify(S, q, k, v, a, b)
+        else:
+            (kp, vp, ap, bp), n = pending
+            nt = torch.tensor([n], dtype=torch.int32, device=self.gpu)
+            o = self.w4v.gdn_step(S, (kp, vp, ap, bp, nt), q, k, v, a, b)
         h = h + self.gemm(o.cpu().numpy().reshape(T, H), self.o)
         for (w_gu, w_d) in self.layers:
             gu = self.gemm(_rms(h).astype(np.float16), w_gu)
@@ -112,18 +119,22 @@ class GpuToy:
             out.append(int(t[0]))
         return out
 
-    def spec(self, prompt, n_new, K, drafter):
+    def spec(self, prompt, n_new, K, drafter, fused=False):
         ctx = list(prompt)
         S = self.fresh_state(ctx)
         out, steps = [], 0
+        pending = None
         while len(out) < n_new:
             d = np.asarray(drafter(ctx, K), np.int32).reshape(1, K)
             seq = ctx + [int(x) if x >= 0 else 0 for x in d[0]]
-            t, gin = self.tokens_at(seq, len(ctx) - 1, K + 1, S)
+            t, gin = self.tokens_at(seq, len(ctx) - 1, K + 1, S, pending)
             n, tok = self.w4v.spec_accept(torch.from_numpy(t.reshape(1, K + 1)).to(self.gpu),
                                           torch.from_numpy(d).to(self.gpu))
             n = int(n.cpu()[0])
-            self.commit(S, gin, n)                 # only positions 0..n of the block
+            if fused:
+                pending = (gin, n)                 # committed by the next block's launch
+            else:
+                self.commit(S, gin, n)             # only positions 0..n of the block
             emitted = [int(x) for x in tok.cpu().numpy()[0, : n + 1]]
             ctx.extend(emitted)
             out.extend(emitted)
@@ -165,6 +176,9 @@ def test_spec_equals_greedy_through_the_kernels(w4v_mod, gpu, seed):
         assert got == want, (seed, name)
         if name == "perfect_then_wrong":
             assert steps < n_new                    # accepted drafts did advance several tokens a step
+    # the previous block's commit fused into the next block's launch (gdn_step)
+    got, _ = toy.spec(prompt, n_new, 15, oracle_perfect, fused=True)
+    assert got == want, (seed, "fused commit")
     assert w4v_mod.get_status() == 0
 
 
