@@ -676,8 +676,9 @@ def run_ngram(dev, w4v, torch):
 def run_gdn(dev, w4v, torch):
     """Recurrent-state handling of one Gated DeltaNet layer across a verify
     block of 16 positions: gdn_verify (outputs, state read) then gdn_commit
-    (replay of the accepted prefix, state written), assumed head shape
-    32 heads x 128 x 128, for 1 and 8 sequences."""
+    (replay of the accepted prefix, state written), and gdn_step (the
+    previous block's commit and this block's verify in one launch), assumed
+    head shape 32 heads x 128 x 128, for 1 and 8 sequences."""
     out = {}
     H, d, T = 32, 128, 16
     g = torch.Generator(device=dev)
@@ -696,10 +697,17 @@ def run_gdn(dev, w4v, torch):
             w4v.gdn_verify(S, q, k, v, a, be, out=o)
             w4v.gdn_commit(S, k, v, a, be, n)
 
+        def fused():
+            # the previous block's commit and this block's verify in one launch
+            w4v.gdn_step(S, (k, v, a, be, n), q, k, v, a, be, out=o)
+
         ms = time_graph(torch, lambda: [step() for _ in range(20)]) / 20
+        ms_f = time_graph(torch, lambda: [fused() for _ in range(20)]) / 20
         state_bytes = 3 * B * H * d * d * 4          # verify read, commit read + write
         out["B=%d" % B] = {"us": round(ms * 1e3, 2), "T": T, "heads": H, "dk": d, "dv": d,
-                           "state_GB/s": round(state_bytes / (ms * 1e-3) / 1e9, 1)}
+                           "state_GB/s": round(state_bytes / (ms * 1e-3) / 1e9, 1),
+                           "step_us": round(ms_f * 1e3, 2),
+                           "step_state_GB/s": round(2 * B * H * d * d * 4 / (ms_f * 1e-3) / 1e9, 1)}
     return out
 
 
