@@ -104,12 +104,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDcol0 = kASlots * kASlotCols;
 constexpr int kAhead = 16;                         // groups of scales / zeros kept in flight
 constexpr int kRing = 32;                          // ring entries (> kAhead + 1)
-// Group size 32 (scales folded into the weights): per dequant warp a ring of
-// 128-k groups, each entry four sub-groups' scales and zero points of the
-// warp's 32 rows; it reuses the space of the two rings above.
-constexpr int kFAhead = 3;
-constexpr int kFRing = 4;
-constexpr int kFEntry = 4 * 32 * 2 + 4 * 32;       // 256 B scales + 128 B zeros
+// Group size 32 (scales folded into the weights): each stage's sub-group
+// scales (16 rows of one tile, 4 KB) and zero points (2 KB) arrive with the
+// stage's weights, into per-stage slots in the space of the group-128 rings.
+constexpr int kFSclSlotBytes = 4 * kStageGroups * kTileN * 2;
+constexpr int kFZroSlotBytes = 4 * kStageGroups * kTileN;
 
 // Group size 128: the producer copies each stage's scales (its four groups'
 // rows of one tile) into a ring of kSclSlots slots with one 2-D TMA, and the
@@ -144,9 +143,10 @@ struct Layout {
     static constexpr int kScl = kBarBytes;                         // offsets inside the fixed block
     static constexpr int kZro = kScl + kDrWarps * kRing * 64;      // 32 fp16 scales per entry
     static constexpr int kMisc = kZro + kDqWarps * kRing * 32;     // 32 uint8 zeros per entry
-    static_assert(kDqWarps * kFRing * kFEntry <= kMisc - kScl, "group-32 ring fits the rings' space");
+    static_assert(kMaxStages * kFSclSlotBytes <= kMisc - kScl, "group-32 stage scales fit the rings' space");
     static constexpr int kSst = kMisc + 128;                        // stage scale ring (128-byte aligned)
     static constexpr int kFixed = kSst + kSclSlots * kSclSlotBytes;
+    static_assert(kMaxStages * kFZroSlotBytes <= kSclSlots * kSclSlotBytes, "group-32 stage zeros fit");
     static constexpr int kPart = 16 * NBLK * kTileN;               // floats of one partial tile
     __host__ __device__ static constexpr int bytes(int stages) { return stages * kStage + kFixed + 1024; }
     static_assert(kStage % 1024 == 0, "stage alignment");
@@ -173,7 +173,7 @@ struct Args {
     int stages;                       // pipeline stages in shared memory
     int cluster;                      // CTAs per tile (cluster size); 0 = stream-K
     int static_w;                     // weights, scales, zeros not written by earlier work in flight
-    int sbox_w, sbox_h;               // scale box of one stage: min(128, N) x min(4, K / 128)
+    int sbox_w, sbox_h;               // scale box of one stage: min(128, N) x min(4 or 16, K / group)
 };
 
 // A unit: tile t, pair p (groups 2p and, if it exists, 2p + 1).
@@ -252,7 +252,7 @@ struct GroupWalk {
 template <int NBLK, bool kFold>
 __global__ void __launch_bounds__(kThreads, 1)
 w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap,
-                    const Args p) {
+                    const __grid_constant__ CUtensorMap zmap, const Args p) {
     using L = Layout<NBLK>;
     constexpr int DS = L::kDSets;
     constexpr int MS = kMaxStages;
@@ -344,12 +344,23 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         // ---------------------------------------------------------- producer
         const uint64_t pol_w = l2_policy_evict_first();
         const uint64_t pol_x = l2_policy_evict_last();
+        const bool fold_zeros = kFold && p.zeros != nullptr;
+        const uint32_t fold_bytes = kFold ? uint32_t(p.sbox_w * p.sbox_h) * (fold_zeros ? 3u : 2u) : 0u;
         auto load_weights = [&](const StageWalk &w, int n, int s) {
             const int g0 = w.gbeg();
             const uint32_t wbytes = (w.gend(n) - g0) * kGroupBytes;
-            mbar_arrive_expect_tx(wfull(s), wbytes);
+            mbar_arrive_expect_tx(wfull(s), wbytes + fold_bytes);
             bulk_load(base_s + s * L::kStage + L::kW, p.wq + (size_t(w.t) * G + g0) * kGroupBytes, wbytes, wfull(s),
                       pol_w);
+            if (kFold) {
+                // the stage's sub-group scales and zero points ride with its weights
+                // (rows past N or K land as zero)
+                tma_load_2d(base_s + fixed_off + L::kScl + uint32_t(s * kFSclSlotBytes), &smap, w.t * kTileN, 4 * g0,
+                            wfull(s), pol_w);
+                if (fold_zeros)
+                    tma_load_2d(base_s + fixed_off + L::kSst + uint32_t(s * kFZroSlotBytes), &zmap, w.t * kTileN,
+                                4 * g0, wfull(s), pol_w);
+            }
         };
         // stage use u's scales into slot u % kSclSlots (rows past N or K land as zero)
         auto load_scales = [&](const StageWalk &w, int u) {
@@ -361,7 +372,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         int w_early = 0;                         // stages whose weights went out before the wait
         if (lane == 0) {
             prefetch_tensormap(&xmap);
-            if (!kFold) prefetch_tensormap(&smap);
+            prefetch_tensormap(&smap);
+            if (kFold && p.zeros != nullptr) prefetch_tensormap(&zmap);
             StageWalk pw(ub, nP, G, nunits);
             for (int st = 0; st < S && pw.left > 0; ++st) {
                 const int n = pw.size();
@@ -516,52 +528,22 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         if (!kFold && has_zeros)
             for (int k = 0; k < kAhead; ++k) zero_issue();
 
-        // Group size 32: scales and zero points of the four sub-groups of each
-        // 128-k group, kFAhead groups ahead (rows past N read as 0 and are
-        // never stored).
-        const uint32_t fring = smem_u32(base + fixed_off + L::kScl) + uint32_t(dq * kFRing * kFEntry);
-        int fissued = 0, fused = 0;
-        auto fold_issue = [&]() {
-            if (zw.more()) {
-                const uint32_t e = fring + uint32_t((fissued % kFRing) * kFEntry);
-                const int g4 = 4 * zw.g();
-                if (lane < 16) {
-                    const int sub = lane >> 2;
-                    const int n0 = zw.t() * kTileN + 32 * q + 8 * (lane & 3);
-                    const bool in = n0 < p.N;
-                    cp_async<16>(e + sub * 64 + (lane & 3) * 16,
-                                 in ? static_cast<const void *>(p.scales + size_t(g4 + sub) * p.N + n0) : p.scales,
-                                 in ? 16u : 0u);
-                } else if (lane < 24 && has_zeros) {
-                    const int sub = (lane - 16) >> 1;
-                    const int n0 = zw.t() * kTileN + 32 * q + 16 * (lane & 1);
-                    const bool in = n0 < p.N;
-                    cp_async<16>(e + 256 + sub * 32 + (lane & 1) * 16,
-                                 in ? static_cast<const void *>(p.zeros + size_t(g4 + sub) * p.N + n0) : p.zeros,
-                                 in ? 16u : 0u);
-                }
-                zw.next();
-            }
-            ++fissued;
-            cp_async_commit();
-        };
-        // The next group's four zero points (bytes of zz) and scales (halves of ss0, ss1).
-        auto fold_take = [&](uint32_t &zz, uint32_t &ss0, uint32_t &ss1) {
-            cp_async_wait<kFAhead - 1>();
-            __syncwarp();
-            const uint32_t e = fring + uint32_t((fused % kFRing) * kFEntry);
-            ss0 = uint32_t(lds_u16(e + 0 * 64 + 2 * lane)) | (uint32_t(lds_u16(e + 1 * 64 + 2 * lane)) << 16);
-            ss1 = uint32_t(lds_u16(e + 2 * 64 + 2 * lane)) | (uint32_t(lds_u16(e + 3 * 64 + 2 * lane)) << 16);
+        // Group size 32: the four sub-groups' zero points (bytes of zz) and
+        // scales (halves of ss0, ss1) of 128-k group gs of the stage in slot s,
+        // for this lane's row.
+        auto fold_read = [&](int s, int gs, uint32_t &zz, uint32_t &ss0, uint32_t &ss1) {
+            const uint32_t sp = uint32_t(p.sbox_w * 2), zp = uint32_t(p.sbox_w);
+            const uint32_t e = base_s + fixed_off + L::kScl + uint32_t(s * kFSclSlotBytes) + uint32_t(4 * gs) * sp +
+                               uint32_t(2 * r);
+            ss0 = uint32_t(lds_u16(e)) | (uint32_t(lds_u16(e + sp)) << 16);
+            ss1 = uint32_t(lds_u16(e + 2 * sp)) | (uint32_t(lds_u16(e + 3 * sp)) << 16);
             zz = 0x08080808u;
-            if (has_zeros)
-                zz = lds_u8(e + 256 + lane) | (lds_u8(e + 256 + 32 + lane) << 8) | (lds_u8(e + 256 + 64 + lane) << 16) |
-                     (lds_u8(e + 256 + 96 + lane) << 24);
-            ++fused;
-            __syncwarp();
-            fold_issue();
+            if (has_zeros) {
+                const uint32_t z = base_s + fixed_off + L::kSst + uint32_t(s * kFZroSlotBytes) + uint32_t(4 * gs) * zp +
+                                   uint32_t(r);
+                zz = lds_u8(z) | (lds_u8(z + zp) << 8) | (lds_u8(z + 2 * zp) << 16) | (lds_u8(z + 3 * zp) << 24);
+            }
         };
-        if (kFold)
-            for (int k = 0; k < kFAhead; ++k) fold_issue();
 
         // One 64-k step: chunks 2kh, 2kh+1 of the packed group at shared address `grp`,
         // dequantized with zero point z into 32 half2 registers.
@@ -653,7 +635,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                     const uint32_t z = gg == 0 ? z0 : z1;
                     uint32_t zz = 0u, ss0 = 0u, ss1 = 0u;
                     if constexpr (kFold) {
-                        fold_take(zz, ss0, ss1);
+                        fold_read(s, kUnitGroups * jj + gg, zz, ss0, ss1);
                         dequant_fold(gp, 0, zz, ss0, ss1, ra);
                     } else {
                         dequant(gp, 0, z, ra);
@@ -1034,7 +1016,8 @@ w4v_status configure() {
 }
 
 template <int NBLK, bool kFold>
-w4v_status launch(const CUtensorMap &xmap, const CUtensorMap &smap, Args &a, int cluster, cudaStream_t stream) {
+w4v_status launch(const CUtensorMap &xmap, const CUtensorMap &smap, const CUtensorMap &zmap, Args &a, int cluster,
+                  cudaStream_t stream) {
     using L = Layout<NBLK>;
     w4v_status st = configure<NBLK, kFold>();
     if (st != W4V_OK) return st;
@@ -1043,7 +1026,7 @@ w4v_status launch(const CUtensorMap &xmap, const CUtensorMap &smap, Args &a, int
     if (cluster > 0) a.P = a.n_tiles * cluster;
     const size_t smem = size_t(L::bytes(a.stages));
     if (launch_pdl_cluster(w4a16_decode_kernel<NBLK, kFold>, dim3(a.P), dim3(kThreads), smem, stream, cluster, xmap,
-                           smap, a) !=
+                           smap, zmap, a) !=
         cudaSuccess) {
         cudaGetLastError();
         return W4V_ERR_CUDA;
@@ -1110,16 +1093,24 @@ w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t
     if (st != W4V_OK) return st;
     // scales [K/group][N]: one stage's rows (up to 4 groups) of one tile (up to 128 columns)
     a.sbox_w = std::min(kTileN, N);
-    a.sbox_h = std::min(kStageGroups, K / group);
+    a.sbox_h = std::min(kStageGroups * (kGroup / group), K / group);
     CUtensorMap smap;
     st = encode_tmap_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, scales, uint64_t(N), uint64_t(K / group),
                         uint64_t(N) * 2, uint32_t(a.sbox_w), uint32_t(a.sbox_h), CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != W4V_OK) return st;
+    // group 32 with zero points: [K/32][N] uint8, the same box (N is a multiple of 16)
+    CUtensorMap zmap = {};
+    if (group == 32 && zeros != nullptr) {
+        st = encode_tmap_2d(&zmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, zeros, uint64_t(N), uint64_t(K / group), uint64_t(N),
+                            uint32_t(a.sbox_w), uint32_t(a.sbox_h), CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st != W4V_OK) return st;
+    }
     const int cluster = cluster_for(a.n_tiles, a.n_pairs, info->sm_count);
     if (group == 32)
-        return nblk == 1 ? launch<1, true>(xmap, smap, a, cluster, stream)
-                         : launch<2, true>(xmap, smap, a, cluster, stream);
-    return nblk == 1 ? launch<1, false>(xmap, smap, a, cluster, stream) : launch<2, false>(xmap, smap, a, cluster, stream);
+        return nblk == 1 ? launch<1, true>(xmap, smap, zmap, a, cluster, stream)
+                         : launch<2, true>(xmap, smap, zmap, a, cluster, stream);
+    return nblk == 1 ? launch<1, false>(xmap, smap, zmap, a, cluster, stream)
+                     : launch<2, false>(xmap, smap, zmap, a, cluster, stream);
 }
 
 }  // namespace w4v
