@@ -41,31 +41,43 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _bind(lib):
+    """Declare the argument types of the C entry points on a loaded library."""
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_half_to_double.restype = ctypes.c_double
+    lib.oracle_dequant_w4.argtypes = [P, P, P, I, I, I, P]
+    lib.oracle_w4a16_gemm.argtypes = [P, P, P, P, I, I, I, I, P, P]
+    lib.oracle_matmul_dequantized.argtypes = [P, P, I, I, I, P]
+    lib.oracle_w4a16_gemm_sampled.argtypes = [P, P, P, P, I, I, I, P, P, I, P]
+    lib.oracle_lmhead_logits.argtypes = [P, P, P, I, I, I, P]
+    lib.oracle_lmhead_argmax_rows.argtypes = [P, P, P, I, I, P, I, P, P, P]
+    lib.oracle_argmax_f64.argtypes = [P, I, I, P]
+    lib.oracle_argmax_f32.argtypes = [P, I, I, P]
+    lib.oracle_spec_accept.argtypes = [P, P, I, I, P, P]
+    lib.oracle_ngram_draft.argtypes = [P, P, I, I, I, I, I, P, P]
+    lib.oracle_gdn_recurrence.argtypes = [P, P, P, P, P, P, I, I, I, P, P]
+    lib.oracle_num_threads.restype = I
+    lib.oracle_set_num_threads.argtypes = [I]
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
             build()
-            lib = ctypes.CDLL(_LIB_PATH)
-            P = ctypes.c_void_p
-            I = ctypes.c_int
-            lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
-            lib.oracle_half_to_double.restype = ctypes.c_double
-            lib.oracle_dequant_w4.argtypes = [P, P, P, I, I, I, P]
-            lib.oracle_w4a16_gemm.argtypes = [P, P, P, P, I, I, I, I, P, P]
-            lib.oracle_matmul_dequantized.argtypes = [P, P, I, I, I, P]
-            lib.oracle_w4a16_gemm_sampled.argtypes = [P, P, P, P, I, I, I, P, P, I, P]
-            lib.oracle_lmhead_logits.argtypes = [P, P, P, I, I, I, P]
-            lib.oracle_lmhead_argmax_rows.argtypes = [P, P, P, I, I, P, I, P, P, P]
-            lib.oracle_argmax_f64.argtypes = [P, I, I, P]
-            lib.oracle_argmax_f32.argtypes = [P, I, I, P]
-            lib.oracle_spec_accept.argtypes = [P, P, I, I, P, P]
-            lib.oracle_ngram_draft.argtypes = [P, P, I, I, I, I, I, P, P]
-            lib.oracle_gdn_recurrence.argtypes = [P, P, P, P, P, P, I, I, I, P, P]
-            lib.oracle_num_threads.restype = I
-            lib.oracle_set_num_threads.argtypes = [I]
-            _lib = lib
+            _lib = _bind(ctypes.CDLL(_LIB_PATH))
     return _lib
+
+
+def _use_library(path: str) -> None:
+    """Route every function of this module through another build of oracle.c
+    (the pin tests run this way against copies with a planted mistake)."""
+    global _lib
+    with _lock:
+        _lib = _bind(ctypes.CDLL(path))
 
 
 def _ptr(a):

@@ -26,10 +26,18 @@ def read_golden(name):
     return rows
 
 
+ORACLE_UNDER_TEST = "W4V_ORACLE_UNDER_TEST"
+
+
 @pytest.fixture(scope="session")
 def oracle_mod():
+    """The oracle; with W4V_ORACLE_UNDER_TEST naming a shared library, that build
+    of oracle.c instead (test_oracle_mutants.py runs the pins that way)."""
     import oracle
     oracle.build()
+    alt = os.environ.get(ORACLE_UNDER_TEST)
+    if alt:
+        oracle._use_library(alt)
     return oracle
 
 

@@ -89,3 +89,27 @@ def test_argmax_rows_matches_full(oracle_mod):
         assert tok[i] == full[r]
         srt = np.sort(L[r])
         assert best[i] == srt[-1] and second[i] == srt[-2]
+
+
+def test_argmax_rows_ties_go_to_the_lowest_index(oracle_mod):
+    """Vocabulary rows copied with their scale give exactly equal logits: the
+    row-sampled argmax takes the first copy, and the second-best logit equals
+    the best one (known by construction, no full logits needed)."""
+    M, K, V = 3, 64, 40
+    rng = np.random.default_rng(4)
+    X = rng.standard_normal((M, K)).astype(np.float16)
+    W = rng.integers(-127, 128, (V, K), dtype=np.int8)
+    s = rng.uniform(1e-3, 5e-3, V).astype(np.float16)
+    tok0, _, _ = oracle_mod.lmhead_argmax_rows(X, W, s, np.arange(M, dtype=np.int32))
+    # copy each row's winner to two other slots, then also to the first slot
+    for r in range(M):
+        W2, s2 = W.copy(), s.copy()
+        w = int(tok0[r])
+        copies = [d for d in (V - 1, V - 7) if d != w]
+        for dst in copies:
+            W2[dst], s2[dst] = W[w], s[w]
+        tok, best, second = oracle_mod.lmhead_argmax_rows(X, W2, s2, np.array([r], np.int32))
+        assert tok[0] == min([w] + copies) and second[0] == best[0]
+        W2[0], s2[0] = W[w], s[w]
+        tok, best, second = oracle_mod.lmhead_argmax_rows(X, W2, s2, np.array([r], np.int32))
+        assert tok[0] == 0 and second[0] == best[0]
