@@ -48,8 +48,9 @@
 //     stage's scales (four groups of one tile) with one 2-D TMA into a ring
 //     of eight slots, which the drain frees stage by stage.  A load issued
 //     by a drain warp stalls behind the weight stream's queued requests.
-//     Zero points (and the group-32 scales) are read by the dequant warps,
-//     which keep them 16 (3) groups ahead with cp.async into rings.
+//     Zero points (and the group-32 scales) come the same way: the
+//     producer's 2-D TMA of the stage's rows lands on the stage's weight
+//     barrier, in per-stage slots that the dequant warps read.
 //   * Work split.  With few 128-row tiles, each tile belongs to a
 //     thread-block cluster of C CTAs (C about the square root of the units
 //     per tile, at most 8, all clusters in one wave)
@@ -102,13 +103,15 @@ static_assert(kASlots == kIssuers && kStageUnits <= kIssuers,
 constexpr uint32_t kASlotCols = kUnitGroups * 64;  // fp16 pairs of 128 rows x 256 k
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDcol0 = kASlots * kASlotCols;
-constexpr int kAhead = 16;                         // groups of scales / zeros kept in flight
-constexpr int kRing = 32;                          // ring entries (> kAhead + 1)
+constexpr int kRing = 32;                          // sizes the metadata region below
 // Group size 32 (scales folded into the weights): each stage's sub-group
 // scales (16 rows of one tile, 4 KB) and zero points (2 KB) arrive with the
-// stage's weights, into per-stage slots in the space of the group-128 rings.
+// stage's weights, into per-stage slots of the metadata region.
 constexpr int kFSclSlotBytes = 4 * kStageGroups * kTileN * 2;
 constexpr int kFZroSlotBytes = 4 * kStageGroups * kTileN;
+// Group size 128 with zero points: each stage's rows of the zero table (four
+// groups x one tile) arrive with its weights into a per-stage slot.
+constexpr int kZroSlotBytes = kStageGroups * kTileN;
 
 // Group size 128: the producer copies each stage's scales (its four groups'
 // rows of one tile) into a ring of kSclSlots slots with one 2-D TMA, and the
@@ -123,7 +126,7 @@ constexpr int kMaxSmem = 227 * 1024;
 // size chosen is about the square root of the units per tile.
 constexpr int kMaxCluster = 8;
 
-// Shared memory: S stages, then a fixed block of barriers, rings and flags.
+// Shared memory: S stages, then a fixed block of barriers, metadata slots and flags.
 // In cluster mode each CTA's partial tile ([row][16 NBLK] fp32) is left in
 // its first stage once all its MMAs have completed.
 template <int NBLK>
@@ -141,12 +144,13 @@ struct Layout {
     static constexpr int kNumBars = 3 * kMaxStages + 3 * kASlots + (1 + kIssuers) * kDSets + 2 + 2 * kSclSlots;
     static constexpr int kBarBytes = (8 * kNumBars + 127) & ~127;
     static constexpr int kScl = kBarBytes;                         // offsets inside the fixed block
-    static constexpr int kZro = kScl + kDrWarps * kRing * 64;      // 32 fp16 scales per entry
-    static constexpr int kMisc = kZro + kDqWarps * kRing * 32;     // 32 uint8 zeros per entry
-    static_assert(kMaxStages * kFSclSlotBytes <= kMisc - kScl, "group-32 stage scales fit the rings' space");
+    static constexpr int kZro = kScl + kDrWarps * kRing * 64;      // group-32 scale slots from kScl
+    static constexpr int kMisc = kZro + kDqWarps * kRing * 32;     // group-128 zero slots from kZro
+    static_assert(kMaxStages * kFSclSlotBytes <= kMisc - kScl, "group-32 stage scales fit the metadata region");
     static constexpr int kSst = kMisc + 128;                        // stage scale ring (128-byte aligned)
     static constexpr int kFixed = kSst + kSclSlots * kSclSlotBytes;
     static_assert(kMaxStages * kFZroSlotBytes <= kSclSlots * kSclSlotBytes, "group-32 stage zeros fit");
+    static_assert(kMaxStages * kZroSlotBytes <= kMisc - kZro, "group-128 stage zeros fit");
     static constexpr int kPart = 16 * NBLK * kTileN;               // floats of one partial tile
     __host__ __device__ static constexpr int bytes(int stages) { return stages * kStage + kFixed + 1024; }
     static_assert(kStage % 1024 == 0, "stage alignment");
@@ -222,25 +226,6 @@ struct StageRing {
             s = 0;
             ph ^= 1u;
             wrapped = true;
-        }
-    }
-};
-
-// Groups of every `step`-th unit starting at the CTA's local unit `first`,
-// in order: drives the scale and zero-point rings.
-struct GroupWalk {
-    UnitPos u;
-    int f, step, nunits, gi;
-    __device__ GroupWalk(long long ub, int first, int stride, int units, int n_pairs, int n_groups)
-        : u(ub + first, n_pairs, n_groups), f(first), step(stride), nunits(units), gi(0) {}
-    __device__ bool more() const { return f < nunits; }
-    __device__ int t() const { return u.t; }
-    __device__ int g() const { return u.g0() + gi; }
-    __device__ void next() {
-        if (++gi == u.ng()) {
-            gi = 0;
-            f += step;
-            for (int k = 0; k < step; ++k) u.next();
         }
     }
 };
@@ -344,12 +329,14 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         // ---------------------------------------------------------- producer
         const uint64_t pol_w = l2_policy_evict_first();
         const uint64_t pol_x = l2_policy_evict_last();
-        const bool fold_zeros = kFold && p.zeros != nullptr;
-        const uint32_t fold_bytes = kFold ? uint32_t(p.sbox_w * p.sbox_h) * (fold_zeros ? 3u : 2u) : 0u;
+        const bool stage_zeros = p.zeros != nullptr;
+        // bytes riding on the weight barrier: group 32 scales (and zeros), group 128 zeros
+        const uint32_t meta_bytes = uint32_t(p.sbox_w * p.sbox_h) *
+                                    (kFold ? (stage_zeros ? 3u : 2u) : (stage_zeros ? 1u : 0u));
         auto load_weights = [&](const StageWalk &w, int n, int s) {
             const int g0 = w.gbeg();
             const uint32_t wbytes = (w.gend(n) - g0) * kGroupBytes;
-            mbar_arrive_expect_tx(wfull(s), wbytes + fold_bytes);
+            mbar_arrive_expect_tx(wfull(s), wbytes + meta_bytes);
             bulk_load(base_s + s * L::kStage + L::kW, p.wq + (size_t(w.t) * G + g0) * kGroupBytes, wbytes, wfull(s),
                       pol_w);
             if (kFold) {
@@ -357,9 +344,12 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                 // (rows past N or K land as zero)
                 tma_load_2d(base_s + fixed_off + L::kScl + uint32_t(s * kFSclSlotBytes), &smap, w.t * kTileN, 4 * g0,
                             wfull(s), pol_w);
-                if (fold_zeros)
+                if (stage_zeros)
                     tma_load_2d(base_s + fixed_off + L::kSst + uint32_t(s * kFZroSlotBytes), &zmap, w.t * kTileN,
                                 4 * g0, wfull(s), pol_w);
+            } else if (stage_zeros) {
+                tma_load_2d(base_s + fixed_off + L::kZro + uint32_t(s * kZroSlotBytes), &zmap, w.t * kTileN, g0,
+                            wfull(s), pol_w);
             }
         };
         // stage use u's scales into slot u % kSclSlots (rows past N or K land as zero)
@@ -373,7 +363,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         if (lane == 0) {
             prefetch_tensormap(&xmap);
             prefetch_tensormap(&smap);
-            if (kFold && p.zeros != nullptr) prefetch_tensormap(&zmap);
+            if (p.zeros != nullptr) prefetch_tensormap(&zmap);
             StageWalk pw(ub, nP, G, nunits);
             for (int st = 0; st < S && pw.left > 0; ++st) {
                 const int n = pw.size();
@@ -496,37 +486,12 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         // reads only weights, zero points and shared memory
         if (!p.static_w) grid_dep_wait();
 
-        // Zero points of this warp's 32 rows for the groups of its units,
-        // kAhead groups ahead (rows past N read as 0 and are never stored).
+        // Zero points (group 128): row g of the stage's slot, for this lane's
+        // row of the tile (rows past N read as 0 and are never stored).
         const bool has_zeros = p.zeros != nullptr;
-        const uint8_t *zring = base + fixed_off + L::kZro + dq * kRing * 32;
-        GroupWalk zw(ub, par, 2, nunits, nP, G);
-        int zissued = 0, zused = 0;
-        auto zero_issue = [&]() {
-            if (zw.more()) {
-                if (lane < 4) {
-                    const int n0 = zw.t() * kTileN + 32 * q + 8 * lane;
-                    const bool in = n0 < p.N;
-                    cp_async<8>(smem_u32(zring + (zissued % kRing) * 32 + 8 * lane),
-                                in ? static_cast<const void *>(p.zeros + size_t(zw.g()) * p.N + n0) : p.zeros,
-                                in ? 8u : 0u);
-                }
-                zw.next();
-            }
-            ++zissued;
-            cp_async_commit();
+        auto zero_read = [&](int s, int gs) -> uint32_t {
+            return lds_u8(base_s + fixed_off + L::kZro + uint32_t(s * kZroSlotBytes) + uint32_t(gs * p.sbox_w + r));
         };
-        auto zero_take = [&]() -> uint32_t {
-            cp_async_wait<kAhead - 1>();
-            __syncwarp();
-            const uint32_t z = lds_u8(smem_u32(zring) + (zused % kRing) * 32 + lane);
-            ++zused;
-            __syncwarp();
-            zero_issue();
-            return z;
-        };
-        if (!kFold && has_zeros)
-            for (int k = 0; k < kAhead; ++k) zero_issue();
 
         // Group size 32: the four sub-groups' zero points (bytes of zz) and
         // scales (halves of ss0, ss1) of 128-k group gs of the stage in slot s,
@@ -622,8 +587,6 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                 const int slot = f % kASlots;
                 const uint32_t g0p = base_s + s * L::kStage + L::kW + (kUnitGroups * jj) * kGroupBytes;
                 const uint32_t g1p = g0p + kGroupBytes;
-                const uint32_t z0 = (!kFold && has_zeros) ? zero_take() : 8u;
-                const uint32_t z1 = (!kFold && has_zeros && ng > 1) ? zero_take() : 8u;
                 const uint32_t col = tmem + lane_base + slot * kASlotCols;
                 // group gg: half 0 into ra, half 1 into rb; each store
                 // overlaps the next half's arithmetic (one copy of the
@@ -632,7 +595,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
 #pragma unroll 1
                 for (int gg = 0; gg < ng; ++gg) {
                     const uint32_t gp = gg == 0 ? g0p : g1p;
-                    const uint32_t z = gg == 0 ? z0 : z1;
+                    const uint32_t z = (!kFold && has_zeros) ? zero_read(s, kUnitGroups * jj + gg) : 8u;
                     uint32_t zz = 0u, ss0 = 0u, ss1 = 0u;
                     if constexpr (kFold) {
                         fold_read(s, kUnitGroups * jj + gg, zz, ss0, ss1);
@@ -674,7 +637,6 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
             f0 += n;
             sw.next(n);
         }
-        cp_async_wait<0>();                     // no ring copy outlives the loop (abort path)
     } else if (warp >= kWarpDr0 && warp < kWarpDr0 + kDrWarps) {
         // ----------------------------------------------------------- drain
         const int dr = warp - kWarpDr0;
@@ -1098,9 +1060,9 @@ w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t
     st = encode_tmap_2d(&smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, scales, uint64_t(N), uint64_t(K / group),
                         uint64_t(N) * 2, uint32_t(a.sbox_w), uint32_t(a.sbox_h), CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != W4V_OK) return st;
-    // group 32 with zero points: [K/32][N] uint8, the same box (N is a multiple of 16)
+    // zero points [K/group][N] uint8, the same box (N is a multiple of 16)
     CUtensorMap zmap = {};
-    if (group == 32 && zeros != nullptr) {
+    if (zeros != nullptr) {
         st = encode_tmap_2d(&zmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, zeros, uint64_t(N), uint64_t(K / group), uint64_t(N),
                             uint32_t(a.sbox_w), uint32_t(a.sbox_h), CU_TENSOR_MAP_SWIZZLE_NONE);
         if (st != W4V_OK) return st;
