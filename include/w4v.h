@@ -23,8 +23,11 @@
  *     row length given.  Device pointers must be 16-byte aligned.
  *   - The caller owns every buffer, including the workspace; no entry point
  *     allocates device memory.  A workspace must be zero-filled once before
- *     its first use; every call that returns W4V_OK leaves it zero-filled
- *     again, so it can be reused by the next call on the same stream.
+ *     its first use; every call that returns W4V_OK leaves the parts that
+ *     must start at zero (arrival counters, best-key slots) at zero again,
+ *     so it can be reused by the next call on the same stream (scratch
+ *     parts such as fp32 partial tiles keep whatever the last call wrote and
+ *     are always written before they are read).
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream).
  *     Argument, shape and alignment errors are returned before anything is
  *     launched.  A launch failure returns W4V_ERR_CUDA.  A kernel that gives
@@ -112,10 +115,10 @@ w4v_status w4v_unpack_int4(const void *packed_host, int N, int K, uint8_t *q_hos
  * Sizes: M >= 0 (M == 0 is a no-op), N % 8 == 0, K % 128 == 0.
  * Workspace: w4a16_workspace_bytes(M, N, K) bytes, zero-filled before first
  * use: fp32 partial sums of output tiles whose k range is split between
- * CTAs, and one arrival counter per tile.  About 1 MB for M <= 32; for
- * M > 32, 256 KB per 128 x 256 output tile when there are at most 1024
- * tiles (the kernel may then split tiles in two k halves), plus 4 bytes per
- * tile. */
+ * CTAs, and one arrival counter per tile.  About 1 MB for M <= 16 and 2 MB
+ * for M <= 32; for M > 32, the larger of the 32-row size and 256 KB per
+ * 128 x 256 output tile when there are at most 1024 tiles (the prefill
+ * kernel may then split tiles in two k halves), plus 4 bytes per tile. */
 size_t w4a16_workspace_bytes(int M, int N, int K);
 w4v_status w4a16_gemm(const uint16_t *A, const void *Bq, const uint16_t *scales,
                       const uint8_t *zeros, int group, uint16_t *C, int M, int N, int K,
@@ -128,13 +131,84 @@ w4v_status w4a16_gemm(const uint16_t *A, const void *Bq, const uint16_t *scales,
  *     loads and dequantizes its first weight stages while the previous
  *     kernel of the stream is still finishing; A is still read, and C and
  *     the workspace still written, only after that kernel has completed.
- *     Without the flag the weights are only prefetched into L2 early.
- * Unknown flag bits: W4V_ERR_ARG.  The pages have no counterpart: it is a
- * scheduling promise of the caller, the result is the same either way. */
+ *     Without the flag the weights are only prefetched into L2 early.  The
+ *     pages have no counterpart: it is a scheduling promise of the caller,
+ *     the result is the same either way.
+ *   W4V_BATCH_INVARIANT: for M > 32, run the rows in blocks of 32 through
+ *     the verify-sized kernel (one launch per block, the weights read once
+ *     per block) instead of the prefill kernel, so that every row of C is
+ *     bit for bit the row a call with that row alone would give.  Greedy
+ *     speculative decoding then emits exactly the tokens of plain greedy
+ *     decoding also when several sequences' verify blocks share one call
+ *     ("Efficient LLM Challenge Results", section 3: verification leaves the
+ *     output unchanged whatever the drafts).  No effect for M <= 32, which
+ *     is batch-invariant anyway.
+ * Unknown flag bits: W4V_ERR_ARG. */
 #define W4V_STATIC_WEIGHTS 1u
+#define W4V_BATCH_INVARIANT 2u
 w4v_status w4a16_gemm_ex(const uint16_t *A, const void *Bq, const uint16_t *scales,
                          const uint8_t *zeros, int group, uint16_t *C, int M, int N, int K,
                          void *workspace, size_t workspace_bytes, unsigned flags, w4v_stream_t stream);
+
+/* ----------------------------------------------------- w4a16_gemm_grouped
+ * Several independent W4A16 products C_i = A_i * W_i^T (each exactly as
+ * w4a16_gemm defines it) in one launch.  Decode and verify read every weight
+ * from HBM once per step ("Efficient LLM Challenge Results", section 2
+ * "Where the time goes"), and a decoder layer's projections are a few MB
+ * each: one launch per projection pays a start-up and a drain of the weight
+ * stream that are comparable to its transfer time.  A grouped launch streams
+ * the weights of every problem through one pipeline, with one start-up.
+ * All problems share M (1..32, the verify-sized kernel), the group size and
+ * whether they carry zero points.  Each output element is computed by the
+ * same arithmetic for every M in 1..32 (batch invariance), but a grouped
+ * launch splits the k ranges differently from a one-problem launch, so its
+ * results may differ from w4a16_gemm in the last fp32 bits before the fp16
+ * rounding; both are within the same error bound of the exact product.
+ *
+ * Use: w4a16_grouped_plan once for a fixed set of buffers (it encodes the
+ * problems into `plan`, device memory of w4a16_grouped_plan_bytes(n) bytes,
+ * 64-byte aligned, and fills the host handle), then w4a16_gemm_grouped per
+ * step.  The plan holds the buffers' addresses: it stays valid while they
+ * do, and must be rebuilt if any of them moves.
+ *   problems[i].A       device, fp16 [M][K_i]
+ *   problems[i].Bq      device, packed int4 of q_i [N_i][K_i] (w4v_pack_int4)
+ *   problems[i].scales  device, fp16 [K_i/G][N_i]
+ *   problems[i].zeros   device, uint8 [K_i/G][N_i] or NULL (all NULL or none;
+ *                       with zero points N_i % 16 == 0)
+ *   problems[i].C       device, fp16 [M][N_i] (written, never read)
+ * Sizes: 1 <= n_problems <= 4096, 1 <= M <= 32, G = 128 or 32,
+ * N_i % 8 == 0, K_i % 128 == 0, N_i, K_i > 0.
+ * w4a16_grouped_plan copies the table to the device and waits for the copy
+ * (it synchronizes `stream`), so it must not be called while `stream` is
+ * being captured into a graph (W4V_ERR_ARG); w4a16_gemm_grouped only
+ * launches and may be captured.  A handle not written by w4a16_grouped_plan,
+ * or changed since, is refused with W4V_ERR_ARG.
+ * Workspace: w4a16_grouped_workspace_bytes(handle) bytes, zero-filled before
+ * first use (fp32 partial tiles and one arrival counter per output tile).
+ * Flags: W4V_STATIC_WEIGHTS as for w4a16_gemm_ex. */
+typedef struct {
+    const uint16_t *A;
+    const void *Bq;
+    const uint16_t *scales;
+    const uint8_t *zeros;
+    uint16_t *C;
+    int N, K;
+} w4a16_problem;
+
+/* Filled by w4a16_grouped_plan; read-only for the caller. */
+typedef struct {
+    const void *plan;       /* the device table this handle describes */
+    long long units;        /* work units of one launch */
+    int n_problems, M, group, has_zeros, tiles;
+    unsigned check;         /* consistency tag */
+} w4a16_grouped_t;
+
+size_t w4a16_grouped_plan_bytes(int n_problems);
+w4v_status w4a16_grouped_plan(const w4a16_problem *problems, int n_problems, int M, int group, void *plan,
+                              size_t plan_bytes, w4a16_grouped_t *handle, w4v_stream_t stream);
+size_t w4a16_grouped_workspace_bytes(const w4a16_grouped_t *handle);
+w4v_status w4a16_gemm_grouped(const w4a16_grouped_t *handle, void *workspace, size_t workspace_bytes,
+                              unsigned flags, w4v_stream_t stream);
 
 /* ------------------------------------------------------- w8_lmhead_argmax
  * Greedy token per row: argmax_out[r] = argmax_v scale[v] * sum_k X[r][k]*W[v][k],

@@ -1,5 +1,6 @@
 // api.cpp -- the C ABI: argument validation (before anything touches the
 // GPU), workspace sizing, the host int4 packer, and dispatch to launchers.
+#include <algorithm>
 #include <cstring>
 
 #include "runtime.h"
@@ -91,7 +92,10 @@ w4v_status w4v_unpack_int4(const void *packed, int N, int K, uint8_t *q) {
 
 size_t w4a16_workspace_bytes(int M, int N, int K) {
     if (M < 0 || !pack_shape_ok(N, K)) return 0;
-    if (M > w4v::kDecodeMaxRows) return w4v::w4a16_prefill_ws_bytes(M, N, K);
+    // M > 32: enough for the prefill kernel and for the 32-row blocks of
+    // the batch-invariant path, whichever the call takes
+    if (M > w4v::kDecodeMaxRows)
+        return std::max(w4v::w4a16_prefill_ws_bytes(M, N, K), w4v::w4a16_decode_ws_bytes(w4v::kDecodeMaxRows, N, K));
     return w4v::w4a16_decode_ws_bytes(M, N, K);
 }
 
@@ -103,7 +107,7 @@ w4v_status w4a16_gemm(const uint16_t *A, const void *Bq, const uint16_t *scales,
 w4v_status w4a16_gemm_ex(const uint16_t *A, const void *Bq, const uint16_t *scales, const uint8_t *zeros,
                          int group, uint16_t *C, int M, int N, int K, void *ws, size_t ws_bytes, unsigned flags,
                          w4v_stream_t stream) {
-    if ((flags & ~unsigned(W4V_STATIC_WEIGHTS)) != 0u) return W4V_ERR_ARG;
+    if ((flags & ~unsigned(W4V_STATIC_WEIGHTS | W4V_BATCH_INVARIANT)) != 0u) return W4V_ERR_ARG;
     if (M < 0 || N <= 0 || K <= 0) return W4V_ERR_SHAPE;
     if (group != kGroup && group != 32) return W4V_ERR_SHAPE;
     if (K % kGroup != 0 || N % 8 != 0) return W4V_ERR_SHAPE;
@@ -115,11 +119,75 @@ w4v_status w4a16_gemm_ex(const uint16_t *A, const void *Bq, const uint16_t *scal
         return W4V_ERR_ALIGN;
     if (ws == nullptr || ws_bytes < w4a16_workspace_bytes(M, N, K)) return W4V_ERR_WORKSPACE;
     if (!w4v::aligned16(ws)) return W4V_ERR_ALIGN;
+    const bool static_w = (flags & W4V_STATIC_WEIGHTS) != 0u;
+    if (M > w4v::kDecodeMaxRows && (flags & W4V_BATCH_INVARIANT) != 0u) {
+        // Blocks of 32 rows through the verify-sized kernel, in order on the
+        // stream (each leaves the workspace zeroed for the next): every row
+        // gets the arithmetic it gets in a call of 1..32 rows.
+        for (int m0 = 0; m0 < M; m0 += w4v::kDecodeMaxRows) {
+            const int mb = std::min(w4v::kDecodeMaxRows, M - m0);
+            const w4v_status st = w4v::launch_w4a16_decode(A + size_t(m0) * K, Bq, scales, zeros, group,
+                                                           C + size_t(m0) * N, mb, N, K, ws, static_w,
+                                                           reinterpret_cast<cudaStream_t>(stream));
+            if (st != W4V_OK) return st;
+        }
+        return W4V_OK;
+    }
     if (M > w4v::kDecodeMaxRows)
         return w4v::launch_w4a16_prefill(A, Bq, scales, zeros, group, C, M, N, K, ws,
                                          reinterpret_cast<cudaStream_t>(stream));
-    return w4v::launch_w4a16_decode(A, Bq, scales, zeros, group, C, M, N, K, ws, (flags & W4V_STATIC_WEIGHTS) != 0u,
+    return w4v::launch_w4a16_decode(A, Bq, scales, zeros, group, C, M, N, K, ws, static_w,
                                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t w4a16_grouped_plan_bytes(int n_problems) {
+    if (n_problems < 1 || n_problems > w4v::kGroupedMaxProblems) return 0;
+    return w4v::w4a16_grouped_table_bytes(n_problems);
+}
+
+w4v_status w4a16_grouped_plan(const w4a16_problem *problems, int n, int M, int group, void *plan,
+                              size_t plan_bytes, w4a16_grouped_t *handle, w4v_stream_t stream) {
+    if (n < 1 || n > w4v::kGroupedMaxProblems || M < 1 || M > w4v::kDecodeMaxRows) return W4V_ERR_SHAPE;
+    if (group != kGroup && group != 32) return W4V_ERR_SHAPE;
+    if (problems == nullptr || plan == nullptr || handle == nullptr) return W4V_ERR_ARG;
+    const bool zeros = problems[0].zeros != nullptr;
+    for (int i = 0; i < n; ++i) {
+        const w4a16_problem &q = problems[i];
+        if (q.N <= 0 || q.K <= 0 || q.K % kGroup != 0 || q.N % 8 != 0) return W4V_ERR_SHAPE;
+        if (zeros && q.N % 16 != 0) return W4V_ERR_SHAPE;
+        if ((q.zeros != nullptr) != zeros) return W4V_ERR_ARG;
+        if (q.A == nullptr || q.Bq == nullptr || q.scales == nullptr || q.C == nullptr) return W4V_ERR_ARG;
+        if (!w4v::aligned16(q.A) || !w4v::aligned16(q.Bq) || !w4v::aligned16(q.scales) ||
+            (q.zeros != nullptr && !w4v::aligned16(q.zeros)) || !w4v::aligned16(q.C))
+            return W4V_ERR_ALIGN;
+    }
+    if (plan_bytes < w4v::w4a16_grouped_table_bytes(n)) return W4V_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(plan) & 63u) return W4V_ERR_ALIGN;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return W4V_ERR_CUDA;
+    }
+    if (cap != cudaStreamCaptureStatusNone) return W4V_ERR_ARG;
+    const w4v::DeviceInfo *info = nullptr;
+    w4v_status st = w4v::device_info(&info);
+    if (st != W4V_OK) return st;
+    return w4v::build_w4a16_grouped(problems, n, M, group, plan, handle, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t w4a16_grouped_workspace_bytes(const w4a16_grouped_t *handle) {
+    if (handle == nullptr || !w4v::w4a16_grouped_handle_ok(*handle)) return 0;
+    return w4v::w4a16_grouped_ws_bytes(*handle);
+}
+
+w4v_status w4a16_gemm_grouped(const w4a16_grouped_t *handle, void *ws, size_t ws_bytes, unsigned flags,
+                              w4v_stream_t stream) {
+    if ((flags & ~unsigned(W4V_STATIC_WEIGHTS)) != 0u) return W4V_ERR_ARG;
+    if (handle == nullptr || !w4v::w4a16_grouped_handle_ok(*handle)) return W4V_ERR_ARG;
+    if (ws == nullptr || ws_bytes < w4v::w4a16_grouped_ws_bytes(*handle)) return W4V_ERR_WORKSPACE;
+    if (!w4v::aligned16(ws)) return W4V_ERR_ALIGN;
+    return w4v::launch_w4a16_grouped(*handle, ws, (flags & W4V_STATIC_WEIGHTS) != 0u,
+                                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t w8_lmhead_argmax_workspace_bytes(int M, int V) {

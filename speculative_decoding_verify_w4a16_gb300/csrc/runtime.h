@@ -93,6 +93,14 @@ w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t
                                const uint8_t *zeros, int group, uint16_t *C, int M, int N, int K,
                                void *ws, bool static_weights, cudaStream_t stream);
 size_t w4a16_decode_ws_bytes(int M, int N, int K);
+// Grouped launch of the verify-sized kernel (arguments validated by the caller).
+size_t w4a16_grouped_table_bytes(int n_problems);
+w4v_status build_w4a16_grouped(const w4a16_problem *probs, int n, int M, int group, void *plan,
+                               w4a16_grouped_t *handle, cudaStream_t stream);
+bool w4a16_grouped_handle_ok(const w4a16_grouped_t &handle);
+size_t w4a16_grouped_ws_bytes(const w4a16_grouped_t &handle);
+w4v_status launch_w4a16_grouped(const w4a16_grouped_t &handle, void *ws, bool static_weights, cudaStream_t stream);
+constexpr int kGroupedMaxProblems = 4096;
 size_t w4a16_prefill_ws_bytes(int M, int N, int K);
 w4v_status launch_w4a16_prefill(const uint16_t *A, const void *Bq, const uint16_t *scales, const uint8_t *zeros,
                                 int group, uint16_t *C, int M, int N, int K, void *ws, cudaStream_t stream);

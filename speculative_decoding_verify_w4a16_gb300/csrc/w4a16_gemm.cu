@@ -73,7 +73,9 @@
 //     dequantized into tensor memory, before the dependency wait; only the
 //     activation copies and the output wait for the previous kernel.  Each
 //     stage therefore has separate weight and activation barriers.
+#include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "runtime.h"
 #define W4V_COMPACT_WAITS 1
@@ -162,7 +164,22 @@ struct Layout {
     static_assert(kPart * 4 <= kStage, "partial tile fits a stage");
 };
 
+// One problem of a grouped launch (w4a16_gemm_grouped): the tensor maps and
+// sizes every role needs, read from a device table written by the host.
+// Problem i owns the global units [u0, u0 + n_tiles * n_pairs) and the
+// global output tiles [tile0, tile0 + n_tiles).
+struct GroupProb {   // 64-byte aligned, as its first member
+    CUtensorMap xmap, smap, zmap;   // activations, scales, zero points (as for one problem)
+    const uint8_t *wq;
+    __half *C;
+    long long u0;
+    int N, n_groups, n_pairs, n_tiles, tile0, sbox_w, sbox_h, pad;
+};
+static_assert(sizeof(GroupProb) % 64 == 0, "tensor maps in the table stay 64-byte aligned");
+
 struct Args {
+    const GroupProb *probs;   // grouped launch: the problem table (else null)
+    int n_probs;
     const uint8_t *wq;
     const __half *scales;
     const uint8_t *zeros;
@@ -180,11 +197,46 @@ struct Args {
     int sbox_w, sbox_h;               // scale box of one stage: min(128, N) x min(4 or 16, K / group)
 };
 
-// A unit: tile t, pair p (groups 2p and, if it exists, 2p + 1).
+// The sizes of the problem a walker is in: units per tile, groups, tiles.
+struct ProbDims {
+    int nP, G, nT;
+};
+
+// The problem whose unit range holds global unit u (the table is ordered by
+// u0 and starts at 0).
+__device__ __forceinline__ int find_prob(const GroupProb *probs, int n, long long u) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(&probs[mid].u0) <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ ProbDims prob_dims(const GroupProb *g) {
+    return ProbDims{__ldg(&g->n_pairs), __ldg(&g->n_groups), __ldg(&g->n_tiles)};
+}
+
+// A unit: problem pi (grouped launches only, else 0), tile t of that
+// problem, pair p (groups 2p and, if it exists, 2p + 1).
+template <bool kG>
 struct UnitPos {
-    int t, p, nP, G;
-    __device__ UnitPos(long long u, int n_pairs, int n_groups)
-        : t(static_cast<int>(u / n_pairs)), p(static_cast<int>(u % n_pairs)), nP(n_pairs), G(n_groups) {}
+    const GroupProb *probs;
+    int n_probs, pi, t, p, nP, G, nT;
+    __device__ UnitPos(long long u, const Args &a)
+        : probs(a.probs), n_probs(a.n_probs), pi(0), nP(a.n_pairs), G(a.n_groups), nT(a.n_tiles) {
+        if constexpr (kG) {
+            pi = find_prob(probs, n_probs, u);
+            u -= __ldg(&probs[pi].u0);
+            const ProbDims d = prob_dims(probs + pi);
+            nP = d.nP;
+            G = d.G;
+            nT = d.nT;
+        }
+        t = static_cast<int>(u / nP);
+        p = static_cast<int>(u % nP);
+    }
     __device__ int g0() const { return 2 * p; }
     __device__ int ng() const { return min(kUnitGroups, G - 2 * p); }
     __device__ bool tile_last() const { return p == nP - 1; }
@@ -192,15 +244,35 @@ struct UnitPos {
         if (++p == nP) {
             p = 0;
             ++t;
+            if (kG && t == nT && pi + 1 < n_probs) {
+                t = 0;
+                const ProbDims d = prob_dims(probs + ++pi);
+                nP = d.nP;
+                G = d.G;
+                nT = d.nT;
+            }
         }
     }
 };
 
 // Stages: runs of at most kStageUnits consecutive units of one tile.
+template <bool kG>
 struct StageWalk {
-    int t, p, nP, G, left;
-    __device__ StageWalk(long long u, int n_pairs, int n_groups, int units)
-        : t(static_cast<int>(u / n_pairs)), p(static_cast<int>(u % n_pairs)), nP(n_pairs), G(n_groups), left(units) {}
+    const GroupProb *probs;
+    int n_probs, pi, t, p, nP, G, nT, left;
+    __device__ StageWalk(long long u, const Args &a, int units)
+        : probs(a.probs), n_probs(a.n_probs), pi(0), nP(a.n_pairs), G(a.n_groups), nT(a.n_tiles), left(units) {
+        if constexpr (kG) {
+            pi = find_prob(probs, n_probs, u);
+            u -= __ldg(&probs[pi].u0);
+            const ProbDims d = prob_dims(probs + pi);
+            nP = d.nP;
+            G = d.G;
+            nT = d.nT;
+        }
+        t = static_cast<int>(u / nP);
+        p = static_cast<int>(u % nP);
+    }
     __device__ int size() const { return min(min(kStageUnits, nP - p), left); }
     __device__ int gbeg() const { return 2 * p; }
     __device__ int gend(int n) const { return min(2 * (p + n), G); }
@@ -210,6 +282,13 @@ struct StageWalk {
         if (p == nP) {
             p = 0;
             ++t;
+            if (kG && t == nT && left > 0 && pi + 1 < n_probs) {
+                t = 0;
+                const ProbDims d = prob_dims(probs + ++pi);
+                nP = d.nP;
+                G = d.G;
+                nT = d.nT;
+            }
         }
     }
 };
@@ -234,7 +313,11 @@ struct StageRing {
 // sub-group's scale (fp16, one rounding) and the accumulators of a 128-k
 // group are added unscaled; with group size 128 the scale is applied to each
 // group's fp32 sum instead.
-template <int NBLK, bool kFold>
+// kG: grouped launch.  The units of every problem of the table are numbered
+// one after the other and split over the CTAs as one stream-K list; each
+// role follows the problem of the unit it is on (its weights, tensor maps,
+// output), so one pipeline and one ramp serve the whole list.
+template <int NBLK, bool kFold, bool kG>
 __global__ void __launch_bounds__(kThreads, 1)
 w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap,
                     const __grid_constant__ CUtensorMap zmap, const Args p) {
@@ -274,16 +357,18 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
-    const int G = p.n_groups;
-    const int nP = p.n_pairs;
-    const int CL = p.cluster;                 // 0: stream-K
+    // 0: stream-K (a grouped launch is always stream-K); the divisions below
+    // see CL only where it is positive
+    const int CL = kG ? 0 : p.cluster;
+    const int CLd = kG ? 1 : max(p.cluster, 1);
     const int crank = CL > 0 ? static_cast<int>(cluster_ctarank()) : 0;
     long long ub, ue;
     if (CL > 0) {
         // one tile per cluster; member `crank` takes its share of the tile's units
-        const long long t0u = (long long)(cta / CL) * nP;
-        ub = t0u + (long long)crank * nP / CL;
-        ue = t0u + (long long)(crank + 1) * nP / CL;
+        const int nP = p.n_pairs;
+        const long long t0u = (long long)(cta / CLd) * nP;
+        ub = t0u + (long long)crank * nP / CLd;
+        ue = t0u + (long long)(crank + 1) * nP / CLd;
     } else {
         ub = split_begin(cta, p.U, p.P);
         ue = split_begin(cta + 1, p.U, p.P);
@@ -325,46 +410,93 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
     const uint32_t tmem = misc[0];
     grid_dep_launch();
 
+    // What each role needs of the problem it is on (a grouped launch reads
+    // the table; one problem reads the launch arguments).
+    auto pr_wq = [&](int pi) -> const uint8_t * {
+        if constexpr (kG) return p.probs[pi].wq;
+        return p.wq;
+    };
+    auto pr_xmap = [&](int pi) -> const CUtensorMap * {
+        if constexpr (kG) return &p.probs[pi].xmap;
+        return &xmap;
+    };
+    auto pr_smap = [&](int pi) -> const CUtensorMap * {
+        if constexpr (kG) return &p.probs[pi].smap;
+        return &smap;
+    };
+    auto pr_zmap = [&](int pi) -> const CUtensorMap * {
+        if constexpr (kG) return &p.probs[pi].zmap;
+        return &zmap;
+    };
+    auto pr_sbox_w = [&](int pi) -> int {
+        if constexpr (kG) return p.probs[pi].sbox_w;
+        return p.sbox_w;
+    };
+    auto pr_sbox_h = [&](int pi) -> int {
+        if constexpr (kG) return p.probs[pi].sbox_h;
+        return p.sbox_h;
+    };
+    using Walk = StageWalk<kG>;
+    // Tile t of problem pi: its first unit (global numbering), units, rows,
+    // output and index among all tiles of the launch (arrival counters).
+    struct TileRef {
+        long long t0u;
+        int nP, N, T;
+        __half *C;
+    };
+    auto tile_ref = [&](int pi, int t) -> TileRef {
+        if constexpr (kG) {
+            const GroupProb &g = p.probs[pi];
+            const int nPp = g.n_pairs;
+            return TileRef{g.u0 + (long long)t * nPp, nPp, g.N, g.tile0 + t, g.C};
+        }
+        return TileRef{(long long)t * p.n_pairs, p.n_pairs, p.N, t, p.C};
+    };
+
     if (warp == kWarpProd) {
         // ---------------------------------------------------------- producer
         const uint64_t pol_w = l2_policy_evict_first();
         const uint64_t pol_x = l2_policy_evict_last();
         const bool stage_zeros = p.zeros != nullptr;
         // bytes riding on the weight barrier: group 32 scales (and zeros), group 128 zeros
-        const uint32_t meta_bytes = uint32_t(p.sbox_w * p.sbox_h) *
-                                    (kFold ? (stage_zeros ? 3u : 2u) : (stage_zeros ? 1u : 0u));
-        auto load_weights = [&](const StageWalk &w, int n, int s) {
+        auto meta_bytes = [&](int pi) -> uint32_t {
+            return uint32_t(pr_sbox_w(pi) * pr_sbox_h(pi)) *
+                   (kFold ? (stage_zeros ? 3u : 2u) : (stage_zeros ? 1u : 0u));
+        };
+        auto load_weights = [&](const Walk &w, int n, int s) {
             const int g0 = w.gbeg();
             const uint32_t wbytes = (w.gend(n) - g0) * kGroupBytes;
-            mbar_arrive_expect_tx(wfull(s), wbytes + meta_bytes);
-            bulk_load(base_s + s * L::kStage + L::kW, p.wq + (size_t(w.t) * G + g0) * kGroupBytes, wbytes, wfull(s),
-                      pol_w);
+            mbar_arrive_expect_tx(wfull(s), wbytes + meta_bytes(w.pi));
+            bulk_load(base_s + s * L::kStage + L::kW, pr_wq(w.pi) + (size_t(w.t) * w.G + g0) * kGroupBytes, wbytes,
+                      wfull(s), pol_w);
             if (kFold) {
                 // the stage's sub-group scales and zero points ride with its weights
                 // (rows past N or K land as zero)
-                tma_load_2d(base_s + fixed_off + L::kScl + uint32_t(s * kFSclSlotBytes), &smap, w.t * kTileN, 4 * g0,
-                            wfull(s), pol_w);
+                tma_load_2d(base_s + fixed_off + L::kScl + uint32_t(s * kFSclSlotBytes), pr_smap(w.pi), w.t * kTileN,
+                            4 * g0, wfull(s), pol_w);
                 if (stage_zeros)
-                    tma_load_2d(base_s + fixed_off + L::kSst + uint32_t(s * kFZroSlotBytes), &zmap, w.t * kTileN,
-                                4 * g0, wfull(s), pol_w);
+                    tma_load_2d(base_s + fixed_off + L::kSst + uint32_t(s * kFZroSlotBytes), pr_zmap(w.pi),
+                                w.t * kTileN, 4 * g0, wfull(s), pol_w);
             } else if (stage_zeros) {
-                tma_load_2d(base_s + fixed_off + L::kZro + uint32_t(s * kZroSlotBytes), &zmap, w.t * kTileN, g0,
-                            wfull(s), pol_w);
+                tma_load_2d(base_s + fixed_off + L::kZro + uint32_t(s * kZroSlotBytes), pr_zmap(w.pi), w.t * kTileN,
+                            g0, wfull(s), pol_w);
             }
         };
         // stage use u's scales into slot u % kSclSlots (rows past N or K land as zero)
-        auto load_scales = [&](const StageWalk &w, int u) {
+        auto load_scales = [&](const Walk &w, int u) {
             if (kFold) return;
             const int b = u % kSclSlots;
-            mbar_arrive_expect_tx(sfull(b), uint32_t(p.sbox_w * p.sbox_h * 2));
-            tma_load_2d(sst + uint32_t(b * kSclSlotBytes), &smap, w.t * kTileN, w.gbeg(), sfull(b), pol_w);
+            mbar_arrive_expect_tx(sfull(b), uint32_t(pr_sbox_w(w.pi) * pr_sbox_h(w.pi) * 2));
+            tma_load_2d(sst + uint32_t(b * kSclSlotBytes), pr_smap(w.pi), w.t * kTileN, w.gbeg(), sfull(b), pol_w);
         };
         int w_early = 0;                         // stages whose weights went out before the wait
         if (lane == 0) {
-            prefetch_tensormap(&xmap);
-            prefetch_tensormap(&smap);
-            if (p.zeros != nullptr) prefetch_tensormap(&zmap);
-            StageWalk pw(ub, nP, G, nunits);
+            if constexpr (!kG) {
+                prefetch_tensormap(&xmap);
+                prefetch_tensormap(&smap);
+                if (p.zeros != nullptr) prefetch_tensormap(&zmap);
+            }
+            Walk pw(ub, p, nunits);
             for (int st = 0; st < S && pw.left > 0; ++st) {
                 const int n = pw.size();
                 if (p.static_w) {
@@ -375,13 +507,13 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                     // Only L2 is warmed before the dependency wait: L2 is the
                     // point of coherence, so this stays correct even if the
                     // previous kernel writes the weights.
-                    prefetch_l2(p.wq + (size_t(pw.t) * G + pw.gbeg()) * kGroupBytes,
+                    prefetch_l2(pr_wq(pw.pi) + (size_t(pw.t) * pw.G + pw.gbeg()) * kGroupBytes,
                                 (pw.gend(n) - pw.gbeg()) * kGroupBytes);
                 }
                 pw.next(n);
             }
         }
-        StageWalk sw(ub, nP, G, nunits);
+        Walk sw(ub, p, nunits);
         int issued = 0;
         grid_dep_wait();
         if (lane == 0) {
@@ -399,7 +531,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                     load_scales(sw, issued);
                 }
                 mbar_arrive_expect_tx(xfull(s), L::kAct);
-                tma_load_3d(base_s + s * L::kStage, &xmap, 0, 0, 2 * sw.gbeg(), xfull(s), pol_x);
+                tma_load_3d(base_s + s * L::kStage, pr_xmap(sw.pi), 0, 0, 2 * sw.gbeg(), xfull(s), pol_x);
                 ++issued;
                 sw.next(n);
             }
@@ -426,7 +558,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
             const int me = warp - kWarpIss0;
             constexpr uint32_t idesc = idesc_f16_f32(128, 16 * NBLK);
             constexpr int kSetPeriod = DS * kIssuers;       // units between uses of one dempty barrier
-            StageWalk sw(ub, nP, G, nunits);
+            Walk sw(ub, p, nunits);
             int f0 = 0;                          // first unit of the stage
             StageRing rg(S);
             for (; sw.left > 0; rg.next()) {
@@ -435,7 +567,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                 const int jj = (me - f0 % kIssuers + kIssuers) % kIssuers;   // my unit in the stage, if any
                 if (jj < n) {
                     const int f = f0 + jj;
-                    const int ng = min(kUnitGroups, G - 2 * (sw.p + jj));
+                    const int ng = min(kUnitGroups, sw.G - 2 * (sw.p + jj));
                     const int slot = f % kASlots;
                     const int set = f % DS;
                     // afull before xfull: the unit's weights were dequantized, so
@@ -489,15 +621,16 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         // Zero points (group 128): row g of the stage's slot, for this lane's
         // row of the tile (rows past N read as 0 and are never stored).
         const bool has_zeros = p.zeros != nullptr;
-        auto zero_read = [&](int s, int gs) -> uint32_t {
-            return lds_u8(base_s + fixed_off + L::kZro + uint32_t(s * kZroSlotBytes) + uint32_t(gs * p.sbox_w + r));
+        // (sbw: the stage's scale and zero box width, min(128, N))
+        auto zero_read = [&](int s, int gs, int sbw) -> uint32_t {
+            return lds_u8(base_s + fixed_off + L::kZro + uint32_t(s * kZroSlotBytes) + uint32_t(gs * sbw + r));
         };
 
         // Group size 32: the four sub-groups' zero points (bytes of zz) and
         // scales (halves of ss0, ss1) of 128-k group gs of the stage in slot s,
         // for this lane's row.
-        auto fold_read = [&](int s, int gs, uint32_t &zz, uint32_t &ss0, uint32_t &ss1) {
-            const uint32_t sp = uint32_t(p.sbox_w * 2), zp = uint32_t(p.sbox_w);
+        auto fold_read = [&](int s, int gs, int sbw, uint32_t &zz, uint32_t &ss0, uint32_t &ss1) {
+            const uint32_t sp = uint32_t(sbw * 2), zp = uint32_t(sbw);
             const uint32_t e = base_s + fixed_off + L::kScl + uint32_t(s * kFSclSlotBytes) + uint32_t(4 * gs) * sp +
                                uint32_t(2 * r);
             ss0 = uint32_t(lds_u16(e)) | (uint32_t(lds_u16(e + sp)) << 16);
@@ -569,7 +702,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
             if (lane == 0) mbar_arrive(empty(s));
         };
 
-        StageWalk sw(ub, nP, G, nunits);
+        Walk sw(ub, p, nunits);
         int f0 = 0;
         uint32_t ra[32], rb[32];
         StageRing rg(S);
@@ -583,8 +716,9 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                 release(s);
             } else {
                 const int f = f0 + jj;
-                const int ng = min(kUnitGroups, G - 2 * (sw.p + jj));
+                const int ng = min(kUnitGroups, sw.G - 2 * (sw.p + jj));
                 const int slot = f % kASlots;
+                const int sbw = (has_zeros || kFold) ? pr_sbox_w(sw.pi) : 0;
                 const uint32_t g0p = base_s + s * L::kStage + L::kW + (kUnitGroups * jj) * kGroupBytes;
                 const uint32_t g1p = g0p + kGroupBytes;
                 const uint32_t col = tmem + lane_base + slot * kASlotCols;
@@ -595,10 +729,10 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
 #pragma unroll 1
                 for (int gg = 0; gg < ng; ++gg) {
                     const uint32_t gp = gg == 0 ? g0p : g1p;
-                    const uint32_t z = (!kFold && has_zeros) ? zero_read(s, kUnitGroups * jj + gg) : 8u;
+                    const uint32_t z = (!kFold && has_zeros) ? zero_read(s, kUnitGroups * jj + gg, sbw) : 8u;
                     uint32_t zz = 0u, ss0 = 0u, ss1 = 0u;
                     if constexpr (kFold) {
-                        fold_read(s, kUnitGroups * jj + gg, zz, ss0, ss1);
+                        fold_read(s, kUnitGroups * jj + gg, sbw, zz, ss0, ss1);
                         dequant_fold(gp, 0, zz, ss0, ss1, ra);
                     } else {
                         dequant(gp, 0, z, ra);
@@ -660,7 +794,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         // The unit's group scales come from the stage scale ring (rows past
         // N read as 0 and are never stored): dw walks the stages as the
         // producer does, du is the stage use, dj the unit within the stage.
-        StageWalk dw(ub, nP, G, nunits);
+        Walk dw(ub, p, nunits);
         int du = 0, dj = 0;
         const uint32_t srow = uint32_t(2 * r);
         if (p.static_w) grid_dep_wait();     // before any write of C or the workspace
@@ -668,9 +802,10 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         // Tile finished by this CTA alone: write C.  Otherwise publish the fp32
         // partial tile and count this CTA in; whether it arrived last is read
         // back after the CTA's last unit (see fixup).
-        auto flush = [&](int t) -> bool {
-            const long long t0u = (long long)t * nP;
-            const long long t1u = t0u + nP;
+        auto flush = [&](int pi, int t) -> bool {
+            const TileRef tr = tile_ref(pi, t);
+            const long long t0u = tr.t0u;
+            const long long t1u = t0u + tr.nP;
             const int n = t * kTileN + r;
             if (CL > 1) {
                 // cluster: partial tile [row][16 NBLK] into this CTA's first
@@ -685,13 +820,13 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                 return true;
             }
             if (ub <= t0u && t1u <= ue) {
-                if (n < p.N) {
+                if (n < tr.N) {
 #pragma unroll
                     for (int b = 0; b < NBLK; ++b)
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int m = 16 * b + j;
-                            if (m < p.M) p.C[size_t(m) * p.N + n] = __float2half_rn(acc[b][j]);
+                            if (m < p.M) tr.C[size_t(m) * tr.N + n] = __float2half_rn(acc[b][j]);
                         }
                 }
                 return true;
@@ -709,7 +844,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
             if (!drain_sync()) return false;
             if (dr == 0 && lane == 0) {
                 misc[2 + slot] = uint32_t(t) + 1u;
-                pend_prev[slot] = atom_add_acq_rel_gpu(&p.tile_cnt[t], 1u);
+                misc[6 + slot] = uint32_t(pi);
+                pend_prev[slot] = atom_add_acq_rel_gpu(&p.tile_cnt[tr.T], 1u);
             }
             return true;
         };
@@ -723,18 +859,18 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                     const uint32_t tp = misc[2 + sl];
                     uint32_t last = 0u;
                     if (tp != 0u) {
-                        const long long t0u = (long long)(tp - 1u) * nP;
-                        const int cf = split_owner(t0u, p.U, p.P);
-                        const int cl = split_owner(t0u + nP - 1, p.U, p.P);
+                        const TileRef tr = tile_ref(int(misc[6 + sl]), int(tp - 1u));
+                        const int cf = split_owner(tr.t0u, p.U, p.P);
+                        const int cl = split_owner(tr.t0u + tr.nP - 1, p.U, p.P);
                         last = pend_prev[sl] == uint32_t(cl - cf) ? 1u : 0u;
-                        if (last) p.tile_cnt[tp - 1u] = 0u;
+                        if (last) p.tile_cnt[tr.T] = 0u;
                     }
                     misc[4 + sl] = last;
                 }
             }
         };
 
-        UnitPos wd(ub, nP, G);
+        UnitPos<kG> wd(ub, p);
         bool ok = true;
         for (int f = 0; f < nunits && ok; ++f) {
             const int set = f % DS;
@@ -781,7 +917,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                 // once per stage (on an abort the values are never stored)
                 if (dj == 0) warp_wait(sfull(b), uint32_t(du / kSclSlots) & 1u, ab);
                 const uint32_t row0 = sst + uint32_t(b * kSclSlotBytes) + srow;
-                const uint32_t pitch = uint32_t(p.sbox_w * 2);
+                const uint32_t pitch = uint32_t(pr_sbox_w(wd.pi) * 2);
                 s0 = __half2float(__ushort_as_half(lds_u16(row0 + uint32_t(2 * dj) * pitch)));
                 if (ng > 1) s1 = __half2float(__ushort_as_half(lds_u16(row0 + uint32_t(2 * dj + 1) * pitch)));
             }
@@ -804,11 +940,11 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                 ++du;
                 dj = 0;
             }
-            const int t = wd.t;
+            const int t = wd.t, tpi = wd.pi;
             const bool tile_end = wd.tile_last();
             wd.next();
             if (tile_end || f == nunits - 1) {
-                if (!flush(t)) {
+                if (!flush(tpi, t)) {
                     ok = false;
                     break;
                 }
@@ -822,13 +958,13 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
     }
 
     __syncthreads();
-    if (CL > 1) {
+    if (!kG && CL > 1) {
         // -------------------- cluster reduction: each CTA finishes 1/CL of the rows
         cluster_sync_all();                       // every CTA's partial is in its shared memory
         if (*ab.flag == 0u) {
             grid_dep_wait();                      // every thread that writes C waits itself
-            const int t = cta / CL;
-            const int r0 = crank * kTileN / CL, r1 = (crank + 1) * kTileN / CL;
+            const int t = cta / CLd;
+            const int r0 = crank * kTileN / CLd, r1 = (crank + 1) * kTileN / CLd;
             const int nrows = r1 - r0;
             for (int item = threadIdx.x; item < nrows * 4 * NBLK; item += kThreads) {
                 const int m4 = item / nrows, row = r0 + item % nrows;   // consecutive threads: consecutive rows
@@ -870,9 +1006,10 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         for (int sl = 0; sl < 2; ++sl) {
             if (!misc[4 + sl]) continue;
             const int t = int(misc[2 + sl]) - 1;
-            const long long t0u = (long long)t * nP;
+            const TileRef tr = tile_ref(int(misc[6 + sl]), t);
+            const long long t0u = tr.t0u;
             const int cf = split_owner(t0u, p.U, p.P);
-            const int cl = split_owner(t0u + nP - 1, p.U, p.P);
+            const int cl = split_owner(t0u + tr.nP - 1, p.U, p.P);
             for (int e4 = threadIdx.x; e4 < kPart / 4; e4 += kThreads) {   // float4 of the [m][128] tile
                 const int m = e4 / (kTileN / 4);
                 const int n0 = t * kTileN + 4 * (e4 % (kTileN / 4));
@@ -900,13 +1037,13 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                             sum.w += v[u].w;
                         }
                 }
-                if (n0 < p.N) {
+                if (n0 < tr.N) {
                     const __half2 lo = __floats2half2_rn(sum.x, sum.y);
                     const __half2 hi = __floats2half2_rn(sum.z, sum.w);
                     uint2 packed;
                     packed.x = h2_as_u32(lo);
                     packed.y = h2_as_u32(hi);
-                    *reinterpret_cast<uint2 *>(p.C + size_t(m) * p.N + n0) = packed;
+                    *reinterpret_cast<uint2 *>(tr.C + size_t(m) * tr.N + n0) = packed;
                 }
             }
         }
@@ -952,7 +1089,7 @@ int pick_cluster(int n_tiles, int n_pairs, int sm_count) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int fit = 0;
-        if (cudaOccupancyMaxActiveClusters(&fit, w4a16_decode_kernel<2, false>, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&fit, w4a16_decode_kernel<2, false, false>, &cfg) != cudaSuccess) {
             cudaGetLastError();
             continue;
         }
@@ -961,13 +1098,13 @@ int pick_cluster(int n_tiles, int n_pairs, int sm_count) {
     return 0;
 }
 
-template <int NBLK, bool kFold>
+template <int NBLK, bool kFold, bool kG = false>
 w4v_status configure() {
     static int configured_for = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_for != dev) {
-        if (cudaFuncSetAttribute(w4a16_decode_kernel<NBLK, kFold>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(w4a16_decode_kernel<NBLK, kFold, kG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kMaxSmem) != cudaSuccess) {
             cudaGetLastError();
             return W4V_ERR_CUDA;
@@ -977,18 +1114,18 @@ w4v_status configure() {
     return W4V_OK;
 }
 
-template <int NBLK, bool kFold>
+template <int NBLK, bool kFold, bool kG = false>
 w4v_status launch(const CUtensorMap &xmap, const CUtensorMap &smap, const CUtensorMap &zmap, Args &a, int cluster,
                   cudaStream_t stream) {
     using L = Layout<NBLK>;
-    w4v_status st = configure<NBLK, kFold>();
+    w4v_status st = configure<NBLK, kFold, kG>();
     if (st != W4V_OK) return st;
     a.cluster = cluster;
     a.stages = L::kStagesMax;
     if (cluster > 0) a.P = a.n_tiles * cluster;
     const size_t smem = size_t(L::bytes(a.stages));
-    if (launch_pdl_cluster(w4a16_decode_kernel<NBLK, kFold>, dim3(a.P), dim3(kThreads), smem, stream, cluster, xmap,
-                           smap, zmap, a) !=
+    if (launch_pdl_cluster(w4a16_decode_kernel<NBLK, kFold, kG>, dim3(a.P), dim3(kThreads), smem, stream, cluster,
+                           xmap, smap, zmap, a) !=
         cudaSuccess) {
         cudaGetLastError();
         return W4V_ERR_CUDA;
@@ -1032,6 +1169,8 @@ w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t
     if (st != W4V_OK) return st;
     const int nblk = (M + 15) / 16;
     Args a;
+    a.probs = nullptr;
+    a.n_probs = 0;
     a.wq = static_cast<const uint8_t *>(Bq);
     a.scales = reinterpret_cast<const __half *>(scales);
     a.zeros = zeros;
@@ -1073,6 +1212,125 @@ w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t
                          : launch<2, true>(xmap, smap, zmap, a, cluster, stream);
     return nblk == 1 ? launch<1, false>(xmap, smap, zmap, a, cluster, stream)
                      : launch<2, false>(xmap, smap, zmap, a, cluster, stream);
+}
+
+// ---------------------------------------------------------------- grouped launch
+namespace {
+
+// FNV-1a over the handle fields a launch relies on, so that a handle not
+// written by w4a16_grouped_plan (or changed since) is refused.
+uint32_t handle_tag(const w4a16_grouped_t &h) {
+    uint32_t x = 2166136261u;
+    auto mix = [&](uint64_t v) {
+        for (int i = 0; i < 8; ++i) {
+            x ^= uint32_t(v >> (8 * i)) & 0xFFu;
+            x *= 16777619u;
+        }
+    };
+    mix(reinterpret_cast<uintptr_t>(h.plan));
+    mix(uint64_t(h.units));
+    mix(uint64_t(uint32_t(h.n_problems)));
+    mix(uint64_t(uint32_t(h.M)));
+    mix(uint64_t(uint32_t(h.group)));
+    mix(uint64_t(uint32_t(h.has_zeros)));
+    mix(uint64_t(uint32_t(h.tiles)));
+    return x ^ 0x57344750u;
+}
+
+}  // namespace
+
+size_t w4a16_grouped_table_bytes(int n_problems) { return size_t(n_problems) * sizeof(GroupProb); }
+
+w4v_status build_w4a16_grouped(const w4a16_problem *probs, int n, int M, int group, void *plan,
+                               w4a16_grouped_t *h, cudaStream_t stream) {
+    const int nblk = (M + 15) / 16;
+    std::vector<GroupProb> table(static_cast<size_t>(n));
+    long long u0 = 0;
+    int tile0 = 0;
+    for (int i = 0; i < n; ++i) {
+        const w4a16_problem &q = probs[i];
+        GroupProb &g = table[size_t(i)];
+        std::memset(&g, 0, sizeof(g));
+        w4v_status st = encode_tmap_kblocks(&g.xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, q.A, uint64_t(q.K),
+                                            uint64_t(M), 64, 16 * nblk, 2 * kStageGroups, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != W4V_OK) return st;
+        g.sbox_w = std::min(kTileN, q.N);
+        g.sbox_h = std::min(kStageGroups * (kGroup / group), q.K / group);
+        st = encode_tmap_2d(&g.smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, q.scales, uint64_t(q.N), uint64_t(q.K / group),
+                            uint64_t(q.N) * 2, uint32_t(g.sbox_w), uint32_t(g.sbox_h), CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st != W4V_OK) return st;
+        if (q.zeros != nullptr) {
+            st = encode_tmap_2d(&g.zmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, q.zeros, uint64_t(q.N), uint64_t(q.K / group),
+                                uint64_t(q.N), uint32_t(g.sbox_w), uint32_t(g.sbox_h), CU_TENSOR_MAP_SWIZZLE_NONE);
+            if (st != W4V_OK) return st;
+        }
+        g.wq = static_cast<const uint8_t *>(q.Bq);
+        g.C = reinterpret_cast<__half *>(q.C);
+        g.N = q.N;
+        g.n_groups = q.K / kGroup;
+        g.n_pairs = (g.n_groups + kUnitGroups - 1) / kUnitGroups;
+        g.n_tiles = (q.N + kTileN - 1) / kTileN;
+        g.u0 = u0;
+        g.tile0 = tile0;
+        u0 += (long long)g.n_tiles * g.n_pairs;
+        tile0 += g.n_tiles;
+    }
+    // The table goes to the device once, synchronously: the handle then
+    // describes device memory that no later host change can affect.
+    if (cudaMemcpyAsync(plan, table.data(), table.size() * sizeof(GroupProb), cudaMemcpyHostToDevice, stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return W4V_ERR_CUDA;
+    }
+    h->plan = plan;
+    h->units = u0;
+    h->n_problems = n;
+    h->M = M;
+    h->group = group;
+    h->has_zeros = probs[0].zeros != nullptr ? 1 : 0;
+    h->tiles = tile0;
+    h->check = handle_tag(*h);
+    return W4V_OK;
+}
+
+bool w4a16_grouped_handle_ok(const w4a16_grouped_t &h) {
+    return h.plan != nullptr && h.check == handle_tag(h) && h.n_problems >= 1 && h.M >= 1 &&
+           h.M <= kDecodeMaxRows && (h.group == 128 || h.group == 32) && h.units >= 1 && h.tiles >= 1;
+}
+
+size_t w4a16_grouped_ws_bytes(const w4a16_grouped_t &h) {
+    const int nblk = (h.M + 15) / 16;
+    const size_t part = size_t(kMaxCtas) * 2 * 16 * nblk * kTileN * sizeof(float);
+    return part + ((size_t(h.tiles) * sizeof(uint32_t) + 255) & ~size_t(255));
+}
+
+w4v_status launch_w4a16_grouped(const w4a16_grouped_t &h, void *ws, bool static_weights, cudaStream_t stream) {
+    const DeviceInfo *info = nullptr;
+    w4v_status st = device_info(&info);
+    if (st != W4V_OK) return st;
+    const int nblk = (h.M + 15) / 16;
+    Args a;
+    std::memset(&a, 0, sizeof(a));
+    a.probs = static_cast<const GroupProb *>(h.plan);
+    a.n_probs = h.n_problems;
+    // only tested against null inside the kernel: whether the problems carry zero points
+    a.zeros = h.has_zeros ? static_cast<const uint8_t *>(h.plan) : nullptr;
+    a.M = h.M;
+    a.U = h.units;
+    a.P = static_cast<int>(std::min<long long>(std::min(info->sm_count, kMaxCtas), a.U));
+    a.partial = static_cast<float *>(ws);
+    a.tile_cnt = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) +
+                                              size_t(kMaxCtas) * 2 * 16 * nblk * kTileN * sizeof(float));
+    a.status = info->status;
+    a.static_w = static_weights ? 1 : 0;
+    CUtensorMap unused;
+    std::memset(&unused, 0, sizeof(unused));
+    if (h.group == 32)
+        return nblk == 1 ? launch<1, true, true>(unused, unused, unused, a, 0, stream)
+                         : launch<2, true, true>(unused, unused, unused, a, 0, stream);
+    return nblk == 1 ? launch<1, false, true>(unused, unused, unused, a, 0, stream)
+                     : launch<2, false, true>(unused, unused, unused, a, 0, stream);
 }
 
 }  // namespace w4v

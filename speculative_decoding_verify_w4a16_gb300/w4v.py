@@ -26,6 +26,19 @@ _lock = threading.Lock()
 _lib = None
 
 
+class Problem(ctypes.Structure):
+    """w4a16_problem (include/w4v.h)."""
+    _fields_ = [("A", ctypes.c_void_p), ("Bq", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("zeros", ctypes.c_void_p), ("C", ctypes.c_void_p), ("N", ctypes.c_int), ("K", ctypes.c_int)]
+
+
+class GroupedHandle(ctypes.Structure):
+    """w4a16_grouped_t (include/w4v.h): filled by w4a16_grouped_plan."""
+    _fields_ = [("plan", ctypes.c_void_p), ("units", ctypes.c_longlong), ("n_problems", ctypes.c_int),
+                ("M", ctypes.c_int), ("group", ctypes.c_int), ("has_zeros", ctypes.c_int), ("tiles", ctypes.c_int),
+                ("check", ctypes.c_uint)]
+
+
 class W4VError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
@@ -58,6 +71,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.w4a16_gemm.restype = I
             lib.w4a16_gemm_ex.argtypes = [P, P, P, P, I, P, I, I, I, P, S, ctypes.c_uint, P]
             lib.w4a16_gemm_ex.restype = I
+            lib.w4a16_grouped_plan_bytes.argtypes = [I]
+            lib.w4a16_grouped_plan_bytes.restype = S
+            lib.w4a16_grouped_plan.argtypes = [P, I, I, I, P, S, P, P]
+            lib.w4a16_grouped_plan.restype = I
+            lib.w4a16_grouped_workspace_bytes.argtypes = [P]
+            lib.w4a16_grouped_workspace_bytes.restype = S
+            lib.w4a16_gemm_grouped.argtypes = [P, P, S, ctypes.c_uint, P]
+            lib.w4a16_gemm_grouped.restype = I
             lib.w8_lmhead_argmax_workspace_bytes.argtypes = [I, I]
             lib.w8_lmhead_argmax_workspace_bytes.restype = S
             lib.w8_lmhead_argmax.argtypes = [P, P, P, I, I, I, P, P, P, P, S, P]
@@ -159,24 +180,62 @@ def workspace(nbytes: int, device="cuda"):
 
 # ------------------------------------------------------------------ compute --
 STATIC_WEIGHTS = 1
+BATCH_INVARIANT = 2
 
 
 def w4a16_gemm(A, Bq, scales, N: int, zeros=None, out=None, ws=None, stream=None, static_weights=False,
-               group: int = GROUP):
+               group: int = GROUP, batch_invariant=False):
     """C = A @ deq(Bq, scales, zeros)^T on the GPU.  A fp16 [M][K] cuda, Bq packed uint8 cuda,
     scales fp16 [K/group][N] (group 128 or 32).
     static_weights: the caller promises no GPU work still in flight writes Bq, scales or zeros
-    (w4a16_gemm_ex with W4V_STATIC_WEIGHTS)."""
+    (w4a16_gemm_ex with W4V_STATIC_WEIGHTS).
+    batch_invariant: for M > 32, 32-row blocks through the verify-sized kernel
+    (W4V_BATCH_INVARIANT): each row equals the row computed alone."""
     import torch
     M, K = A.shape
     if out is None:
         out = torch.empty((M, N), dtype=torch.float16, device=A.device)
     if ws is None:
         ws = workspace(w4a16_workspace_bytes(M, N, K), A.device)
+    flags = (STATIC_WEIGHTS if static_weights else 0) | (BATCH_INVARIANT if batch_invariant else 0)
     code = load().w4a16_gemm_ex(_ptr(A), _ptr(Bq), _ptr(scales), _ptr(zeros), int(group), _ptr(out), M, N, K,
-                                _ptr(ws), ws.numel(), STATIC_WEIGHTS if static_weights else 0, _stream(stream))
+                                _ptr(ws), ws.numel(), flags, _stream(stream))
     _check(code, "w4a16_gemm")
     return out
+
+
+class GroupedGemm:
+    """Several independent W4A16 products in one launch (w4a16_grouped_plan +
+    w4a16_gemm_grouped).  `problems` is a list of (A, Bq, scales, zeros, C)
+    device tensors (zeros None or a uint8 table for every problem), all with
+    the same number of rows M; the plan keeps them alive and refers to their
+    addresses, so call it again with the same tensors (refill them in place)."""
+
+    def __init__(self, problems, group: int = GROUP, stream=None):
+        import torch
+        lib = load()
+        self.problems = list(problems)
+        n = len(self.problems)
+        M = self.problems[0][0].shape[0]
+        dev = self.problems[0][0].device
+        arr = (Problem * n)()
+        for i, (A, Bq, sc, z, C) in enumerate(self.problems):
+            arr[i] = Problem(_ptr(A), _ptr(Bq), _ptr(sc), _ptr(z), _ptr(C), int(C.shape[1]), int(A.shape[1]))
+        nbytes = lib.w4a16_grouped_plan_bytes(n)
+        # torch's allocations start on 512-byte boundaries (the plan needs 64)
+        self.plan = torch.empty(max(int(nbytes), 64), dtype=torch.uint8, device=dev)
+        self.handle = GroupedHandle()
+        code = lib.w4a16_grouped_plan(arr, n, int(M), int(group), _ptr(self.plan), self.plan.numel(),
+                                      ctypes.byref(self.handle), _stream(stream))
+        _check(code, "w4a16_grouped_plan")
+        self.ws = workspace(lib.w4a16_grouped_workspace_bytes(ctypes.byref(self.handle)), dev)
+
+    def __call__(self, stream=None, static_weights: bool = False, ws=None):
+        ws = self.ws if ws is None else ws
+        code = load().w4a16_gemm_grouped(ctypes.byref(self.handle), _ptr(ws), ws.numel(),
+                                         STATIC_WEIGHTS if static_weights else 0, _stream(stream))
+        _check(code, "w4a16_gemm_grouped")
+        return [p[4] for p in self.problems]
 
 
 def w8_lmhead_argmax(X, W, scale, out=None, maxlogit=None, logits=None, ws=None, stream=None):

@@ -93,7 +93,10 @@ def test_argument_validation_before_launch(w4v_mod):
     assert lib.w4a16_gemm(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 512, 256, None, 1 << 30, None) == w4v_mod.ERR_WORKSPACE
     assert lib.w4a16_gemm(None, None, None, None, 128, None, 0, 512, 256, None, 0, None) == w4v_mod.OK   # M == 0
     # w4a16_gemm_ex: the same checks plus unknown flag bits
-    assert lib.w4a16_gemm_ex(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 512, 256, FAKE, 1 << 30, 2, None) == w4v_mod.ERR_ARG
+    assert lib.w4a16_gemm_ex(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 512, 256, FAKE, 1 << 30, 4, None) == w4v_mod.ERR_ARG
+    # the batch-invariant path for M > 32 needs the 32-row workspace as well
+    assert w4v_mod.w4a16_workspace_bytes(128, 2560, 2560) >= w4v_mod.w4a16_workspace_bytes(32, 2560, 2560)
+    assert lib.w4a16_gemm_ex(FAKE, FAKE, FAKE, None, 128, FAKE, 128, 512, 256, FAKE, 1 << 20, 3, None) == w4v_mod.ERR_WORKSPACE
     assert lib.w4a16_gemm_ex(FAKE, FAKE, FAKE, None, 128, FAKE, 16, 500, 256, FAKE, 1 << 30, 1, None) == w4v_mod.ERR_SHAPE
     assert lib.w4a16_gemm_ex(None, None, None, None, 128, None, 0, 512, 256, None, 0, 1, None) == w4v_mod.OK
     # w8_lmhead_argmax
@@ -168,6 +171,57 @@ def test_argument_validation_before_launch(w4v_mod):
     assert lib.w4v_pack_int4(None, 128, 128, FAKE) == w4v_mod.ERR_ARG
     buf = ctypes.create_string_buffer(16)
     assert lib.w4v_pack_int4(ctypes.addressof(buf), 100, 128, ctypes.addressof(buf)) == w4v_mod.ERR_SHAPE
+
+
+def test_grouped_argument_validation_before_launch(w4v_mod):
+    """w4a16_grouped_plan / w4a16_gemm_grouped reject bad arguments before any
+    device work: sizes, null or misaligned pointers, mixed zero tables, a
+    small or misaligned plan, unknown flags and handles not written by the
+    planner."""
+    lib = w4v_mod.load()
+    Pr = w4v_mod.Problem
+
+    def probs(*specs):
+        arr = (Pr * len(specs))()
+        for i, (A, Bq, sc, z, C, N, K) in enumerate(specs):
+            arr[i] = Pr(A, Bq, sc, z, C, N, K)
+        return arr
+
+    F = FAKE
+    good = (F, F, F, None, F, 512, 256)
+    big = 1 << 30
+    h = w4v_mod.GroupedHandle()
+    plan = lib.w4a16_grouped_plan
+    hb = ctypes.byref(h)
+    assert lib.w4a16_grouped_plan_bytes(0) == 0
+    assert lib.w4a16_grouped_plan_bytes(4097) == 0
+    assert lib.w4a16_grouped_plan_bytes(4) >= 4 * 3 * 128
+    assert plan(probs(good), 0, 16, 128, F, big, hb, None) == w4v_mod.ERR_SHAPE          # no problem
+    assert plan(probs(good), 4097, 16, 128, F, big, hb, None) == w4v_mod.ERR_SHAPE
+    assert plan(probs(good), 1, 0, 128, F, big, hb, None) == w4v_mod.ERR_SHAPE           # M = 0
+    assert plan(probs(good), 1, 33, 128, F, big, hb, None) == w4v_mod.ERR_SHAPE          # M > 32
+    assert plan(probs(good), 1, 16, 64, F, big, hb, None) == w4v_mod.ERR_SHAPE           # group
+    assert plan(None, 1, 16, 128, F, big, hb, None) == w4v_mod.ERR_ARG
+    assert plan(probs(good), 1, 16, 128, None, big, hb, None) == w4v_mod.ERR_ARG
+    assert plan(probs(good), 1, 16, 128, F, big, None, None) == w4v_mod.ERR_ARG
+    assert plan(probs((F, F, F, None, F, 500, 256)), 1, 16, 128, F, big, hb, None) == w4v_mod.ERR_SHAPE
+    assert plan(probs((F, F, F, None, F, 512, 200)), 1, 16, 128, F, big, hb, None) == w4v_mod.ERR_SHAPE
+    assert plan(probs((F, F, F, F, F, 512, 256), (F, F, F, F, F, 520, 256)), 2, 16, 128, F, big, hb,
+                None) == w4v_mod.ERR_SHAPE                                                    # zeros: N % 16
+    assert plan(probs(good, (F, F, F, F, F, 512, 256)), 2, 16, 128, F, big, hb, None) == w4v_mod.ERR_ARG
+    assert plan(probs(good, (F, F, None, None, F, 512, 256)), 2, 16, 128, F, big, hb, None) == w4v_mod.ERR_ARG
+    assert plan(probs(good, (F, F + 8, F, None, F, 512, 256)), 2, 16, 128, F, big, hb, None) == w4v_mod.ERR_ALIGN
+    assert plan(probs(good, (F, F, F, None, F + 2, 512, 256)), 2, 16, 128, F, big, hb, None) == w4v_mod.ERR_ALIGN
+    assert plan(probs(good), 1, 16, 128, F, 16, hb, None) == w4v_mod.ERR_WORKSPACE      # plan too small
+    assert plan(probs(good), 1, 16, 128, F + 16, big, hb, None) == w4v_mod.ERR_ALIGN    # plan not 64-aligned
+    # a handle the planner did not write (or changed since) is refused
+    assert lib.w4a16_grouped_workspace_bytes(hb) == 0
+    assert lib.w4a16_grouped_workspace_bytes(None) == 0
+    assert lib.w4a16_gemm_grouped(hb, F, big, 0, None) == w4v_mod.ERR_ARG
+    assert lib.w4a16_gemm_grouped(None, F, big, 0, None) == w4v_mod.ERR_ARG
+    h.plan, h.units, h.n_problems, h.M, h.group, h.tiles = F, 10, 1, 16, 128, 1
+    assert lib.w4a16_gemm_grouped(hb, F, big, 0, None) == w4v_mod.ERR_ARG
+    assert lib.w4a16_gemm_grouped(hb, F, big, 2, None) == w4v_mod.ERR_ARG             # unknown flag
 
 
 def test_split_owner_matches_even_split():

@@ -42,10 +42,13 @@ def test_shapes(w4v_mod, gpu, oracle_mod, M, N, K):
     assert gemm_rel_err(C, oracle_mod.w4a16_gemm(A, q, s)) <= GEMM_TOL
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 512, 512), (3, 272, 640), (24, 400, 3200)])
+@pytest.mark.parametrize("M,N,K", [(16, 512, 512), (3, 272, 640), (24, 400, 3200), (16, 16, 128), (5, 48, 256),
+                                   (1, 112, 384), (21, 48, 384)])
 def test_zero_points(w4v_mod, gpu, oracle_mod, M, N, K):
     """Per-(group, row) zero points, including odd group counts (a unit
-    with a single group at each tile end) and a partial last tile."""
+    with a single group at each tile end), a partial last tile, a zero-table
+    box narrower than a tile (N < 128) and shorter than a stage (K of one to
+    three groups)."""
     A = inputs.activations(3, M, K)
     q = inputs.w4_codes(3, N, K)
     s = inputs.w4_scales(3, N, K)
@@ -114,20 +117,25 @@ def test_workspace_reuse_is_clean(w4v_mod, gpu):
     assert w4v_mod.get_status() == 0
 
 
+@pytest.mark.parametrize("zeros", [False, True], ids=["sym", "zeros"])
+@pytest.mark.parametrize("M", [16, 21, 32])
 @pytest.mark.parametrize("proj", inputs.LAYER_PROJS, ids=lambda p: p.name)
-def test_layer_projection_sampled(w4v_mod, gpu, oracle_mod, proj):
-    """The 4B-shaped projections at M = 16 (the verify block of K = 15 drafts):
-    4000 sampled outputs plus two full output rows against the oracle."""
-    M = 16
+def test_layer_projection_sampled(w4v_mod, gpu, oracle_mod, proj, M, zeros):
+    """The 4B-shaped projections at the verify sizes of K = 15 drafts (M = 16),
+    of the runner-up's constant K = 20 (M = 21) and at 32 rows, each with and
+    without a zero table (gate_up takes the stream-K split, the others the
+    cluster split): 4000 sampled outputs plus two full output rows against
+    the oracle."""
     A = inputs.activations(1, M, proj.K, 0, proj.name)
     q, s = inputs.layer_weights(1, 0, proj)
-    C = _gpu_gemm(w4v_mod, gpu, A, q, s)
-    r = np.random.default_rng(1)
+    z = inputs.w4_zeros(1, proj.N, proj.K, proj.name) if zeros else None
+    C = _gpu_gemm(w4v_mod, gpu, A, q, s, zeros=z)
+    r = np.random.default_rng(M)
     rows = r.integers(0, M, 4000).astype(np.int32)
     cols = r.integers(0, proj.N, 4000).astype(np.int32)
     rows = np.concatenate([rows, np.zeros(proj.N, np.int32), np.full(proj.N, M - 1, np.int32)])
     cols = np.concatenate([cols, np.arange(proj.N, dtype=np.int32), np.arange(proj.N, dtype=np.int32)])
-    R = oracle_mod.w4a16_gemm_sampled(A, q, s, rows, cols)
+    R = oracle_mod.w4a16_gemm_sampled(A, q, s, rows, cols, zeros=z)
     assert gemm_rel_err(C[rows, cols], R) <= GEMM_TOL
 
 
@@ -224,3 +232,35 @@ def test_back_to_back_layer_launches_clean_and_deterministic(w4v_mod, gpu, M):
     assert w4v_mod.get_status() == 0
     for r, C in zip(ref, outs):
         assert torch.equal(r, C)
+
+
+@pytest.mark.parametrize("zeros", [False, True], ids=["sym", "zeros"])
+def test_batch_invariant_blocks(w4v_mod, gpu, oracle_mod, zeros):
+    """W4V_BATCH_INVARIANT: 8 sequences x 16 verify positions (128 rows) in
+    one call give each sequence's rows bit for bit what that sequence's own
+    16-row call gives (and each row what a 1-row call gives), so a batched
+    verify never changes an accepted token; sampled outputs meet the oracle
+    bound.  Without the flag 128 rows take the prefill kernel, whose
+    rounding differs."""
+    N, K = 2560, 2560
+    A = inputs.activations(81, 128, K, "binv")
+    q = inputs.w4_codes(81, N, K, "binv")
+    s = inputs.w4_scales(81, N, K, "binv")
+    z = inputs.w4_zeros(81, N, K, "binv") if zeros else None
+    packed = to_dev(w4v_mod.pack_int4(q), gpu)
+    sd = to_dev(s, gpu)
+    zd = None if z is None else to_dev(z, gpu)
+    Ad = to_dev(A, gpu)
+    C128 = w4v_mod.w4a16_gemm(Ad, packed, sd, N, zeros=zd, batch_invariant=True).cpu().numpy()
+    for b in range(8):
+        C16 = w4v_mod.w4a16_gemm(Ad[16 * b:16 * b + 16].contiguous(), packed, sd, N, zeros=zd).cpu().numpy()
+        assert np.array_equal(C16, C128[16 * b:16 * b + 16]), b
+    for m in (0, 45, 127):
+        C1 = w4v_mod.w4a16_gemm(Ad[m:m + 1].contiguous(), packed, sd, N, zeros=zd).cpu().numpy()
+        assert np.array_equal(C1[0], C128[m]), m
+    r = np.random.default_rng(81)
+    rows = r.integers(0, 128, 3000).astype(np.int32)
+    cols = r.integers(0, N, 3000).astype(np.int32)
+    R = oracle_mod.w4a16_gemm_sampled(A, q, s, rows, cols, zeros=z)
+    assert gemm_rel_err(C128.astype(np.float64)[rows, cols], R) <= GEMM_TOL
+    assert w4v_mod.get_status() == 0

@@ -60,6 +60,23 @@ def test_zero_points(w4v_mod, gpu, oracle_mod, M, N, K):
     assert gemm_rel_err(C, oracle_mod.w4a16_gemm(A, q, s, zeros=z, group=G)) <= GEMM_TOL
 
 
+@pytest.mark.parametrize("M", [16, 21])
+def test_zero_points_stream_k(w4v_mod, gpu, oracle_mod, M):
+    """The gate_up shape (19456 x 2560, the stream-K split, where a CTA's
+    range starts and ends inside tiles) with a group-32 zero table: sampled
+    outputs and two full rows against the oracle."""
+    N, K = 19456, 2560
+    A, q, s, z = _case(13, M, N, K, True, "g32zk")
+    C = _gemm(w4v_mod, gpu, A, q, s, zeros=z)
+    r = np.random.default_rng(M + 32)
+    rows = r.integers(0, M, 4000).astype(np.int32)
+    cols = r.integers(0, N, 4000).astype(np.int32)
+    rows = np.concatenate([rows, np.zeros(N, np.int32), np.full(N, M - 1, np.int32)])
+    cols = np.concatenate([cols, np.arange(N, dtype=np.int32), np.arange(N, dtype=np.int32)])
+    R = oracle_mod.w4a16_gemm_sampled(A, q, s, rows, cols, zeros=z, group=G)
+    assert gemm_rel_err(C[rows, cols], R) <= GEMM_TOL
+
+
 @pytest.mark.parametrize("M,N,K", [(33, 512, 256), (128, 2560, 2560), (200, 520, 640), (300, 384, 9728)])
 def test_prefill_sizes(w4v_mod, gpu, oracle_mod, M, N, K):
     A, q, s, _ = _case(M, M, N, K, False, "g32p")
