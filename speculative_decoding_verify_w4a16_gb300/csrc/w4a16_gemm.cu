@@ -140,10 +140,10 @@ struct Layout {
     static constexpr int kStage = kW + kStageGroups * kGroupBytes;
     static constexpr uint32_t kDUnit = kUnitGroups * 16 * NBLK;   // accumulator columns per unit
     static constexpr int kDSets = int((kTmemCols - kDcol0) / kDUnit);
-    // wfull, xfull, empty per stage (room for kMaxStages); afull per A slot, aempty
-    // per A slot and dequant parity;
+    // wfull, xfull, empty per stage (room for kMaxStages); afull per A slot
+    // and group, aempty per A slot and dequant parity;
     // dfull, dempty per set; done; drain sync; sfull, sempty per scale slot
-    static constexpr int kNumBars = 3 * kMaxStages + 3 * kASlots + (1 + kIssuers) * kDSets + 2 + 2 * kSclSlots;
+    static constexpr int kNumBars = 3 * kMaxStages + 4 * kASlots + (1 + kIssuers) * kDSets + 2 + 2 * kSclSlots;
     static constexpr int kBarBytes = (8 * kNumBars + 127) & ~127;
     static constexpr int kScl = kBarBytes;                         // offsets inside the fixed block
     static constexpr int kZro = kScl + kDrWarps * kRing * 64;      // group-32 scale slots from kScl
@@ -335,18 +335,20 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
     auto wfull = [&](int s) { return bar0 + 8u * s; };          // stage's weights landed
     auto xfull = [&](int s) { return bar0 + 8u * (MS + s); };   // stage's activations landed
     auto empty = [&](int s) { return bar0 + 8u * (2 * MS + s); };
-    auto afull = [&](int a) { return bar0 + 8u * (3 * MS + a); };
+    // group g of the unit in A slot a dequantized (the slot's issuer starts
+    // on group 0 while group 1 is still being dequantized)
+    auto afull = [&](int a, int g) { return bar0 + 8u * (3 * MS + 2 * a + g); };
     // A slot a freed for the dequant warps of parity par: unit u's MMAs release
     // slot u % 3 to its next user u + 3, of parity (u + 1) % 2.  Each waiter
     // so sees every phase of its barrier in turn (one barrier per slot would
     // let a parity skip a phase).
-    auto aempty = [&](int a, int par) { return bar0 + 8u * (3 * MS + kASlots + 2 * a + par); };
-    auto dfull = [&](int b) { return bar0 + 8u * (3 * MS + 3 * kASlots + b); };
+    auto aempty = [&](int a, int par) { return bar0 + 8u * (3 * MS + 2 * kASlots + 2 * a + par); };
+    auto dfull = [&](int b) { return bar0 + 8u * (3 * MS + 4 * kASlots + b); };
     // accumulator set b freed for issuer i: the drain of unit u releases set
     // u % DS to its next user u + DS, issued by (u + DS) % 3, so each issuer
     // sees every phase of its own barriers
-    auto dempty = [&](int b, int i) { return bar0 + 8u * (3 * MS + 3 * kASlots + DS + b * kIssuers + i); };
-    const uint32_t done_bar = bar0 + 8u * (3 * MS + 3 * kASlots + (1 + kIssuers) * DS);
+    auto dempty = [&](int b, int i) { return bar0 + 8u * (3 * MS + 4 * kASlots + DS + b * kIssuers + i); };
+    const uint32_t done_bar = bar0 + 8u * (3 * MS + 4 * kASlots + (1 + kIssuers) * DS);
     const uint32_t drain_bar = done_bar + 8u;
     auto sfull = [&](int b) { return drain_bar + 8u * (1 + b); };               // a stage's scales landed
     auto sempty = [&](int b) { return drain_bar + 8u * (1 + kSclSlots + b); };  // the drain has read them
@@ -383,7 +385,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
             mbar_init(empty(s), kDqWarps + kStageUnits);   // dequant warps + one per unit's issuer
         }
         for (int a = 0; a < kASlots; ++a) {
-            mbar_init(afull(a), kDqWarps / 2);     // the four quarter warps of the unit's parity
+            mbar_init(afull(a, 0), kDqWarps / 2);  // the four quarter warps of the unit's parity
+            mbar_init(afull(a, 1), kDqWarps / 2);
             mbar_init(aempty(a, 0), 1);            // the unit's issuer
             mbar_init(aempty(a, 1), 1);
         }
@@ -575,15 +578,26 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                     // xfull names this use (an issuer skips the stages it has no
                     // unit in).  The free accumulator set is waited for first
                     // with four sets (M <= 16), last with two (measured).
+                    // (every unit arrives on both group barriers of its slot, a
+                    // unit with one group without data on the second)
                     const bool set_ok = f < DS || NBLK != 1 ||
                                         warp_wait(dempty(set, me), uint32_t((f - DS) / kSetPeriod) & 1u, ab);
-                    if (!set_ok || !warp_wait(afull(slot), (f / kASlots) & 1, ab) || !warp_wait(xfull(s), rg.ph, ab) ||
+                    if (!set_ok || !warp_wait(afull(slot, 0), (f / kASlots) & 1, ab) ||
+                        !warp_wait(xfull(s), rg.ph, ab) ||
                         (NBLK != 1 && f >= DS &&
                          !warp_wait(dempty(set, me), uint32_t((f - DS) / kSetPeriod) & 1u, ab)))
                         break;
                     tc_fence_after();
                     const uint32_t dset = tmem + kDcol0 + set * L::kDUnit;
+                    bool gok = true;
                     for (int gg = 0; gg < ng; ++gg) {
+                        if (gg > 0) {
+                            if (!warp_wait(afull(slot, gg), (f / kASlots) & 1, ab)) {
+                                gok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
                         const uint32_t act = base_s + s * L::kStage + 2 * (kUnitGroups * jj + gg) * L::kActBox;
 #pragma unroll
                         for (int j = 0; j < kGroup / 16; ++j) {
@@ -593,6 +607,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                                              sdesc_sw128(baddr), idesc, j > 0 ? 1u : 0u);
                         }
                     }
+                    if (!gok) break;
+                    if (ng == 1 && !warp_wait(afull(slot, 1), (f / kASlots) & 1, ab)) break;
                     mma_commit_lane0(aempty(slot, (f + 1) & 1));
                     mma_commit_lane0(dfull(set));
                     // one release of the stage per unit (a one-unit stage counts twice)
@@ -744,9 +760,6 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                             break;
                         }
                         tc_fence_after();
-                    } else {
-                        tc_wait_st();
-                        tc_keep_alive<32>(rb);
                     }
                     tmem_st_32x32b_x32(col + 64 * gg, ra);
                     if constexpr (kFold)
@@ -754,19 +767,22 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                     else
                         dequant(gp, 1, z, rb);
                     if (gg == ng - 1) release(s);     // last shared-memory read of the stage
+                    tmem_st_32x32b_x32(col + 64 * gg + 32, rb);
+                    // the group is in tensor memory: the slot's issuer may start on
+                    // it while the next group is being dequantized
                     tc_wait_st();
                     tc_keep_alive<32>(ra);
-                    tmem_st_32x32b_x32(col + 64 * gg + 32, rb);
+                    tc_keep_alive<32>(rb);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(afull(slot, gg));
                 }
                 if (aborted) {
                     release(s);
                     break;
                 }
-                tc_wait_st();
-                tc_keep_alive<32>(rb);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(afull(slot));
+                // a unit with one group still completes its group-1 barrier
+                if (ng == 1 && lane == 0) mbar_arrive(afull(slot, 1));
             }
             f0 += n;
             sw.next(n);
