@@ -561,62 +561,66 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
             const int me = warp - kWarpIss0;
             constexpr uint32_t idesc = idesc_f16_f32(128, 16 * NBLK);
             constexpr int kSetPeriod = DS * kIssuers;       // units between uses of one dempty barrier
+            const int slot = me;                            // unit f uses A slot f % 3
+            // The issuer visits its own units f = me, me + 3, ... only (never two
+            // in one stage): the stage walker is advanced to the unit's stage.
             Walk sw(ub, p, nunits);
-            int f0 = 0;                          // first unit of the stage
+            int f0 = 0, n = sw.size();
             StageRing rg(S);
-            for (; sw.left > 0; rg.next()) {
-                const int n = sw.size();
-                const int s = rg.s;
-                const int jj = (me - f0 % kIssuers + kIssuers) % kIssuers;   // my unit in the stage, if any
-                if (jj < n) {
-                    const int f = f0 + jj;
-                    const int ng = min(kUnitGroups, sw.G - 2 * (sw.p + jj));
-                    const int slot = f % kASlots;
-                    const int set = f % DS;
-                    // afull before xfull: the unit's weights were dequantized, so
-                    // this stage's previous use is complete and the parity of
-                    // xfull names this use (an issuer skips the stages it has no
-                    // unit in).  The free accumulator set is waited for first
-                    // with four sets (M <= 16), last with two (measured).
-                    // (every unit arrives on both group barriers of its slot, a
-                    // unit with one group without data on the second)
-                    const bool set_ok = f < DS || NBLK != 1 ||
-                                        warp_wait(dempty(set, me), uint32_t((f - DS) / kSetPeriod) & 1u, ab);
-                    if (!set_ok || !warp_wait(afull(slot, 0), (f / kASlots) & 1, ab) ||
-                        !warp_wait(xfull(s), rg.ph, ab) ||
-                        (NBLK != 1 && f >= DS &&
-                         !warp_wait(dempty(set, me), uint32_t((f - DS) / kSetPeriod) & 1u, ab)))
-                        break;
-                    tc_fence_after();
-                    const uint32_t dset = tmem + kDcol0 + set * L::kDUnit;
-                    bool gok = true;
-                    for (int gg = 0; gg < ng; ++gg) {
-                        if (gg > 0) {
-                            if (!warp_wait(afull(slot, gg), (f / kASlots) & 1, ab)) {
-                                gok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                        }
-                        const uint32_t act = base_s + s * L::kStage + 2 * (kUnitGroups * jj + gg) * L::kActBox;
-#pragma unroll
-                        for (int j = 0; j < kGroup / 16; ++j) {
-                            // all 16 NBLK activation rows in one MMA (N = 16 NBLK)
-                            const uint32_t baddr = act + (j >> 2) * L::kActBox + (j & 3) * 32;
-                            mma_f16_ts_lane0(dset + gg * NBLK * 16, tmem + slot * kASlotCols + gg * 64 + 8 * j,
-                                             sdesc_sw128(baddr), idesc, j > 0 ? 1u : 0u);
-                        }
-                    }
-                    if (!gok) break;
-                    if (ng == 1 && !warp_wait(afull(slot, 1), (f / kASlots) & 1, ab)) break;
-                    mma_commit_lane0(aempty(slot, (f + 1) & 1));
-                    mma_commit_lane0(dfull(set));
-                    // one release of the stage per unit (a one-unit stage counts twice)
-                    mma_commit_lane0(empty(s));
-                    if (n == 1) mma_commit_lane0(empty(s));
+            int set = me % DS;
+            for (int f = me; f < nunits; f += kIssuers) {
+                while (f >= f0 + n) {
+                    f0 += n;
+                    sw.next(n);
+                    rg.next();
+                    n = sw.size();
                 }
-                f0 += n;
-                sw.next(n);
+                const int jj = f - f0;
+                const int s = rg.s;
+                const int ng = min(kUnitGroups, sw.G - 2 * (sw.p + jj));
+                const uint32_t apar = uint32_t(f / kASlots) & 1u;
+                const uint32_t dpar = uint32_t((f - DS) / kSetPeriod) & 1u;
+                // afull before xfull: the unit's weights were dequantized, so
+                // this stage's previous use is complete and the parity of xfull
+                // names this use (an issuer skips the stages it has no unit
+                // in).  The free accumulator set is waited for first with four
+                // sets (M <= 16), last with two (measured).  Every unit arrives
+                // on both group barriers of its slot (a unit with one group
+                // without data on the second).
+                const bool set_ok = f < DS || NBLK != 1 || warp_wait(dempty(set, me), dpar, ab);
+                if (!set_ok || !warp_wait(afull(slot, 0), apar, ab) || !warp_wait(xfull(s), rg.ph, ab) ||
+                    (NBLK != 1 && f >= DS && !warp_wait(dempty(set, me), dpar, ab)))
+                    break;
+                tc_fence_after();
+                const uint32_t dset = tmem + kDcol0 + set * L::kDUnit;
+                const uint32_t act = base_s + s * L::kStage + 2 * (kUnitGroups * jj) * L::kActBox;
+                bool gok = true;
+                for (int gg = 0; gg < ng; ++gg) {
+                    if (gg > 0) {
+                        if (!warp_wait(afull(slot, gg), apar, ab)) {
+                            gok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    const uint64_t desc0 = sdesc_sw128(act + 2 * gg * L::kActBox);
+#pragma unroll
+                    for (int j = 0; j < kGroup / 16; ++j) {
+                        // all 16 NBLK activation rows in one MMA (N = 16 NBLK); the
+                        // descriptor's start address field is in 16-byte units
+                        const uint64_t desc = desc0 + uint64_t(((j >> 2) * L::kActBox + (j & 3) * 32) >> 4);
+                        mma_f16_ts_lane0(dset + gg * NBLK * 16, tmem + slot * kASlotCols + gg * 64 + 8 * j, desc,
+                                         idesc, j > 0 ? 1u : 0u);
+                    }
+                }
+                if (!gok) break;
+                if (ng == 1 && !warp_wait(afull(slot, 1), apar, ab)) break;
+                mma_commit_lane0(aempty(slot, (f + 1) & 1));
+                mma_commit_lane0(dfull(set));
+                // one release of the stage per unit (a one-unit stage counts twice)
+                mma_commit_lane0(empty(s));
+                if (n == 1) mma_commit_lane0(empty(s));
+                set = (set + kIssuers) % DS;     // DS may be smaller than the stride
             }
             // Every MMA of this issuer has finished once this arrives.
             mma_commit_lane0(done_bar);
