@@ -1,24 +1,30 @@
 #!/usr/bin/env python3
-"""Verify-step benchmark: W4A16 layer set + int8 lm_head argmax + acceptance.
+"""Verify-step benchmark: the W4A16 projection GEMM of the verify block.
 
-Workload (the 4B-shaped verify step at M = 16, i.e. K = 15 drafts + 1): the
-four W4A16 g128 projections of one decoder layer set (qkv 2560->7680,
-o 2560->2560, gate_up 2560->19456, down 9728->2560), the int8 lm_head
-2560->151936 with fused greedy argmax, and longest-prefix acceptance of 15
-seeded drafts (run by the lm_head's last CTA, in the same launch).  One step
-= all of it once, captured as one CUDA graph.
+Workload (config 1: the 4B-shaped verify step at M = 16, i.e. K = 15 drafts
++ 1): the four W4A16 g128 projections of one decoder layer set (qkv
+2560->7680, o 2560->2560, gate_up 2560->19456, down 9728->2560) in one
+grouped launch, each step on the weights of another of 36 layers drawn on
+the device (1.87 GB, far above L2).
 
-value      = algorithmic input bytes per step (packed int4 + fp16 group
-             scales + fp16 activations, int8 lm_head + row scales + its
-             activations) / device time per step, in GB/s, summed over ranks.
-e2e        = the same through the public API with host buffers: pinned host
-             -> device copies of the step's activations and drafts, the
-             kernels, and the device -> host read of the accepted tokens.
-roofline   = the dominant kernel (the lm_head at M = 16), its duration timed
-             live with CUDA events around a graph of repeated launches, against the measured HBM
-             copy bandwidth; per-kernel rooflines sit in "kernels", and the
-             W4A16 GEMM alone across a 36-layer stack in "sweep".
-cpu_baseline = the CPU oracle on one full step of the same workload.
+value      = the metric's quantity: W4A16 GEMM algorithmic bytes (packed
+             int4 + fp16 group scales + fp16 activations) per step / device
+             time per step, GB/s, summed over ranks; K steps timed with CUDA
+             events on the launching stream.
+roofline   = the same kernel (one grouped launch per step) against the
+             measured HBM copy bandwidth, with ncu's DRAM bytes per launch.
+verify_step = the whole hot path per step: the layer set, then the int8
+             lm_head 2560->151936 with fused greedy argmax and the acceptance
+             of 15 seeded drafts in one launch.
+e2e        = that whole step through the C ABI with host buffers: one
+             cudaMemcpyAsync of the step's inputs from pinned host memory,
+             the library's calls (captured as one CUDA graph), one
+             cudaMemcpyAsync of the accepted tokens back, host synchronize;
+             no torch in the timed loop ("e2e_torch": the same through the
+             Python binding).
+sweep      = config 2: the 36-layer stack at M in {1,2,4,8,16,21}, as one
+             grouped launch for the whole stack and as one per layer set.
+cpu_baseline = the CPU oracle on the same layer set.
 
 --impl reference times the oracle alone (the only reference this method has
 here) on a bounded sample of the same workload per step.
@@ -170,13 +176,13 @@ class VerifyStep:
         self.out_dev = torch.empty(2 + K_DRAFT + 1, dtype=torch.int32, device=dev)
         self.n_acc = self.out_dev[0:1]
         self.out_tok = self.out_dev[2:].view(1, K_DRAFT + 1)
-        self.launches_per_step = len(inputs.LAYER_PROJS) + 1
+        # one grouped launch per layer set (plan per weight copy)
+        self.plans = [w4v.GroupedGemm([(self.acts[p.name], packed, s, None, self.outs[p.name])
+                                       for (p, packed, s) in layer]) for layer in self.projs]
+        self.launches_per_step = 2
 
     def enqueue(self, copy):
-        w4v = self.w4v
-        for p, packed, s in self.projs[copy]:
-            w4v.w4a16_gemm(self.acts[p.name], packed, s, p.N, out=self.outs[p.name], ws=self.ws[p.name],
-                           static_weights=True)
+        self.plans[copy](static_weights=True)
         self.lm_head()
 
     def lm_head(self):
@@ -192,11 +198,14 @@ def capture(torch, fn):
     return g
 
 
-# The lm_head kernel's device code: its source and the PTX helpers it inlines
-# (runtime.h, also included, holds host-side launch declarations of every
-# kernel family and changes whenever one is added).
+# A kernel's device code: its source and the PTX helpers it inlines (runtime.h,
+# also included, holds host-side launch declarations of every kernel family and
+# changes whenever one is added).
+PROFILES = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles")
 LM_HEAD_SOURCES = ("w8_lmhead_argmax.cu", "sm103_ptx.cuh")
-LM_HEAD_PROFILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "w8_lmhead_argmax_m16.md")
+LM_HEAD_PROFILE = os.path.join(PROFILES, "w8_lmhead_argmax_m16.json")
+GEMM_SOURCES = ("w4a16_gemm.cu", "sm103_ptx.cuh")
+GEMM_PROFILE = os.path.join(PROFILES, "w4a16_grouped_layer_set_m16.json")
 
 
 def kernel_source_sha(names):
@@ -211,23 +220,19 @@ def kernel_source_sha(names):
 
 
 def profiled_traffic(profile, names):
-    """DRAM bytes per launch (read + write) from the committed ncu summary of a
-    kernel, or None when the summary was taken from other sources than the
-    ones the kernel is built from now."""
+    """DRAM bytes per launch (read + write) from the committed ncu record of a
+    kernel (a small JSON file under profiles/), or None when the record was
+    taken from other sources than the ones the kernel is built from now."""
     try:
-        lines = open(profile).read().splitlines()
-    except OSError:
+        with open(profile) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    vals = {}
-    for ln in lines:
-        if ":" in ln and ln.split(":", 1)[0].strip() in ("source_sha256", "dram_bytes_read", "dram_bytes_write"):
-            k, v = ln.split(":", 1)
-            vals[k.strip()] = v.strip()
-    if vals.get("source_sha256") != kernel_source_sha(names):
+    if rec.get("source_sha256") != kernel_source_sha(names):
         return None
     try:
-        return int(vals["dram_bytes_read"]) + int(vals["dram_bytes_write"])
-    except (KeyError, ValueError):
+        return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
+    except (KeyError, TypeError, ValueError):
         return None
 
 
@@ -248,6 +253,18 @@ def job_value(bytes_per_rank, ms_step, world):
     return world * bytes_per_rank / (ms_step * 1e-3) / 1e9
 
 
+def layer_set_bytes(M=M_VERIFY, group=128):
+    return sum(p.N * p.K // 2 + (p.K // group) * p.N * 2 + M * p.K * 2 for p in inputs.LAYER_PROJS)
+
+
+def replay_steps(graph_all, graph_rem, steps, per):
+    """Replay a graph of `per` steps (and one of the remainder) for exactly `steps` steps."""
+    for _ in range(steps // per):
+        graph_all.replay()
+    if graph_rem is not None:
+        graph_rem.replay()
+
+
 def run_gpu(args, rank, world):
     import torch
     from speculative_decoding_verify_w4a16_gb300 import _build, w4v
@@ -262,84 +279,104 @@ def run_gpu(args, rank, world):
     w4v.load()
     w4v.init()
     peaks = load_peaks()
-    step = VerifyStep(dev, w4v, torch)
-    proj_bytes, lm_bytes = step_bytes()
-    total_bytes = proj_bytes + lm_bytes
+    gemm_bytes = layer_set_bytes()
 
-    # warm-up eagerly (first launches configure kernels), then capture graphs
+    # ---- config 1: the layer set at M = 16, one grouped launch per step, each
+    # step on the weights of another of 36 layers (1.87 GB, far above L2)
+    stack = Stack(dev, w4v, torch)
+    sets = stack.layer_plans(M_VERIFY)
+    L = stack.LAYERS
     for i in range(max(args.warmup, 3)):
-        step.enqueue(i % COPIES)
+        sets[i % L](static_weights=True)
     torch.cuda.synchronize()
-    graphs = [capture(torch, lambda c=c: step.enqueue(c)) for c in range(COPIES)]
-    for i in range(max(args.warmup, 3)):
-        graphs[i % COPIES].replay()
+    g_all = capture(torch, lambda: [sets[i](static_weights=True) for i in range(L)])
+    rem = args.steps % L
+    g_rem = capture(torch, lambda: [sets[i](static_weights=True) for i in range(rem)]) if rem else None
+    replay_steps(g_all, None, max(args.warmup, 3) * L, L)
     torch.cuda.synchronize()
 
-    # ---- timed region: K graph replays, no host synchronisation inside ---------
+    # ---- timed region: exactly K steps, no host synchronisation inside -------
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
         start.record()
-        for i in range(args.steps):
-            graphs[i % COPIES].replay()
+        replay_steps(g_all, g_rem, args.steps, L)
         end.record()
         torch.cuda.synchronize()
     ms_total = start.elapsed_time(end)
     ms_step = reduce_step_time(ms_total / args.steps, world, dev)
-    value = job_value(total_bytes, ms_step, world)
+    value = job_value(gemm_bytes, ms_step, world)
+    gemm_gbs = gemm_bytes / (ms_step * 1e-3) / 1e9
+    del g_all, g_rem
+    check_device_status(w4v, "layer set")
 
-    # ---- per-kernel durations: each kernel alone in a graph of repeated launches
-    kern = {}
+    # ---- the whole verify step: layer set + lm_head argmax + acceptance -------
+    step = VerifyStep(dev, w4v, torch)
+    proj_bytes, lm_bytes = step_bytes()
+    for i in range(3):
+        step.enqueue(i % COPIES)
+    torch.cuda.synchronize()
     reps = 20
+    step_ms = time_graph(torch, lambda: [step.enqueue(i % COPIES) for i in range(reps)]) / reps
     lm_ms = time_graph(torch, lambda: [step.lm_head() for _ in range(reps)]) / reps
     lm_gbs = lm_bytes / (lm_ms * 1e-3) / 1e9
-    kern["lm_head"] = {"ms": lm_ms, "bytes": lm_bytes, "GB/s": lm_gbs, "frac": lm_gbs / peaks["hbm_gbs"]}
-    stack = Stack(dev, w4v, torch)
+    verify_step = {"ms": round(step_ms, 5), "bytes": proj_bytes + lm_bytes,
+                   "GB/s": round((proj_bytes + lm_bytes) / (step_ms * 1e-3) / 1e9, 1),
+                   "launches": step.launches_per_step,
+                   "what": "grouped W4A16 layer set (3 rotating weight copies) + fused int8 lm_head argmax and "
+                           "acceptance of 15 drafts, %d steps in one CUDA graph" % reps,
+                   "lm_head": {"ms": round(lm_ms, 5), "bytes": lm_bytes, "GB/s": round(lm_gbs, 1),
+                               "frac": round(lm_gbs / peaks["hbm_gbs"], 4),
+                               "traffic": profiled_traffic(LM_HEAD_PROFILE, LM_HEAD_SOURCES)}}
+    check_device_status(w4v, "verify step")
+
+    # ---- per projection, one launch each (each launch on another layer) ------
+    kern = {}
     for p in inputs.LAYER_PROJS:
         ms = stack.time_projection(p, M_VERIFY)
         b = p.N * p.K // 2 + (p.K // 128) * p.N * 2 + M_VERIFY * p.K * 2
         gbs = b / (ms * 1e-3) / 1e9
-        kern[p.name] = {"ms": ms, "bytes": b, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"]}
-    lm = kern["lm_head"]
-    gemm_ms = sum(kern[p.name]["ms"] for p in inputs.LAYER_PROJS)
-    gemm_gbs = proj_bytes / (gemm_ms * 1e-3) / 1e9
+        kern[p.name] = {"ms": round(ms, 5), "bytes": b, "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    single_ms = sum(kern[p.name]["ms"] for p in inputs.LAYER_PROJS)
+    check_device_status(w4v, "per-projection launches")
 
-    check_device_status(w4v, "verify step and per-kernel graphs")
-
-    # ---- end to end through the public API with host buffers -----------------
-    e2e = run_e2e(args, step, torch, total_bytes, world)
-    check_device_status(w4v, "end to end")
+    # ---- end to end through the C ABI with host buffers ------------------------
+    e2e = run_e2e_capi(args, step, w4v, torch, proj_bytes + lm_bytes, gemm_bytes, world)
+    check_device_status(w4v, "end to end (C ABI)")
+    e2e_torch = run_e2e(args, step, torch, proj_bytes + lm_bytes, world)
+    check_device_status(w4v, "end to end (binding)")
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
-        "config": {"workload": "cfg1 verify step: 4B-shaped W4A16 g128 layer set (qkv, o, gate_up, down) "
-                               "+ int8 lm_head 2560->151936 argmax + accept, M=16 (K=15)",
-                   "M": M_VERIFY, "K_draft": K_DRAFT, "bytes_per_step": total_bytes,
-                   "l2": "inputs larger than L2: 442 MB read per step, projection weights rotate over "
-                         "%d copies" % COPIES,
-                   "graph": "one CUDA graph per step", "parallelism": "replicas" if world > 1 else "1 GPU",
-                   "weights": "static (W4V_STATIC_WEIGHTS: projection weights may be loaded before the previous "
-                              "kernel ends; inputs and outputs wait for it)"},
-        "roofline": {"bound": "hbm", "kernel": "w8_lmhead_argmax_accept (M=16, V=151936, K=2560, 15 drafts), "
-                               "%d launches "
-                               "in one graph, CUDA events on the launching stream" % reps,
-                     "achieved": round(lm["GB/s"], 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(lm["frac"], 4),
-                     "traffic": profiled_traffic(LM_HEAD_PROFILE, LM_HEAD_SOURCES),
-                     "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum per launch, ncu summary "
-                                       "profiles/w8_lmhead_argmax_m16.md (null if taken from other sources)",
+        "config": {"workload": "cfg1: 4B-shaped W4A16 g128 layer set (qkv 2560->7680, o 2560->2560, gate_up "
+                               "2560->19456, down 9728->2560) at M=16 (K=15 drafts + 1), one grouped launch per step",
+                   "M": M_VERIFY, "K_draft": K_DRAFT, "bytes_per_step": gemm_bytes,
+                   "l2": "inputs larger than L2: each step reads another of 36 layers' weights (1.87 GB in all)",
+                   "graph": "36 steps per CUDA graph (the remainder in a second graph)",
+                   "parallelism": "replicas" if world > 1 else "1 GPU",
+                   "weights": "static (W4V_STATIC_WEIGHTS: weights may be loaded before the previous kernel ends; "
+                              "activations and outputs wait for it)"},
+        "roofline": {"bound": "hbm", "kernel": "w4a16_decode_kernel (grouped launch of the layer set, M=16)",
+                     "achieved": round(gemm_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gemm_gbs / peaks["hbm_gbs"], 4),
+                     "traffic": profiled_traffic(GEMM_PROFILE, GEMM_SOURCES),
+                     "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum per launch, ncu record "
+                                       "profiles/w4a16_grouped_layer_set_m16.json (null if taken from other sources)",
+                     "algorithmic_bytes": gemm_bytes,
+                     "timing": "CUDA events on the launching stream around the K timed steps",
                      "peak_source": peaks["source"] + " (hbm copy, burst)"},
-        "gemm_m16": {"GB/s": round(gemm_gbs, 1), "frac": round(gemm_gbs / peaks["hbm_gbs"], 4),
-                     "ms": round(gemm_ms, 5), "bytes": proj_bytes},
-        "kernels": {k: {kk: (round(vv, 5) if isinstance(vv, float) else vv) for kk, vv in v.items()}
-                    for k, v in kern.items()},
+        "verify_step": verify_step,
+        "gemm_m16_single_launches": {"ms": round(single_ms, 5), "GB/s": round(gemm_bytes / (single_ms * 1e-3) / 1e9, 1),
+                                     "frac": round(gemm_bytes / (single_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                                     "per_projection": kern},
         "e2e": e2e,
-        "gpu_launches": step.launches_per_step * args.steps,
+        "e2e_torch": e2e_torch,
+        "gpu_launches": args.steps,
         "clocks": clk.summary(),
     }
     if args.sweep:
@@ -361,7 +398,7 @@ def run_gpu(args, rank, world):
         result["gemm_m16_g32"] = g32.layer_set(peaks)
         check_device_status(w4v, "group-32 layer set")
         del g32
-    del stack
+    del stack, sets
     torch.cuda.empty_cache()
     if args.prefill:
         result["prefill"] = run_prefill(dev, w4v, torch, peaks)
@@ -414,11 +451,114 @@ def run_e2e(args, step, torch, total_bytes, world):
     ms = reduce_step_time((time.perf_counter() - t0) / steps * 1e3, world, step.draft.device)
     h2d = step.in_host.numel()
     d2h = h_out.numel() * 4
-    return {"value": round(job_value(total_bytes, ms, world), 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "how": "one pinned host -> device copy of all activations and drafts, one CUDA graph of the step, "
-                   "one device -> host copy of the accepted length and tokens, host synchronize each step "
-                   "(wall clock)"}
+    return {"value": round(job_value(layer_set_bytes(), ms, world), 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "whole_step_GB/s": round(job_value(total_bytes, ms, world), 1),
+            "how": "through the Python binding: one pinned host -> device copy of all activations and drafts, "
+                   "one CUDA graph of the step, one device -> host copy of the accepted length and tokens, "
+                   "host synchronize each step (wall clock)"}
+
+
+def _cudart():
+    """The CUDA runtime library (for the C-ABI end-to-end leg)."""
+    import ctypes
+    import ctypes.util
+    for cand in (ctypes.util.find_library("cudart"), "/usr/local/cuda/lib64/libcudart.so", "libcudart.so.13"):
+        if not cand:
+            continue
+        try:
+            return ctypes.CDLL(cand)
+        except OSError:
+            continue
+    raise RuntimeError("libcudart not found")
+
+
+def run_e2e_capi(args, step, w4v, torch, total_bytes, gemm_bytes, world):
+    """The whole verify step end to end through the C ABI with host buffers and
+    no torch in the timed loop: per step one cudaMemcpyAsync of all the step's
+    inputs (activations of the four projections and the lm_head, drafts) from
+    pinned host memory, the grouped W4A16 launch and the fused lm_head argmax +
+    acceptance (libw4v's C entry points), one cudaMemcpyAsync of the accepted
+    length and tokens back, all captured once as a CUDA graph per weight copy;
+    the host launches the graph, synchronizes and reads the accepted length."""
+    import ctypes
+    cu = _cudart()
+    lib = w4v.load()
+    P, S = ctypes.c_void_p, ctypes.c_size_t
+    cu.cudaStreamCreateWithFlags.argtypes = [ctypes.POINTER(P), ctypes.c_uint]
+    cu.cudaHostAlloc.argtypes = [ctypes.POINTER(P), S, ctypes.c_uint]
+    cu.cudaFreeHost.argtypes = [P]
+    cu.cudaMemcpyAsync.argtypes = [P, P, S, ctypes.c_int, P]
+    cu.cudaStreamBeginCapture.argtypes = [P, ctypes.c_int]
+    cu.cudaStreamEndCapture.argtypes = [P, ctypes.POINTER(P)]
+    cu.cudaGraphInstantiate.argtypes = [ctypes.POINTER(P), P, ctypes.c_ulonglong]
+    cu.cudaGraphLaunch.argtypes = [P, P]
+    cu.cudaStreamSynchronize.argtypes = [P]
+    cu.cudaGraphExecDestroy.argtypes = [P]
+    cu.cudaGraphDestroy.argtypes = [P]
+    cu.cudaStreamDestroy.argtypes = [P]
+
+    def ok(code, what):
+        if code != 0:
+            raise RuntimeError("%s failed with CUDA error %d" % (what, code))
+
+    stream = P()
+    ok(cu.cudaStreamCreateWithFlags(ctypes.byref(stream), 1), "cudaStreamCreateWithFlags")
+    n_in = step.in_host.numel()
+    n_out = step.out_dev.numel() * 4
+    h_in, h_out = P(), P()
+    ok(cu.cudaHostAlloc(ctypes.byref(h_in), n_in, 0), "cudaHostAlloc")
+    ok(cu.cudaHostAlloc(ctypes.byref(h_out), n_out, 0), "cudaHostAlloc")
+    ctypes.memmove(h_in, step.in_host.data_ptr(), n_in)
+    V, H = inputs.V_4B, inputs.H_4B
+    execs, graphs = [], []
+    for c in range(COPIES):
+        plan = step.plans[c]
+        ok(cu.cudaStreamBeginCapture(stream, 2), "cudaStreamBeginCapture")     # relaxed mode
+        ok(cu.cudaMemcpyAsync(P(step.in_dev.data_ptr()), h_in, n_in, 1, stream), "cudaMemcpyAsync in")
+        st = lib.w4a16_gemm_grouped(ctypes.byref(plan.handle), P(plan.ws.data_ptr()), plan.ws.numel(),
+                                    w4v.STATIC_WEIGHTS, stream)
+        st2 = lib.w8_lmhead_argmax_accept(P(step.X.data_ptr()), P(step.W8.data_ptr()), P(step.s8.data_ptr()),
+                                          1, K_DRAFT, H, V, P(step.draft.data_ptr()), P(step.tok.data_ptr()),
+                                          P(step.n_acc.data_ptr()), P(step.out_tok.data_ptr()), None,
+                                          P(step.ws_lm.data_ptr()), step.ws_lm.numel(), stream)
+        ok(cu.cudaMemcpyAsync(h_out, P(step.out_dev.data_ptr()), n_out, 2, stream), "cudaMemcpyAsync out")
+        g = P()
+        ok(cu.cudaStreamEndCapture(stream, ctypes.byref(g)), "cudaStreamEndCapture")
+        if st != 0 or st2 != 0:
+            raise RuntimeError("library call failed during capture: %d %d" % (st, st2))
+        ex = P()
+        ok(cu.cudaGraphInstantiate(ctypes.byref(ex), g, 0), "cudaGraphInstantiate")
+        graphs.append(g)
+        execs.append(ex)
+    n_acc = ctypes.cast(h_out, ctypes.POINTER(ctypes.c_int32))
+    for i in range(max(args.warmup, 3)):
+        ok(cu.cudaGraphLaunch(execs[i % COPIES], stream), "cudaGraphLaunch")
+        ok(cu.cudaStreamSynchronize(stream), "cudaStreamSynchronize")
+    if world > 1:
+        torch.distributed.barrier()
+    launch, sync = cu.cudaGraphLaunch, cu.cudaStreamSynchronize
+    t0 = time.perf_counter()
+    acc = 0
+    for i in range(args.steps):
+        launch(execs[i % COPIES], stream)
+        sync(stream)
+        acc += n_acc[0]                      # the host reads the accepted length every step
+    ms = reduce_step_time((time.perf_counter() - t0) / args.steps * 1e3, world, step.draft.device)
+    for ex, g in zip(execs, graphs):
+        cu.cudaGraphExecDestroy(ex)
+        cu.cudaGraphDestroy(g)
+    cu.cudaFreeHost(h_in)
+    cu.cudaFreeHost(h_out)
+    cu.cudaStreamDestroy(stream)
+    return {"value": round(job_value(gemm_bytes, ms, world), 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
+            "h2d_bytes_per_step": int(n_in), "d2h_bytes_per_step": int(n_out),
+            "whole_step_GB/s": round(job_value(total_bytes, ms, world), 1),
+            "how": "C ABI through ctypes and the CUDA runtime, no torch in the loop: per step one CUDA graph "
+                   "(cudaMemcpyAsync of the inputs from pinned host memory, w4a16_gemm_grouped, "
+                   "w8_lmhead_argmax_accept, cudaMemcpyAsync of the accepted tokens back), then "
+                   "cudaStreamSynchronize and a host read of the accepted length (wall clock); value = the "
+                   "W4A16 GEMM bytes of the step over the step's end-to-end time"}
 
 
 def time_graph(torch, fn, reps=3):
@@ -489,62 +629,85 @@ class Stack:
 
         return time_graph(self.torch, run) / self.LAYERS
 
+    def layer_plans(self, M, bufs=None):
+        """One grouped plan per layer: its four projections in one launch."""
+        acts, outs, _ = bufs if bufs is not None else self._buffers(M)
+        return [self.w4v.GroupedGemm([(acts[p.name], packed, sc, None, outs[p.name]) for (p, packed, sc) in lay],
+                                     group=self.group) for lay in self.layers]
+
+    def stack_plan(self, M, bufs=None):
+        """The whole stack (every projection of every layer) as one grouped launch."""
+        acts, outs, _ = bufs if bufs is not None else self._buffers(M)
+        return self.w4v.GroupedGemm([(acts[p.name], packed, sc, None, outs[p.name])
+                                     for lay in self.layers for (p, packed, sc) in lay], group=self.group)
+
+    def bytes(self, M):
+        return self.LAYERS * sum(self.proj_bytes(p, M) for p in inputs.LAYER_PROJS)
+
     def layer_set(self, peaks, M=M_VERIFY):
-        """Per-projection device time (each in a graph of one launch per layer) and the layer set's GB/s."""
-        out, tot_ms, tot_b = {}, 0.0, 0
+        """The layer set in one grouped launch per layer (36 launches, one graph),
+        and per projection one launch each."""
+        plans = self.layer_plans(M)
+        ms = time_graph(self.torch, lambda: [g(static_weights=True) for g in plans]) / self.LAYERS
+        b = sum(self.proj_bytes(p, M) for p in inputs.LAYER_PROJS)
+        gbs = b / (ms * 1e-3) / 1e9
+        per = {}
         for p in inputs.LAYER_PROJS:
-            ms = self.time_projection(p, M)
-            b = self.proj_bytes(p, M)
-            out[p.name] = {"ms": round(ms, 5), "GB/s": round(b / (ms * 1e-3) / 1e9, 1)}
-            tot_ms += ms
-            tot_b += b
-        gbs = tot_b / (tot_ms * 1e-3) / 1e9
-        return {"group": self.group, "M": M, "ms": round(tot_ms, 5), "bytes": tot_b, "GB/s": round(gbs, 1),
-                "frac": round(gbs / peaks["hbm_gbs"], 4), "per_projection": out}
+            pm = self.time_projection(p, M)
+            per[p.name] = {"ms": round(pm, 5), "GB/s": round(self.proj_bytes(p, M) / (pm * 1e-3) / 1e9, 1)}
+        return {"group": self.group, "M": M, "ms": round(ms, 5), "bytes": b, "GB/s": round(gbs, 1),
+                "frac": round(gbs / peaks["hbm_gbs"], 4), "launch": "one grouped launch per layer set",
+                "single_launches_per_projection": per}
 
     def stack_graph(self, peaks, M=M_VERIFY):
-        """Every projection of every layer in one CUDA graph at M rows."""
-        acts, outs, wss = self._buffers(M)
-
-        def run():
-            for lay in self.layers:
-                for (p, packed, sc) in lay:
-                    self.w4v.w4a16_gemm(acts[p.name], packed, sc, p.N, out=outs[p.name], ws=wss[p.name],
-                                        static_weights=True, group=self.group)
-
-        ms = time_graph(self.torch, run)
-        b = self.LAYERS * sum(self.proj_bytes(p, M) for p in inputs.LAYER_PROJS)
+        """Every projection of every layer in one grouped launch."""
+        big = self.stack_plan(M)
+        ms = time_graph(self.torch, lambda: [big(static_weights=True) for _ in range(3)]) / 3
+        b = self.bytes(M)
         gbs = b / (ms * 1e-3) / 1e9
         return {"layers": self.LAYERS, "group": self.group, "M": M, "ms": round(ms, 4), "bytes": b,
-                "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4), "launches": 4 * self.LAYERS}
+                "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4), "launches": 1}
 
     def sweep(self, peaks):
+        """Config 2: the 36-layer stack at each verify size, as one grouped launch
+        for the whole stack, as one grouped launch per layer set, and as one
+        launch per projection."""
         out = {}
         for M in (1, 2, 4, 8, 16, 21):
-            acts, outs, wss = self._buffers(M)
+            bufs = self._buffers(M)
+            acts, outs, wss = bufs
+            b = self.bytes(M)
+            big = self.stack_plan(M, bufs)
+            ms_big = time_graph(self.torch, lambda: [big(static_weights=True) for _ in range(3)]) / 3
+            plans = self.layer_plans(M, bufs)
+            ms_lay = time_graph(self.torch, lambda: [g(static_weights=True) for g in plans])
 
             def run():
                 for lay in self.layers:
                     for (p, packed, sc) in lay:
                         self.w4v.w4a16_gemm(acts[p.name], packed, sc, p.N, out=outs[p.name], ws=wss[p.name],
-                                    static_weights=True)
+                                            static_weights=True)
 
-            ms = time_graph(self.torch, run)
-            b = self.LAYERS * sum(p.N * p.K // 2 + (p.K // 128) * p.N * 2 + M * p.K * 2 for p in inputs.LAYER_PROJS)
-            gbs = b / (ms * 1e-3) / 1e9
-            out["M=%d" % M] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
-                               "launches": 4 * self.LAYERS}
+            ms_one = time_graph(self.torch, run)
+            f = lambda ms: round(b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
+            out["M=%d" % M] = {"ms": round(ms_big, 4), "GB/s": round(b / (ms_big * 1e-3) / 1e9, 1),
+                               "frac": f(ms_big), "launches": 1,
+                               "per_layer_set": {"ms": round(ms_lay, 4), "frac": f(ms_lay), "launches": self.LAYERS},
+                               "per_projection": {"ms": round(ms_one, 4), "frac": f(ms_one),
+                                                  "launches": 4 * self.LAYERS}}
+            del big, plans
         return out
 
     def full_verify(self, W8, s8, peaks):
-        """The whole 36-layer verify step as one CUDA graph: every projection of
-        every layer, then the lm_head argmax with acceptance of M-1 drafts in one
-        launch (M = 16: K = 15; M = 21: K = 20 with seeded -1 padding)."""
+        """The whole 36-layer verify step as one CUDA graph: one grouped launch per
+        layer set (the layers of a model run one after the other), then the
+        lm_head argmax with acceptance of M-1 drafts in one launch (M = 16:
+        K = 15; M = 21: K = 20 with seeded -1 padding)."""
         torch, w4v = self.torch, self.w4v
         H, V = inputs.H_4B, inputs.V_4B
         out = {}
         for M in (16, 21):
-            acts, outs, wss = self._buffers(M)
+            plans = self.layer_plans(M)
             X = torch.randn((M, H), generator=self.g, device=self.dev).half()
             d = inputs.rng(SEED, "stack-drafts", M).integers(0, V, size=(1, M - 1)).astype(np.int32)
             if M == 21:
@@ -556,18 +719,16 @@ class Stack:
             ws = w4v.workspace(w4v.w8_lmhead_argmax_workspace_bytes(M, V), self.dev)
 
             def run():
-                for lay in self.layers:
-                    for (p, packed, sc) in lay:
-                        w4v.w4a16_gemm(acts[p.name], packed, sc, p.N, out=outs[p.name], ws=wss[p.name],
-                                       static_weights=True)
+                for g in plans:
+                    g(static_weights=True)
                 w4v.w8_lmhead_argmax_accept(X, W8, s8, d, out=tok, n_out=n, tok_out=o, ws=ws)
 
             ms = time_graph(torch, run)
-            b = self.LAYERS * sum(p.N * p.K // 2 + (p.K // 128) * p.N * 2 + M * p.K * 2 for p in inputs.LAYER_PROJS)
-            b += V * H + 2 * V + 2 * M * H
+            b = self.bytes(M) + V * H + 2 * V + 2 * M * H
             gbs = b / (ms * 1e-3) / 1e9
             out["M=%d" % M] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
-                               "launches": 4 * self.LAYERS + 1, "K_draft": M - 1}
+                               "launches": self.LAYERS + 1, "K_draft": M - 1}
+            del plans
         return out
 
 
@@ -719,10 +880,10 @@ def _cores():
         return os.cpu_count() or 1
 
 
-def oracle_step(host, frac=1.0):
-    """The oracle on the config-1 step; frac < 1 keeps that fraction of every
-    weight matrix's output rows (all 16 activation rows, full K).  Returns the
-    algorithmic bytes it processed."""
+def oracle_gemm(host, frac=1.0):
+    """The oracle on the config-1 layer set (the metric's quantity); frac < 1
+    keeps that fraction of every weight matrix's output rows (all 16
+    activation rows, full K).  Returns the algorithmic bytes it processed."""
     import oracle
     nbytes = 0
     for p in inputs.LAYER_PROJS:
@@ -731,6 +892,14 @@ def oracle_step(host, frac=1.0):
         A = host["acts"][p.name]
         oracle.w4a16_gemm(A, q[:n], np.ascontiguousarray(s[:, :n]))
         nbytes += n * p.K // 2 + (p.K // 128) * n * 2 + M_VERIFY * p.K * 2
+    return nbytes
+
+
+def oracle_step(host, frac=1.0):
+    """The oracle on the whole config-1 step: the layer set, then the lm_head,
+    argmax and acceptance (same sampling).  Returns the bytes processed."""
+    import oracle
+    nbytes = oracle_gemm(host, frac)
     W8, s8 = host["lm"]
     v = max(8, int(W8.shape[0] * frac))
     L = oracle.lmhead_logits(host["X"], W8[:v], s8[:v])
@@ -746,13 +915,16 @@ def cpu_baseline(step):
     oracle.build()
     threads = oracle.num_threads()
     t0 = time.perf_counter()
-    nbytes = oracle_step(step.host, 1.0)
+    nbytes = oracle_gemm(step.host, 1.0)
     dt = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    nbytes_step = oracle_step(step.host, 1.0)
+    dt_step = time.perf_counter() - t0
     # the same oracle on one thread, on 1/16 of every matrix's output rows
     oracle.set_num_threads(1)
     try:
         t1 = time.perf_counter()
-        nb1 = oracle_step(step.host, 1.0 / 16)
+        nb1 = oracle_gemm(step.host, 1.0 / 16)
         dt1 = time.perf_counter() - t1
     finally:
         oracle.set_num_threads(threads)
@@ -769,9 +941,11 @@ def cpu_baseline(step):
         t_mm += t4 - t3
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle", "seconds": round(dt, 2),
-            "sample": "one full cfg1 verify step (4 projections + lm_head + argmax + accept), M=16, "
-                      "double precision, OpenMP over output rows",
+            "sample": "the full cfg1 W4A16 layer set (4 projections, M=16), double precision, OpenMP over "
+                      "output rows",
             "affinity_cores": _cores(), "nproc": os.cpu_count(),
+            "whole_step": {"GB/s": round(nbytes_step / dt_step / 1e9, 4), "seconds": round(dt_step, 2),
+                           "sample": "layer set + lm_head + argmax + acceptance"},
             "single_thread": {"GB/s": round(nb1 / dt1 / 1e9, 4), "seconds": round(dt1, 2),
                               "sample": "1/16 of every matrix's output rows, one thread"},
             "projections_split_s": {"dequant": round(t_deq, 3), "gemm": round(t_mm, 3)}}
@@ -793,21 +967,21 @@ def run_reference(args, rank, world):
     host = host_inputs()
     frac = args.ref_frac
     for _ in range(args.warmup):
-        oracle_step(host, frac)
+        oracle_gemm(host, frac)
     t0 = time.perf_counter()
     nbytes = 0
     for _ in range(args.steps):
-        nbytes = oracle_step(host, frac)
+        nbytes = oracle_gemm(host, frac)
     dt = (time.perf_counter() - t0) / args.steps
     value = nbytes / dt / 1e9
     cb = {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-          "sample": "per step: %.4g of every weight matrix's output rows of the cfg1 verify step "
+          "sample": "per step: %.4g of every weight matrix's output rows of the cfg1 W4A16 layer set "
                     "(all 16 rows, full K), double precision" % frac}
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": "cfg1 verify step (CPU oracle sample)", "M": M_VERIFY,
+            "config": {"workload": "cfg1 W4A16 layer set at M=16 (CPU oracle sample)", "M": M_VERIFY,
                        "bytes_per_step": nbytes, "parallelism": "host cores"},
             "cpu_baseline": cb,
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -824,6 +998,8 @@ def main():
     ap.add_argument("--no-prefill", dest="prefill", action="store_false")
     ap.add_argument("--prefill-only", action="store_true", help="run only the prefill leg (profiling aid)")
     ap.add_argument("--gdn-only", action="store_true", help="run only the gated-delta state leg (profiling aid)")
+    ap.add_argument("--lmhead-only", action="store_true",
+                    help="run only the batched lm_head leg (8 x 16 rows, then the last row; profiling aid)")
     ap.add_argument("--ref-frac", type=float, default=1.0 / 16)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -838,7 +1014,7 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
-    if args.prefill_only or args.gdn_only:
+    if args.prefill_only or args.gdn_only or args.lmhead_only:
         import torch
         from speculative_decoding_verify_w4a16_gb300 import _build, w4v
         _build.build()
@@ -846,10 +1022,12 @@ def main():
         w4v.init()
         dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
         if args.prefill_only:
-            out = {"prefill": run_prefill(dev, w4v, torch, load_peaks())}
+            out, leg = {"prefill": run_prefill(dev, w4v, torch, load_peaks())}, "prefill"
+        elif args.lmhead_only:
+            out, leg = {"lmhead_batched": run_lmhead_batched(dev, w4v, torch, load_peaks())}, "batched lm_head"
         else:
-            out = {"gdn_state": run_gdn(dev, w4v, torch)}
-        check_device_status(w4v, "prefill" if args.prefill_only else "recurrent state")
+            out, leg = {"gdn_state": run_gdn(dev, w4v, torch)}, "recurrent state"
+        check_device_status(w4v, leg)
         print(json.dumps(out), flush=True)
         return
     res = run_gpu(args, rank, world)

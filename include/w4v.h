@@ -231,6 +231,22 @@ w4v_status w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uint16_t *
                             float *logits_debug, void *workspace, size_t workspace_bytes,
                             w4v_stream_t stream);
 
+/* w8_lmhead_argmax with flags (w8_lmhead_argmax is this with flags == 0).
+ *   W4V_BATCH_INVARIANT: for M > 32, run the rows in blocks of 32 (one launch
+ *     each, the weights read once per block), so that every row's logits and
+ *     token are bit for bit those of a call with that row alone.  Up to 32
+ *     rows every logit comes from the same arithmetic whatever M is; a
+ *     single launch over more rows sums each logit in another order (within
+ *     the same fp32 error bound), which may flip a token between two logits
+ *     that close.  Several sequences' verify blocks in one call then accept
+ *     exactly the tokens each would accept alone ("Efficient LLM Challenge
+ *     Results", section 3: greedy verification leaves the output unchanged).
+ * Unknown flag bits: W4V_ERR_ARG.  Other arguments as w8_lmhead_argmax. */
+w4v_status w8_lmhead_argmax_ex(const uint16_t *X, const int8_t *W, const uint16_t *scale,
+                               int M, int K, int V, int32_t *argmax_out, float *maxlogit,
+                               float *logits_debug, void *workspace, size_t workspace_bytes,
+                               unsigned flags, w4v_stream_t stream);
+
 /* ---------------------------------------------- w8_lmhead_argmax_noalloc
  * The paper has no counterpart to this entry point; it exists for callers
  * that cannot allocate device memory for a workspace -- for example a plugin
@@ -292,6 +308,18 @@ w4v_status w8_lmhead_argmax_accept(const uint16_t *X, const int8_t *W, const uin
                                    int32_t *argmax_out, int32_t *n_accepted, int32_t *out_tokens,
                                    float *maxlogit, void *workspace, size_t workspace_bytes,
                                    w4v_stream_t stream);
+
+/* w8_lmhead_argmax_accept with flags (the plain entry point is this with
+ * flags == 0).  W4V_BATCH_INVARIANT: for M = B*(n_draft+1) > 32, the argmax
+ * runs as in w8_lmhead_argmax_ex with that flag (blocks of 32 rows) and the
+ * acceptance follows in one more launch; the results are those of
+ * w8_lmhead_argmax_ex followed by spec_accept.  Unknown flag bits:
+ * W4V_ERR_ARG. */
+w4v_status w8_lmhead_argmax_accept_ex(const uint16_t *X, const int8_t *W, const uint16_t *scale,
+                                      int B, int n_draft, int K, int V, const int32_t *draft,
+                                      int32_t *argmax_out, int32_t *n_accepted, int32_t *out_tokens,
+                                      float *maxlogit, void *workspace, size_t workspace_bytes,
+                                      unsigned flags, w4v_stream_t stream);
 
 /* ------------------------------------------------------------ ngram_draft
  * Model-free drafts by prompt lookup ("Efficient LLM Challenge Results",

@@ -198,6 +198,30 @@ size_t w8_lmhead_argmax_workspace_bytes(int M, int V) {
 w4v_status w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uint16_t *scale, int M, int K,
                             int V, int32_t *argmax_out, float *maxlogit, float *logits_debug,
                             void *ws, size_t ws_bytes, w4v_stream_t stream) {
+    return w8_lmhead_argmax_ex(X, W, scale, M, K, V, argmax_out, maxlogit, logits_debug, ws, ws_bytes, 0u, stream);
+}
+
+namespace {
+// The rows in blocks of at most 32, one launch each, in order on the stream
+// (each leaves the workspace cleared for the next): every row gets the
+// arithmetic of a call with 1..32 rows.
+w4v_status lmhead_row_blocks(const uint16_t *X, const int8_t *W, const uint16_t *scale, int M, int K, int V,
+                             int32_t *argmax_out, float *maxlogit, float *logits, void *ws, cudaStream_t stream) {
+    for (int m0 = 0; m0 < M; m0 += w4v::kDecodeMaxRows) {
+        const int mb = std::min(w4v::kDecodeMaxRows, M - m0);
+        const w4v_status st = w4v::launch_w8_lmhead_argmax(
+            X + size_t(m0) * K, W, scale, mb, K, V, argmax_out + m0, maxlogit != nullptr ? maxlogit + m0 : nullptr,
+            logits != nullptr ? logits + size_t(m0) * V : nullptr, ws, stream);
+        if (st != W4V_OK) return st;
+    }
+    return W4V_OK;
+}
+}  // namespace
+
+w4v_status w8_lmhead_argmax_ex(const uint16_t *X, const int8_t *W, const uint16_t *scale, int M, int K,
+                               int V, int32_t *argmax_out, float *maxlogit, float *logits_debug,
+                               void *ws, size_t ws_bytes, unsigned flags, w4v_stream_t stream) {
+    if ((flags & ~unsigned(W4V_BATCH_INVARIANT)) != 0u) return W4V_ERR_ARG;
     if (M < 0 || M > 128 || K <= 0 || V <= 0 || K % 128 != 0 || V % 8 != 0) return W4V_ERR_SHAPE;
     if (M == 0) return W4V_OK;
     if (X == nullptr || W == nullptr || scale == nullptr || argmax_out == nullptr) return W4V_ERR_ARG;
@@ -207,6 +231,9 @@ w4v_status w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uint16_t *
         return W4V_ERR_ALIGN;
     if (ws == nullptr || ws_bytes < w4v::w8_lmhead_ws_bytes(M, V)) return W4V_ERR_WORKSPACE;
     if (!w4v::aligned16(ws)) return W4V_ERR_ALIGN;
+    if (M > w4v::kDecodeMaxRows && (flags & W4V_BATCH_INVARIANT) != 0u)
+        return lmhead_row_blocks(X, W, scale, M, K, V, argmax_out, maxlogit, logits_debug, ws,
+                                 reinterpret_cast<cudaStream_t>(stream));
     return w4v::launch_w8_lmhead_argmax(X, W, scale, M, K, V, argmax_out, maxlogit, logits_debug, ws,
                                         reinterpret_cast<cudaStream_t>(stream));
 }
@@ -215,6 +242,15 @@ w4v_status w8_lmhead_argmax_accept(const uint16_t *X, const int8_t *W, const uin
                                    int K, int V, const int32_t *draft, int32_t *argmax_out, int32_t *n_accepted,
                                    int32_t *out_tokens, float *maxlogit, void *ws, size_t ws_bytes,
                                    w4v_stream_t stream) {
+    return w8_lmhead_argmax_accept_ex(X, W, scale, B, n_draft, K, V, draft, argmax_out, n_accepted, out_tokens,
+                                      maxlogit, ws, ws_bytes, 0u, stream);
+}
+
+w4v_status w8_lmhead_argmax_accept_ex(const uint16_t *X, const int8_t *W, const uint16_t *scale, int B,
+                                      int n_draft, int K, int V, const int32_t *draft, int32_t *argmax_out,
+                                      int32_t *n_accepted, int32_t *out_tokens, float *maxlogit, void *ws,
+                                      size_t ws_bytes, unsigned flags, w4v_stream_t stream) {
+    if ((flags & ~unsigned(W4V_BATCH_INVARIANT)) != 0u) return W4V_ERR_ARG;
     if (B < 0 || n_draft < 0 || K <= 0 || V <= 0 || K % 128 != 0 || V % 8 != 0) return W4V_ERR_SHAPE;
     if (B > 128 || long(B) * (n_draft + 1) > 128) return W4V_ERR_SHAPE;
     if (B == 0) return W4V_OK;
@@ -229,6 +265,14 @@ w4v_status w8_lmhead_argmax_accept(const uint16_t *X, const int8_t *W, const uin
         return W4V_ERR_ALIGN;
     if (ws == nullptr || ws_bytes < w4v::w8_lmhead_ws_bytes(M, V)) return W4V_ERR_WORKSPACE;
     if (!w4v::aligned16(ws)) return W4V_ERR_ALIGN;
+    if (M > w4v::kDecodeMaxRows && (flags & W4V_BATCH_INVARIANT) != 0u) {
+        // the row blocks' tokens, then the acceptance of every sequence over them
+        const w4v_status st = lmhead_row_blocks(X, W, scale, M, K, V, argmax_out, maxlogit, nullptr, ws,
+                                                reinterpret_cast<cudaStream_t>(stream));
+        if (st != W4V_OK) return st;
+        return w4v::launch_spec_accept(argmax_out, draft, B, n_draft, n_accepted, out_tokens,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    }
     const w4v::LmAccept acc{draft, B, n_draft, n_accepted, out_tokens};
     return w4v::launch_w8_lmhead_argmax(X, W, scale, M, K, V, argmax_out, maxlogit, nullptr, ws,
                                         reinterpret_cast<cudaStream_t>(stream), &acc);

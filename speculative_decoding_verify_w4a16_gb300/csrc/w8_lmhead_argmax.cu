@@ -451,6 +451,10 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
                     __syncwarp();
                     if (lane == 0) mbar_arrive(dempty(buf));
                 }
+                // the warp's best key and lowest winning lane for each of the
+                // block's 16 rows land in lane jj; lanes 0..15 then fold them
+                // into the CTA's row keys with one atomic instruction
+                uint32_t mykey = 0u, mylane = 0u;
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
                     const int m = 16 * b + jj;
@@ -459,11 +463,15 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
                     const uint32_t key = valid ? logit_key(x) : 0u;
                     const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, key);
                     const uint32_t wlane = __reduce_min_sync(0xFFFFFFFFu, key == wmax ? uint32_t(lane) : 32u);
-                    if (lane == 0 && m < p.M && wmax != 0u) {
-                        const uint32_t vbest = uint32_t(t * kTileV + 32 * q) + wlane;
-                        atomicMax(&best[m], (static_cast<unsigned long long>(wmax) << 32) |
-                                                (0xFFFFFFFFull - vbest));
+                    if (lane == jj) {
+                        mykey = wmax;
+                        mylane = wlane;
                     }
+                }
+                const int mrow = 16 * b + lane;
+                if (lane < 16 && mrow < p.M && mykey != 0u) {
+                    const uint32_t vbest = uint32_t(t * kTileV + 32 * q) + mylane;
+                    atomicMax(&best[mrow], (static_cast<unsigned long long>(mykey) << 32) | (0xFFFFFFFFull - vbest));
                 }
             }
         }

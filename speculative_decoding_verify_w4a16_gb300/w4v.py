@@ -83,6 +83,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.w8_lmhead_argmax_workspace_bytes.restype = S
             lib.w8_lmhead_argmax.argtypes = [P, P, P, I, I, I, P, P, P, P, S, P]
             lib.w8_lmhead_argmax.restype = I
+            lib.w8_lmhead_argmax_ex.argtypes = [P, P, P, I, I, I, P, P, P, P, S, ctypes.c_uint, P]
+            lib.w8_lmhead_argmax_ex.restype = I
+            lib.w8_lmhead_argmax_accept_ex.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, S, ctypes.c_uint, P]
+            lib.w8_lmhead_argmax_accept_ex.restype = I
             lib.spec_accept.argtypes = [P, P, I, I, P, P, P]
             lib.spec_accept.restype = I
             lib.w8_lmhead_argmax_accept.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, S, P]
@@ -238,8 +242,11 @@ class GroupedGemm:
         return [p[4] for p in self.problems]
 
 
-def w8_lmhead_argmax(X, W, scale, out=None, maxlogit=None, logits=None, ws=None, stream=None):
-    """Greedy token per row of X through the int8 lm_head; returns the int32 [M] token tensor."""
+def w8_lmhead_argmax(X, W, scale, out=None, maxlogit=None, logits=None, ws=None, stream=None,
+                     batch_invariant=False):
+    """Greedy token per row of X through the int8 lm_head; returns the int32 [M] token tensor.
+    batch_invariant: for M > 32, blocks of 32 rows (W4V_BATCH_INVARIANT): each row's
+    logits and token equal those of the row computed alone."""
     import torch
     M, K = X.shape
     V = W.shape[0]
@@ -247,8 +254,9 @@ def w8_lmhead_argmax(X, W, scale, out=None, maxlogit=None, logits=None, ws=None,
         out = torch.empty(M, dtype=torch.int32, device=X.device)
     if ws is None:
         ws = workspace(w8_lmhead_argmax_workspace_bytes(M, V), X.device)
-    code = load().w8_lmhead_argmax(_ptr(X), _ptr(W), _ptr(scale), M, K, V, _ptr(out), _ptr(maxlogit),
-                                   _ptr(logits), _ptr(ws), ws.numel(), _stream(stream))
+    code = load().w8_lmhead_argmax_ex(_ptr(X), _ptr(W), _ptr(scale), M, K, V, _ptr(out), _ptr(maxlogit),
+                                      _ptr(logits), _ptr(ws), ws.numel(), BATCH_INVARIANT if batch_invariant else 0,
+                                      _stream(stream))
     _check(code, "w8_lmhead_argmax")
     return out
 
@@ -269,7 +277,7 @@ def spec_accept(target, draft, n_out=None, tok_out=None, stream=None):
 
 
 def w8_lmhead_argmax_accept(X, W, scale, draft, out=None, n_out=None, tok_out=None, maxlogit=None, ws=None,
-                            stream=None):
+                            stream=None, batch_invariant=False):
     """lm_head argmax of the B*(n+1) rows of X and greedy acceptance of drafts [B][n] in one launch.
     Returns (tokens [B*(n+1)], n_accepted [B], emitted tokens [B][n+1])."""
     import torch
@@ -286,9 +294,10 @@ def w8_lmhead_argmax_accept(X, W, scale, draft, out=None, n_out=None, tok_out=No
         raise W4VError(ERR_SHAPE, "w8_lmhead_argmax_accept")
     if ws is None:
         ws = workspace(w8_lmhead_argmax_workspace_bytes(M, V), X.device)
-    code = load().w8_lmhead_argmax_accept(_ptr(X), _ptr(W), _ptr(scale), B, nd, K, V,
-                                          _ptr(draft) if nd > 0 else None, _ptr(out), _ptr(n_out),
-                                          _ptr(tok_out), _ptr(maxlogit), _ptr(ws), ws.numel(), _stream(stream))
+    code = load().w8_lmhead_argmax_accept_ex(_ptr(X), _ptr(W), _ptr(scale), B, nd, K, V,
+                                             _ptr(draft) if nd > 0 else None, _ptr(out), _ptr(n_out),
+                                             _ptr(tok_out), _ptr(maxlogit), _ptr(ws), ws.numel(),
+                                             BATCH_INVARIANT if batch_invariant else 0, _stream(stream))
     _check(code, "w8_lmhead_argmax_accept")
     return out, n_out, tok_out
 

@@ -107,6 +107,18 @@ def test_argument_validation_before_launch(w4v_mod):
     assert lib.w8_lmhead_argmax(FAKE, FAKE + 8, FAKE, 16, 256, 1024, FAKE, None, None, FAKE, 1 << 30, None) == w4v_mod.ERR_ALIGN
     assert lib.w8_lmhead_argmax(FAKE, FAKE, FAKE, 16, 256, 1024, FAKE, None, None, FAKE, ws_small, None) == w4v_mod.ERR_WORKSPACE
     assert lib.w8_lmhead_argmax(None, None, None, 0, 256, 1024, None, None, None, None, 0, None) == w4v_mod.OK
+    # w8_lmhead_argmax_ex / _accept_ex: unknown flag bits, then the same checks
+    ex = lib.w8_lmhead_argmax_ex
+    assert ex(FAKE, FAKE, FAKE, 16, 256, 1024, FAKE, None, None, FAKE, 1 << 30, 1, None) == w4v_mod.ERR_ARG
+    assert ex(FAKE, FAKE, FAKE, 129, 256, 1024, FAKE, None, None, FAKE, 1 << 30, 2, None) == w4v_mod.ERR_SHAPE
+    assert ex(FAKE, FAKE, FAKE, 64, 256, 1024, FAKE, None, None, FAKE, ws_small, 2, None) == w4v_mod.ERR_WORKSPACE
+    assert ex(None, None, None, 0, 256, 1024, None, None, None, None, 0, 2, None) == w4v_mod.OK
+    aex = lib.w8_lmhead_argmax_accept_ex
+    assert aex(FAKE, FAKE, FAKE, 8, 15, 256, 1024, FAKE, FAKE, FAKE, None, None, FAKE, 1 << 30, 4,
+               None) == w4v_mod.ERR_ARG
+    assert aex(FAKE, FAKE, FAKE, 8, 16, 256, 1024, FAKE, FAKE, FAKE, None, None, FAKE, 1 << 30, 2,
+               None) == w4v_mod.ERR_SHAPE
+    assert aex(None, None, None, 0, 15, 256, 1024, None, None, None, None, None, None, 0, 2, None) == w4v_mod.OK
     # spec_accept
     assert lib.spec_accept(FAKE, FAKE, 4, 1025, FAKE, None, None) == w4v_mod.ERR_SHAPE
     assert lib.spec_accept(FAKE, FAKE, -1, 4, FAKE, None, None) == w4v_mod.ERR_SHAPE

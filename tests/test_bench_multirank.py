@@ -56,19 +56,26 @@ def test_reference_arm_only_on_rank0():
 
 
 def test_profiled_traffic_needs_matching_sources(tmp_path):
-    """The roofline's DRAM traffic comes from a committed ncu summary and is
-    used only while the summary names the fingerprint of the sources being
-    built; otherwise it is null."""
+    """The roofline's DRAM traffic comes from a committed ncu record (a small
+    JSON file) and is used only while the record names the fingerprint of the
+    sources being built; otherwise it is null."""
+    import json
     sys.path.insert(0, ROOT)
     import bench
-    sha = bench.kernel_source_sha(bench.LM_HEAD_SOURCES)
-    good = tmp_path / "good.md"
-    good.write_text("# summary\nsource_sha256: %s\ndram_bytes_read: 389400320\ndram_bytes_write: 2908160\n" % sha)
-    assert bench.profiled_traffic(str(good), bench.LM_HEAD_SOURCES) == 389400320 + 2908160
-    stale = tmp_path / "stale.md"
-    stale.write_text("source_sha256: 0000000000000000\ndram_bytes_read: 1\ndram_bytes_write: 2\n")
-    assert bench.profiled_traffic(str(stale), bench.LM_HEAD_SOURCES) is None
-    assert bench.profiled_traffic(str(tmp_path / "missing.md"), bench.LM_HEAD_SOURCES) is None
+    for names in (bench.LM_HEAD_SOURCES, bench.GEMM_SOURCES):
+        sha = bench.kernel_source_sha(names)
+        good = tmp_path / "good.json"
+        good.write_text(json.dumps({"source_sha256": sha, "dram_bytes_read": 389400320,
+                                    "dram_bytes_write": 2908160}))
+        assert bench.profiled_traffic(str(good), names) == 389400320 + 2908160
+        stale = tmp_path / "stale.json"
+        stale.write_text(json.dumps({"source_sha256": "0000000000000000", "dram_bytes_read": 1,
+                                     "dram_bytes_write": 2}))
+        assert bench.profiled_traffic(str(stale), names) is None
+        assert bench.profiled_traffic(str(tmp_path / "missing.json"), names) is None
+        broken = tmp_path / "broken.json"
+        broken.write_text("not json")
+        assert bench.profiled_traffic(str(broken), names) is None
 
 
 def test_device_status_fails_the_bench_leg():

@@ -110,3 +110,27 @@ def test_fused_reuses_workspace_and_graphs(w4v_mod, gpu, oracle_mod):
         assert np.array_equal(out.cpu().numpy(), out_o)
     assert torch.all(ws == 0)
     assert w4v_mod.get_status() == 0
+
+
+@pytest.mark.parametrize("B,nd,V", [(8, 15, inputs.V_4B), (5, 24, 2048), (2, 63, 520)])
+def test_fused_batch_invariant(w4v_mod, gpu, oracle_mod, B, nd, V):
+    """W4V_BATCH_INVARIANT with more than 32 rows: the argmax in 32-row blocks,
+    then the acceptance over every block.  Each sequence's tokens equal the
+    tokens of that sequence's rows verified alone, and the accepted lengths
+    and emitted tokens are the oracle's acceptance of them."""
+    K = inputs.H_4B if V == inputs.V_4B else 256
+    M = B * (nd + 1)
+    X = inputs.activations(B + nd, M, K, "binv-x")
+    W, s = inputs.lmhead_weights(B + nd, V, K, "binv")
+    Xd, Wd, sd = to_dev(X, gpu), to_dev(W, gpu), to_dev(s, gpu)
+    alone = np.concatenate([w4v_mod.w8_lmhead_argmax(Xd[b * (nd + 1):(b + 1) * (nd + 1)].contiguous(), Wd, sd)
+                            .cpu().numpy() for b in range(B)])
+    t = alone.reshape(B, nd + 1)
+    d = np.ascontiguousarray(inputs.drafts_alpha(B + nd, t, V, 0.8, "binv").reshape(B, nd), dtype=np.int32)
+    tok, n, out = w4v_mod.w8_lmhead_argmax_accept(Xd, Wd, sd, to_dev(d, gpu), batch_invariant=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(tok.cpu().numpy(), alone)
+    n_o, out_o = oracle_mod.spec_accept(t, d)
+    assert np.array_equal(n.cpu().numpy(), n_o)
+    assert np.array_equal(out.cpu().numpy(), out_o)
+    assert w4v_mod.get_status() == 0

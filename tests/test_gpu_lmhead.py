@@ -17,13 +17,13 @@ from speculative_decoding_verify_w4a16_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-def _run(w4v_mod, gpu, X, W, s, debug=True):
+def _run(w4v_mod, gpu, X, W, s, debug=True, batch_invariant=False):
     M = X.shape[0]
     V = W.shape[0]
     Xd, Wd, sd = to_dev(X, gpu), to_dev(W, gpu), to_dev(s, gpu)
     maxl = torch.empty(M, dtype=torch.float32, device=gpu)
     logits = torch.empty((M, V), dtype=torch.float32, device=gpu) if debug else None
-    tok = w4v_mod.w8_lmhead_argmax(Xd, Wd, sd, maxlogit=maxl, logits=logits)
+    tok = w4v_mod.w8_lmhead_argmax(Xd, Wd, sd, maxlogit=maxl, logits=logits, batch_invariant=batch_invariant)
     torch.cuda.synchronize()
     return tok.cpu().numpy(), maxl.cpu().numpy(), (logits.cpu().numpy() if debug else None)
 
@@ -148,15 +148,21 @@ def test_batch_invariance(w4v_mod, gpu):
         assert np.array_equal(tok, tok32[:m]), m
 
 
-def test_batch_invariance_batched_verify(w4v_mod, gpu):
-    """The batched verify of 8 sequences x 16 positions (128 rows in one
-    launch) gives every row the logits and token of the same row verified
-    alone (16 rows) and decoded alone (1 row), bit for bit, so batching never
-    changes an accepted token."""
+def test_batch_invariance_batched_verify(w4v_mod, gpu, oracle_mod):
+    """With W4V_BATCH_INVARIANT the batched verify of 8 sequences x 16
+    positions (128 rows in one call) gives every row the logits and token of
+    the same row verified alone (16 rows) and decoded alone (1 row), bit for
+    bit, so batching never changes an accepted token.  Without the flag the
+    128 rows run in one launch that sums each logit in another order: every
+    logit still within the fp32 bound of the oracle."""
     K, V = 2560, 8192
     X = inputs.activations(78, 128, K, "inv128")
     W, s = inputs.lmhead_weights(78, V, K, "inv128")
-    tok128, _, L128 = _run(w4v_mod, gpu, X, W, s)
+    _, _, Lfast = _run(w4v_mod, gpu, X, W, s)
+    r = np.random.default_rng(78)
+    vs = np.sort(r.choice(V, 600, replace=False))
+    assert np.all(np.abs(Lfast[:, vs] - oracle_mod.lmhead_logits(X, W[vs], s[vs])) <= logit_bound(X, W[vs], s[vs]))
+    tok128, _, L128 = _run(w4v_mod, gpu, X, W, s, batch_invariant=True)
     for b in range(8):
         tok, _, L = _run(w4v_mod, gpu, X[16 * b:16 * b + 16], W, s)
         assert np.array_equal(L, L128[16 * b:16 * b + 16]), b

@@ -48,8 +48,11 @@ class GpuToy:
         self.W8, self.s8 = dev(W8), dev(s8)
 
     def gemm(self, x16, w):
+        # more than 32 rows (several sequences' verify blocks) in 32-row blocks,
+        # so that every row is computed as it would be alone
         packed, s, N = w
-        out = self.w4v.w4a16_gemm(torch.from_numpy(np.ascontiguousarray(x16)).to(self.gpu), packed, s, N)
+        out = self.w4v.w4a16_gemm(torch.from_numpy(np.ascontiguousarray(x16)).to(self.gpu), packed, s, N,
+                                  batch_invariant=True)
         return out.cpu().numpy().astype(np.float64)
 
     def inputs_at(self, tokens, p0, T):
@@ -58,19 +61,22 @@ class GpuToy:
         pos = np.arange(p0, p0 + T)
         return emb[pos] + csum[pos] / (pos[:, None] + 1.0)
 
-    def gdn_inputs(self, h):
-        T = h.shape[0]
+    def gdn_inputs(self, h, B=1):
+        """The recurrence's inputs for B sequences' blocks of T positions each
+        (h holds the B*T rows one block after the other)."""
+        T = h.shape[0] // B
         r = _rms(h).astype(np.float16)
         qkv = self.gemm(r, self.qkv)
-        q = qkv[:, :H].reshape(T, HEADS, D)
-        k = qkv[:, H:2 * H].reshape(T, HEADS, D)
-        v = qkv[:, 2 * H:].reshape(T, HEADS, D)
+        q = qkv[:, :H].reshape(B * T, HEADS, D)
+        k = qkv[:, H:2 * H].reshape(B * T, HEADS, D)
+        v = qkv[:, 2 * H:].reshape(B * T, HEADS, D)
         q = q / np.linalg.norm(q, axis=-1, keepdims=True)
         k = k / np.linalg.norm(k, axis=-1, keepdims=True)
         rd = r.astype(np.float64)
         alpha = 1.0 / (1.0 + np.exp(-(2.0 + rd @ self.wa.T)))
         beta = 1.0 / (1.0 + np.exp(-(rd @ self.wb.T)))
-        dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a[None].astype(dt))).to(self.gpu)
+        dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a.reshape(B, T, *a.shape[1:]).astype(dt))).to(
+            self.gpu)
         return (dev(q, np.float16), dev(k, np.float16), dev(v, np.float16),
                 dev(alpha, np.float32), dev(beta, np.float32))
 
@@ -194,3 +200,64 @@ def test_commit_all_corrupts_the_recurrent_state(w4v_mod, gpu):
     toy.commit = lambda S, gin, n: orig_commit(S, gin, 15)   # planted: always all K+1 positions
     got, _ = toy.spec(prompt, 24, 15, lambda ctx, K: [int(x) for x in rng.integers(0, V, K)])
     assert got != want
+
+
+def spec_batched(toy, prompts, n_new, K, drafter):
+    """Speculative decoding of several sequences at once: one verify pass over
+    every sequence's block of K+1 positions (B*(K+1) rows in each GEMM, the
+    recurrent state of all B sequences, the lm_head argmax with each
+    sequence's acceptance in one call), all in batch-invariant mode."""
+    w4v, gpu = toy.w4v, toy.gpu
+    B, T = len(prompts), K + 1
+    ctxs = [list(p) for p in prompts]
+    S = torch.cat([toy.fresh_state(c) for c in ctxs], dim=0)
+    outs = [[] for _ in range(B)]
+    while min(len(o) for o in outs) < n_new:
+        d = np.stack([np.asarray(drafter(b, ctxs[b], K), np.int32) for b in range(B)])
+        h = np.concatenate([toy.inputs_at(ctxs[b] + [int(x) if x >= 0 else 0 for x in d[b]], len(ctxs[b]) - 1, T)
+                            for b in range(B)])
+        q, k, v, a, be = toy.gdn_inputs(h, B)
+        o = w4v.gdn_verify(S, q, k, v, a, be)
+        h = h + toy.gemm(o.cpu().numpy().reshape(B * T, H), toy.o)
+        for (w_gu, w_d) in toy.layers:
+            gu = toy.gemm(_rms(h).astype(np.float16), w_gu)
+            act = (gu[:, :H] / (1.0 + np.exp(-gu[:, :H]))) * gu[:, H:]
+            h = h + toy.gemm(act.astype(np.float16), w_d)
+        X = torch.from_numpy(_rms(h).astype(np.float16)).to(gpu)
+        _, n, tok = w4v.w8_lmhead_argmax_accept(X, toy.W8, toy.s8, torch.from_numpy(d).to(gpu),
+                                                batch_invariant=True)
+        w4v.gdn_commit(S, k, v, a, be, n)              # each sequence keeps positions 0..n[b]
+        n, tok = n.cpu().numpy(), tok.cpu().numpy()
+        for b in range(B):
+            emitted = [int(x) for x in tok[b, : n[b] + 1]]
+            ctxs[b].extend(emitted)
+            outs[b].extend(emitted)
+    return [o[:n_new] for o in outs]
+
+
+def test_batched_spec_equals_greedy_through_the_kernels(w4v_mod, gpu):
+    """8 sequences verified together, 16 positions each (128 rows per GEMM and
+    in the lm_head, one recurrent state per sequence): every sequence emits
+    exactly its own one-position greedy tokens, for random drafts and for
+    drafts that follow the greedy continuation up to a seeded cut."""
+    toy = GpuToy(w4v_mod, gpu, 34)
+    B, n_new, K = 8, 20, 15
+    prompts = [inputs.random_tokens(800 + b, 4, V) for b in range(B)]
+    want = [toy.greedy(p, n_new) for p in prompts]
+    rng = np.random.default_rng(34)
+
+    def random_drafts(b, ctx, K):
+        return [int(x) for x in rng.integers(0, V, K)]
+
+    def perfect_then_wrong(b, ctx, K):
+        # (a sequence already past n_new tokens, waiting for the others, gets zeros)
+        done = len(ctx) - len(prompts[b])
+        good = (want[b] + [0] * (done + K + 1))[done:done + K]
+        cut = int(rng.integers(0, K + 1))
+        return good[:cut] + [(g + 1) % V for g in good[cut:]]
+
+    for name, drafter in (("random", random_drafts), ("perfect_then_wrong", perfect_then_wrong)):
+        got = spec_batched(toy, prompts, n_new, K, drafter)
+        for b in range(B):
+            assert got[b] == want[b], (name, b)
+    assert w4v_mod.get_status() == 0
