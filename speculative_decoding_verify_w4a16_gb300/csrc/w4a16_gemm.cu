@@ -150,6 +150,7 @@ struct Layout {
     static constexpr int kMisc = kZro + kDqWarps * kRing * 32;     // group-128 zero slots from kZro
     static_assert(kMaxStages * kFSclSlotBytes <= kMisc - kScl, "group-32 stage scales fit the metadata region");
     static constexpr int kSst = kMisc + 128;                        // stage scale ring (128-byte aligned)
+    static_assert(kMisc % 16 == 0, "misc words hold 8-byte fields");
     static constexpr int kFixed = kSst + kSclSlots * kSclSlotBytes;
     static_assert(kMaxStages * kFZroSlotBytes <= kSclSlots * kSclSlotBytes, "group-32 stage zeros fit");
     static_assert(kMaxStages * kZroSlotBytes <= kMisc - kZro, "group-128 stage zeros fit");
@@ -353,7 +354,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
     auto sfull = [&](int b) { return drain_bar + 8u * (1 + b); };               // a stage's scales landed
     auto sempty = [&](int b) { return drain_bar + 8u * (1 + kSclSlots + b); };  // the drain has read them
     const uint32_t sst = base_s + fixed_off + L::kSst;
-    // [0] tmem base, [1] abort flag, [2..3] pending tile + 1 per slot, [4..5] last-arriver flags
+    // [0] tmem base, [1] abort flag, [2..3] pending tile + 1 per slot, [4..5] last-arriver flags,
+    // [8..27] the pending tiles themselves (PendTile, one per slot)
     uint32_t *misc = reinterpret_cast<uint32_t *>(base + fixed_off + L::kMisc);
 
     const int warp = threadIdx.x >> 5;
@@ -447,6 +449,15 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         int nP, N, T;
         __half *C;
     };
+    // A split tile this CTA published a partial of, as the drain saw it when
+    // it flushed (the fix-up then needs no second look at the problem table),
+    // with the CTAs contributing to it.
+    struct PendTile {
+        TileRef tr;
+        int cf, cl;
+    };
+    static_assert(2 * sizeof(PendTile) <= 20 * sizeof(uint32_t), "pending tiles fit the misc words");
+    PendTile *pend = reinterpret_cast<PendTile *>(misc + 8);
     auto tile_ref = [&](int pi, int t) -> TileRef {
         if constexpr (kG) {
             const GroupProb &g = p.probs[pi];
@@ -863,9 +874,9 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                 }
             if (!drain_sync()) return false;
             if (dr == 0 && lane == 0) {
-                misc[2 + slot] = uint32_t(t) + 1u;
-                misc[6 + slot] = uint32_t(pi);
                 pend_prev[slot] = atom_add_acq_rel_gpu(&p.tile_cnt[tr.T], 1u);
+                misc[2 + slot] = uint32_t(t) + 1u;
+                pend[slot] = PendTile{tr, split_owner(t0u, p.U, p.P), split_owner(t1u - 1, p.U, p.P)};
             }
             return true;
         };
@@ -876,14 +887,11 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         auto mark_last = [&]() {
             if (dr == 0 && lane == 0) {
                 for (int sl = 0; sl < 2; ++sl) {
-                    const uint32_t tp = misc[2 + sl];
                     uint32_t last = 0u;
-                    if (tp != 0u) {
-                        const TileRef tr = tile_ref(int(misc[6 + sl]), int(tp - 1u));
-                        const int cf = split_owner(tr.t0u, p.U, p.P);
-                        const int cl = split_owner(tr.t0u + tr.nP - 1, p.U, p.P);
-                        last = pend_prev[sl] == uint32_t(cl - cf) ? 1u : 0u;
-                        if (last) p.tile_cnt[tr.T] = 0u;
+                    if (misc[2 + sl] != 0u) {
+                        const PendTile &pt = pend[sl];
+                        last = pend_prev[sl] == uint32_t(pt.cl - pt.cf) ? 1u : 0u;
+                        if (last) p.tile_cnt[pt.tr.T] = 0u;
                     }
                     misc[4 + sl] = last;
                 }
@@ -1026,10 +1034,10 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         for (int sl = 0; sl < 2; ++sl) {
             if (!misc[4 + sl]) continue;
             const int t = int(misc[2 + sl]) - 1;
-            const TileRef tr = tile_ref(int(misc[6 + sl]), t);
+            const TileRef tr = pend[sl].tr;
             const long long t0u = tr.t0u;
-            const int cf = split_owner(t0u, p.U, p.P);
-            const int cl = split_owner(t0u + tr.nP - 1, p.U, p.P);
+            const int cf = pend[sl].cf;
+            const int cl = pend[sl].cl;
             for (int e4 = threadIdx.x; e4 < kPart / 4; e4 += kThreads) {   // float4 of the [m][128] tile
                 const int m = e4 / (kTileN / 4);
                 const int n0 = t * kTileN + 4 * (e4 % (kTileN / 4));
