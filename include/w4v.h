@@ -69,7 +69,10 @@ const char *w4v_status_string(w4v_status status);
  * tiny kernel, so that a library built for another architecture fails here
  * rather than at the first real launch ("DFlash K=15 for Qwen3.5-4B on a
  * single A10G", section "What transfers": build for the card you run on).
- * Idempotent per device; every entry point calls it implicitly. */
+ * Idempotent per device; every entry point calls it implicitly.  What it
+ * finds (the SM count, the device status word's address) is kept per device
+ * for the life of the process, so a process that resets a device
+ * (cudaDeviceReset) must be restarted before it calls the library again. */
 w4v_status w4v_init(void);
 
 /* Synchronizes `stream`, then returns and clears the device status word of
@@ -259,10 +262,19 @@ w4v_status w8_lmhead_argmax_ex(const uint16_t *X, const int8_t *W, const uint16_
  * library keeps until the process exits.
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  *     call.  It clears the scratch with an asynchronous memset on `stream`
- *     before each launch.
+ *     before each launch.  That memset sits between the previous kernel on
+ *     the stream and the lm_head, so the lm_head's programmatic launch no
+ *     longer overlaps its set-up with the previous kernel's end (the
+ *     workspace entry keeps that overlap; the kernel itself leaves the
+ *     scratch cleared on success, and the memset covers a call that gave
+ *     up a bounded wait).
  *   - The first call on a device looks up that device's address of the
- *     array (cudaGetSymbolAddress with the device current); make that first
- *     call outside any stream capture.
+ *     array (cudaGetSymbolAddress with the device current) and keeps it for
+ *     the life of the process; make that first call outside any stream
+ *     capture.  After cudaDeviceReset (or anything else that unloads the
+ *     library's module from a device) the kept address is stale: restart
+ *     the process before calling this entry point again, as for the
+ *     library's other per-device state (w4v_init).
  *   - Every call on a device shares the one array: calls that overlap on the
  *     GPU (different streams without ordering between them) race and give
  *     wrong tokens.  Serialize them, or use w8_lmhead_argmax with a

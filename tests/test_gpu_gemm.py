@@ -178,12 +178,13 @@ def test_prefill_layer_projection_sampled(w4v_mod, gpu, oracle_mod, proj, M):
     assert gemm_rel_err(C[rows, cols], R) <= GEMM_TOL
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 2560, 2560), (2048, 2560, 9728)])
+@pytest.mark.parametrize("M,N,K", [(300, 2560, 2560), (2048, 2560, 9728), (2048, 2560, 2560)])
 def test_prefill_split_tiles_deterministic_and_clean(w4v_mod, gpu, oracle_mod, M, N, K):
     """Shapes whose last wave is mostly empty split the k range of tiles
-    between CTAs (fp32 partials added by the last contributor in CTA order):
-    repeated calls on one workspace are bit-identical, the arrival counters
-    are left at zero, and sampled outputs match the oracle."""
+    between CTAs (fp32 partials added by the last contributor in CTA order;
+    o and down at 2048 rows among them): repeated calls on one workspace are
+    bit-identical, the arrival counters are left at zero, and sampled
+    outputs match the oracle."""
     A = inputs.activations(M, M, K, "split")
     q = inputs.w4_codes(M, N, K, "split")
     s = inputs.w4_scales(M, N, K, "split")
