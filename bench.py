@@ -73,8 +73,42 @@ def load_peaks():
                 "source": "fallback"}
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (SM clock, its maximum, and the
+    active clock event reasons); None where the library is missing."""
+    SM = 1                                                  # NVML_CLOCK_SM
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, index):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        mx = ctypes.c_uint()
+        self.max_mhz = mx.value if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM, ctypes.byref(mx)) == 0 else None
+
+    def sample(self):
+        c = self.c
+        mhz, rs = c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, c.byref(mhz)) != 0:
+            return None
+        get = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        if get(self.h, c.byref(rs)) != 0:
+            return None
+        return [str(mhz.value), str(self.max_mhz), ""] + \
+            ["Active" if rs.value & bit else "Not Active" for bit in (0x8, 0x40, 0x20, 0x4)]
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    """SM clocks and throttle reasons sampled during the timed region: NVML
+    every millisecond (the region can be a fraction of a second), else
+    nvidia-smi every 200 ms.  The first sample is taken just before the
+    timed region starts and the last just after it ends."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -82,24 +116,38 @@ class ClockSampler:
     def __init__(self, index=0):
         self.index = index
         self.rows = []
+        self.source = "nvidia-smi"
         self._stop = threading.Event()
+        self._ready = threading.Event()
         self._thr = None
+        try:
+            self._nvml = _Nvml(index)
+            self.source = "nvml"
+        except Exception:
+            self._nvml = None
 
     def _run(self):
         while not self._stop.is_set():
             try:
-                out = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                                      "--format=csv,noheader,nounits"], capture_output=True, text=True,
-                                     timeout=5).stdout.strip()
-                if out:
-                    self.rows.append([x.strip() for x in out.split(",")])
+                if self._nvml is not None:
+                    row = self._nvml.sample()
+                    if row:
+                        self.rows.append(row)
+                else:
+                    out = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                                         timeout=5).stdout.strip()
+                    if out:
+                        self.rows.append([x.strip() for x in out.split(",")])
             except Exception:
                 pass
-            self._stop.wait(0.2)
+            self._ready.set()
+            self._stop.wait(0.001 if self._nvml is not None else 0.2)
 
     def __enter__(self):
         self._thr = threading.Thread(target=self._run, daemon=True)
         self._thr.start()
+        self._ready.wait(timeout=10)
         return self
 
     def __exit__(self, *a):
@@ -115,7 +163,7 @@ class ClockSampler:
         reasons = sorted({names[i] for r in self.rows for i in range(4)
                           if len(r) > 3 + i and r[3 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.rows)}
+                "reasons": reasons, "samples": len(self.rows), "source": self.source}
 
 
 # --------------------------------------------------------------------- GPU arm
@@ -914,8 +962,12 @@ def cpu_baseline(step):
     import oracle
     oracle.build()
     threads = oracle.num_threads()
+    # the full layer set, repeated for about 10 s of CPU work (at most 64 times)
+    reps, nbytes = 0, 0
     t0 = time.perf_counter()
-    nbytes = oracle_gemm(step.host, 1.0)
+    while reps < 64 and (reps == 0 or time.perf_counter() - t0 < 10.0):
+        nbytes += oracle_gemm(step.host, 1.0)
+        reps += 1
     dt = time.perf_counter() - t0
     t0 = time.perf_counter()
     nbytes_step = oracle_step(step.host, 1.0)
@@ -942,7 +994,7 @@ def cpu_baseline(step):
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle", "seconds": round(dt, 2),
             "sample": "the full cfg1 W4A16 layer set (4 projections, M=16), double precision, OpenMP over "
-                      "output rows",
+                      "output rows, %d times back to back" % reps, "repetitions": reps,
             "affinity_cores": _cores(), "nproc": os.cpu_count(),
             "whole_step": {"GB/s": round(nbytes_step / dt_step / 1e9, 4), "seconds": round(dt_step, 2),
                            "sample": "layer set + lm_head + argmax + acceptance"},
