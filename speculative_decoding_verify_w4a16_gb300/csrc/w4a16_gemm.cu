@@ -318,7 +318,10 @@ struct StageRing {
 // one after the other and split over the CTAs as one stream-K list; each
 // role follows the problem of the unit it is on (its weights, tensor maps,
 // output), so one pipeline and one ramp serve the whole list.
-template <int NBLK, bool kFold, bool kG>
+// kZ (group size 128 only): a zero-point table is given; without one the
+// zero point 8 is a compile-time constant of the dequantization (its
+// offsets become immediates: ~5 % of the unit period).
+template <int NBLK, bool kFold, bool kG, bool kZ = false>
 __global__ void __launch_bounds__(kThreads, 1)
 w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap smap,
                     const __grid_constant__ CUtensorMap zmap, const Args p) {
@@ -749,18 +752,21 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                 const int f = f0 + jj;
                 const int ng = min(kUnitGroups, sw.G - 2 * (sw.p + jj));
                 const int slot = f % kASlots;
-                const int sbw = (has_zeros || kFold) ? pr_sbox_w(sw.pi) : 0;
+                const int sbw = (kZ || kFold) ? pr_sbox_w(sw.pi) : 0;
                 const uint32_t g0p = base_s + s * L::kStage + L::kW + (kUnitGroups * jj) * kGroupBytes;
                 const uint32_t g1p = g0p + kGroupBytes;
                 const uint32_t col = tmem + lane_base + slot * kASlotCols;
                 // group gg: half 0 into ra, half 1 into rb; each store
-                // overlaps the next half's arithmetic (one copy of the
-                // dequant code per register set keeps the kernel small)
+                // overlaps the next half's arithmetic.  Both groups are
+                // unrolled, so the second group's loads and arithmetic
+                // schedule against the first's tail (~14 % of the unit
+                // period against a loop of one group per trip).
                 bool aborted = false;
-#pragma unroll 1
-                for (int gg = 0; gg < ng; ++gg) {
+#pragma unroll
+                for (int gg = 0; gg < kUnitGroups; ++gg) {
+                    if (gg >= ng) break;
                     const uint32_t gp = gg == 0 ? g0p : g1p;
-                    const uint32_t z = (!kFold && has_zeros) ? zero_read(s, kUnitGroups * jj + gg, sbw) : 8u;
+                    const uint32_t z = (!kFold && kZ) ? zero_read(s, kUnitGroups * jj + gg, sbw) : 8u;
                     uint32_t zz = 0u, ss0 = 0u, ss1 = 0u;
                     if constexpr (kFold) {
                         fold_read(s, kUnitGroups * jj + gg, sbw, zz, ss0, ss1);
@@ -1126,13 +1132,13 @@ int pick_cluster(int n_tiles, int n_pairs, int sm_count) {
     return 0;
 }
 
-template <int NBLK, bool kFold, bool kG = false>
+template <int NBLK, bool kFold, bool kG = false, bool kZ = false>
 w4v_status configure() {
     static int configured_for = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_for != dev) {
-        if (cudaFuncSetAttribute(w4a16_decode_kernel<NBLK, kFold, kG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(w4a16_decode_kernel<NBLK, kFold, kG, kZ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kMaxSmem) != cudaSuccess) {
             cudaGetLastError();
             return W4V_ERR_CUDA;
@@ -1142,17 +1148,17 @@ w4v_status configure() {
     return W4V_OK;
 }
 
-template <int NBLK, bool kFold, bool kG = false>
+template <int NBLK, bool kFold, bool kG = false, bool kZ = false>
 w4v_status launch(const CUtensorMap &xmap, const CUtensorMap &smap, const CUtensorMap &zmap, Args &a, int cluster,
                   cudaStream_t stream) {
     using L = Layout<NBLK>;
-    w4v_status st = configure<NBLK, kFold, kG>();
+    w4v_status st = configure<NBLK, kFold, kG, kZ>();
     if (st != W4V_OK) return st;
     a.cluster = cluster;
     a.stages = L::kStagesMax;
     if (cluster > 0) a.P = a.n_tiles * cluster;
     const size_t smem = size_t(L::bytes(a.stages));
-    if (launch_pdl_cluster(w4a16_decode_kernel<NBLK, kFold, kG>, dim3(a.P), dim3(kThreads), smem, stream, cluster,
+    if (launch_pdl_cluster(w4a16_decode_kernel<NBLK, kFold, kG, kZ>, dim3(a.P), dim3(kThreads), smem, stream, cluster,
                            xmap, smap, zmap, a) !=
         cudaSuccess) {
         cudaGetLastError();
@@ -1238,6 +1244,9 @@ w4v_status launch_w4a16_decode(const uint16_t *A, const void *Bq, const uint16_t
     if (group == 32)
         return nblk == 1 ? launch<1, true>(xmap, smap, zmap, a, cluster, stream)
                          : launch<2, true>(xmap, smap, zmap, a, cluster, stream);
+    if (zeros != nullptr)
+        return nblk == 1 ? launch<1, false, false, true>(xmap, smap, zmap, a, cluster, stream)
+                         : launch<2, false, false, true>(xmap, smap, zmap, a, cluster, stream);
     return nblk == 1 ? launch<1, false>(xmap, smap, zmap, a, cluster, stream)
                      : launch<2, false>(xmap, smap, zmap, a, cluster, stream);
 }
@@ -1357,6 +1366,9 @@ w4v_status launch_w4a16_grouped(const w4a16_grouped_t &h, void *ws, bool static_
     if (h.group == 32)
         return nblk == 1 ? launch<1, true, true>(unused, unused, unused, a, 0, stream)
                          : launch<2, true, true>(unused, unused, unused, a, 0, stream);
+    if (h.has_zeros)
+        return nblk == 1 ? launch<1, false, true, true>(unused, unused, unused, a, 0, stream)
+                         : launch<2, false, true, true>(unused, unused, unused, a, 0, stream);
     return nblk == 1 ? launch<1, false, true>(unused, unused, unused, a, 0, stream)
                      : launch<2, false, true>(unused, unused, unused, a, 0, stream);
 }
