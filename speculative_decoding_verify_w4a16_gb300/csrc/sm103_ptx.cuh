@@ -522,6 +522,19 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 
 
 // ----------------------------------------------------------- int -> fp16 bits
+// (a0, a1) += s * (d0, d1) as fp32 bit patterns, in one packed instruction
+// (sm_100 and later); each lane rounds once, like fmaf.
+__device__ __forceinline__ void fma_f32x2(float &a0, float &a1, float s, uint32_t d0, uint32_t d1) {
+    asm("{\n\t.reg .b64 A, D, S;\n\t"
+        "mov.b64 A, {%0, %1};\n\t"
+        "mov.b64 D, {%3, %4};\n\t"
+        "mov.b64 S, {%2, %2};\n\t"
+        "fma.rn.f32x2 A, S, D, A;\n\t"
+        "mov.b64 {%0, %1}, A;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(s), "r"(d0), "r"(d1));
+}
+
 // The fp16 pattern 0x6400 is 1024 with a unit last place, so OR-ing an
 // integer 0 <= x < 1024 into its low bits gives exactly 1024 + x.  Both
 // halves of a 32-bit word are handled at once.

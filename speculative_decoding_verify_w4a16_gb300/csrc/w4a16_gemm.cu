@@ -955,15 +955,17 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                 s0 = __half2float(__ushort_as_half(lds_u16(row0 + uint32_t(2 * dj) * pitch)));
                 if (ng > 1) s1 = __half2float(__ushort_as_half(lds_u16(row0 + uint32_t(2 * dj + 1) * pitch)));
             }
+            // two lanes of fp32 per instruction (each lane rounds like fmaf)
 #pragma unroll
             for (int b = 0; b < NBLK; ++b)
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[b][j] = fmaf(s0, __uint_as_float(d[b][j]), acc[b][j]);
+                for (int j = 0; j < 16; j += 2) fma_f32x2(acc[b][j], acc[b][j + 1], s0, d[b][j], d[b][j + 1]);
             if (ng > 1) {
 #pragma unroll
                 for (int b = 0; b < NBLK; ++b)
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc[b][j] = fmaf(s1, __uint_as_float(d[NBLK + b][j]), acc[b][j]);
+                    for (int j = 0; j < 16; j += 2)
+                        fma_f32x2(acc[b][j], acc[b][j + 1], s1, d[NBLK + b][j], d[NBLK + b][j + 1]);
             }
             if (++dj == dw.size()) {             // the stage's last unit: its scales are read
                 if (!kFold) {
