@@ -63,11 +63,16 @@ constexpr int kWarps = kWarpDq0 + kDqWarps;
 constexpr int kThreads = 32 * kWarps;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAcol0 = 0;
-constexpr int kStageChunks = 2;             // k-chunks per stage = per unit
-constexpr uint32_t kASlotCols = kStageChunks * 64;
+// k-chunks per stage = per unit: two up to 32 rows; one beyond, where each
+// chunk's activations (64 rows or more x 128 k) are as large as its weights,
+// so that four shorter stages fit instead of two long ones (a stage is
+// held until its MMAs complete, and with two the ring stalled on reloads).
+__host__ __device__ constexpr int stage_chunks(int nblk) { return nblk >= 4 ? 1 : 2; }
 
 template <int NBLK>
 struct Layout {
+    static constexpr int kStageChunks = stage_chunks(NBLK);
+    static constexpr uint32_t kASlotCols = kStageChunks * 64;
     static constexpr int kRows = 16 * NBLK;
     static constexpr int kActBox = kRows * 128;         // one 64-k block, swizzled
     static constexpr int kAct = 2 * kStageChunks * kActBox;
@@ -85,8 +90,9 @@ struct Layout {
     // out [acc][block][16].
     static constexpr bool kWide = NBLK >= 2;
     static constexpr uint32_t kDSet = kAcc * 16 * NBLK;
-    // A slots: as many 128-column units as fit beside two accumulator sets
-    static constexpr int kASlots = NBLK == 1 ? 3 : 2;
+    // A slots: as many units as fit beside two accumulator sets
+    static constexpr int kASlots = (kTmemCols - kDSets * kDSet) / kASlotCols > 4
+                                       ? 4 : int((kTmemCols - kDSets * kDSet) / kASlotCols);
     static constexpr uint32_t kDcol0 = kASlots * kASlotCols;
     static constexpr int kBar = kStages * kStage;
     static constexpr int kNumBars = 2 * kStages + 2 * kASlots + 4 + 2;
@@ -98,12 +104,13 @@ struct Layout {
     static_assert(kBytes <= 227 * 1024, "shared memory plan");
 };
 
-// Stages: runs of at most kStageChunks consecutive k-chunks of one tile.
+// Stages: runs of at most SC consecutive k-chunks of one tile.
+template <int SC>
 struct ChunkWalk {
     int j, c, nch, ntiles;
     __device__ ChunkWalk(int n_chunks, int tiles) : j(0), c(0), nch(n_chunks), ntiles(tiles) {}
     __device__ bool more() const { return j < ntiles; }
-    __device__ int size() const { return min(kStageChunks, nch - c); }
+    __device__ int size() const { return min(SC, nch - c); }
     __device__ void next(int ng) {
         c += ng;
         if (c == nch) {
@@ -214,7 +221,7 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
             prefetch_tensormap(&xmap);
             // Only L2 is warmed before the dependency wait (L2 is the point
             // of coherence, so this is safe whatever the previous kernel writes).
-            ChunkWalk pw(p.n_chunks, ntiles);
+            ChunkWalk<L::kStageChunks> pw(p.n_chunks, ntiles);
             for (int st = 0; st < S && pw.more(); ++st) {
                 prefetch_l2_3d(&wmap, 0, (tb + pw.j) * kTileV, pw.c);
                 pw.next(pw.size());
@@ -225,13 +232,13 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
             const uint64_t pol_w = l2_policy_evict_first();
             const uint64_t pol_x = l2_policy_evict_last();
             int issued = 0;
-            ChunkWalk cw(p.n_chunks, ntiles);
+            ChunkWalk<L::kStageChunks> cw(p.n_chunks, ntiles);
             for (int st = 0; cw.more(); ++st) {
                 const int ng = cw.size();
                 const int s = st % S;
                 if (st >= S && !mbar_wait(empty(s), ((st / S) - 1) & 1, ab)) break;
                 const uint32_t sa = base_s + s * L::kStage;
-                mbar_arrive_expect_tx(full(s), kStageChunks * kWBytes + L::kAct);
+                mbar_arrive_expect_tx(full(s), L::kStageChunks * kWBytes + L::kAct);
                 tma_load_3d(sa + L::kW, &wmap, 0, (tb + cw.j) * kTileV, cw.c, full(s), pol_w);
                 tma_load_3d(sa, &xmap, 0, 0, 2 * cw.c, full(s), pol_x);
                 ++issued;
@@ -251,7 +258,7 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
             const int me = warp - kWarpIss0;
             constexpr uint32_t idesc = idesc_f16_f32(128, 16);
             constexpr uint32_t idesc_wide = idesc_f16_f32(128, 16 * NBLK);
-            ChunkWalk cw(p.n_chunks, ntiles);
+            ChunkWalk<L::kStageChunks> cw(p.n_chunks, ntiles);
             bool ok = true;
             for (int st = 0; cw.more() && ok; ++st) {      // unit st = stage st
                 const int ng = cw.size();
@@ -276,7 +283,7 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
                             // accumulator a belongs to issuer a: all NBLK blocks in one MMA
                             if (a % kIssuers != me) continue;
                             const uint32_t baddr = act + (kk >> 2) * L::kActBox + (kk & 3) * 32;
-                            mma_f16_ts_lane0(dset + a * (16 * NBLK), tmem + kAcol0 + slot * kASlotCols + jj * 64 + 8 * kk,
+                            mma_f16_ts_lane0(dset + a * (16 * NBLK), tmem + kAcol0 + slot * L::kASlotCols + jj * 64 + 8 * kk,
                                        sdesc_sw128(baddr), idesc_wide, (c > 0 || kk >= L::kAcc) ? 1u : 0u);
                         } else {
 #pragma unroll
@@ -284,7 +291,7 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
                                 if ((a * NBLK + b) % kIssuers != me) continue;
                                 const uint32_t baddr = act + (kk >> 2) * L::kActBox + b * 2048 + (kk & 3) * 32;
                                 mma_f16_ts_lane0(dset + (b * L::kAcc + a) * 16,
-                                           tmem + kAcol0 + slot * kASlotCols + jj * 64 + 8 * kk, sdesc_sw128(baddr),
+                                           tmem + kAcol0 + slot * L::kASlotCols + jj * 64 + 8 * kk, sdesc_sw128(baddr),
                                            idesc, (c > 0 || kk >= L::kAcc) ? 1u : 0u);
                             }
                         }
@@ -337,7 +344,7 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
             if (lane == 0) mbar_arrive(empty(s));
         };
 
-        ChunkWalk cw(p.n_chunks, ntiles);
+        ChunkWalk<L::kStageChunks> cw(p.n_chunks, ntiles);
         uint32_t ra[32], rb[32];
         for (int st = 0; cw.more(); ++st) {
             const int ng = cw.size();
@@ -348,7 +355,7 @@ w8_lmhead_argmax_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_c
             if (!warp_wait(full(s), (st / S) & 1, ab)) break;
             const uint32_t c0p = base_s + s * L::kStage + L::kW;
             const uint32_t c1p = c0p + kWBytes;
-            const uint32_t col = tmem + lane_base + kAcol0 + slot * kASlotCols;
+            const uint32_t col = tmem + lane_base + kAcol0 + slot * L::kASlotCols;
             dequant(c0p, 0, ra);
             if (st >= kASlots && !warp_wait(aempty(slot), ((st / kASlots) - 1) & 1, ab)) {
                 release(s);
@@ -603,10 +610,10 @@ w4v_status launch_w8_lmhead_argmax(const uint16_t *X, const int8_t *W, const uin
     a.P = std::min(std::min(info->sm_count, kMaxCtas), a.n_tiles);
     CUtensorMap xmap, wmap;
     st = encode_tmap_kblocks(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, X, uint64_t(K), uint64_t(M), 64, 16 * nblk,
-                             2 * kStageChunks, CU_TENSOR_MAP_SWIZZLE_128B);
+                             2 * stage_chunks(nblk), CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != W4V_OK) return st;
     st = encode_tmap_kblocks(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, uint64_t(K), uint64_t(V), kChunk, kTileV,
-                             kStageChunks, CU_TENSOR_MAP_SWIZZLE_128B);
+                             stage_chunks(nblk), CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != W4V_OK) return st;
     switch (nblk) {
         case 1: return launch<1>(xmap, wmap, a, stream);
