@@ -679,9 +679,11 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
 
         // One 64-k step: chunks 2kh, 2kh+1 of the packed group at shared address `grp`,
         // dequantized with zero point z into 32 half2 registers.
-        auto dequant = [&](uint32_t grp, int kh, uint32_t z, uint32_t (&regs)[32]) {
-            const uint4 va = lds128(grp + ((2 * kh) * 128 + r) * 16);
-            const uint4 vb = lds128(grp + ((2 * kh + 1) * 128 + r) * 16);
+        auto load_half = [&](uint32_t grp, int kh, uint4 &va, uint4 &vb) {
+            va = lds128(grp + ((2 * kh) * 128 + r) * 16);
+            vb = lds128(grp + ((2 * kh + 1) * 128 + r) * 16);
+        };
+        auto convert = [&](const uint4 &va, const uint4 &vb, uint32_t z, uint32_t (&regs)[32]) {
             const __half2 zlo = u32_as_h2((0x6400u + z) * 0x10001u);          // 1024 + z
             const __half2 zhi = __float2half2_rn(-(64.f + float(z)));
             const uint32_t words[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
@@ -761,18 +763,27 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                 // unrolled, so the second group's loads and arithmetic
                 // schedule against the first's tail (~14 % of the unit
                 // period against a loop of one group per trip).
-                bool aborted = false;
+                bool aborted = false, released = false;
 #pragma unroll
                 for (int gg = 0; gg < kUnitGroups; ++gg) {
                     if (gg >= ng) break;
                     const uint32_t gp = gg == 0 ? g0p : g1p;
                     const uint32_t z = (!kFold && kZ) ? zero_read(s, kUnitGroups * jj + gg, sbw) : 8u;
                     uint32_t zz = 0u, ss0 = 0u, ss1 = 0u;
+                    // group size 128: both halves' packed words are loaded up
+                    // front, so the shared-memory latency is paid once a group
+                    uint4 h0a, h0b, h1a, h1b;
                     if constexpr (kFold) {
                         fold_read(s, kUnitGroups * jj + gg, sbw, zz, ss0, ss1);
                         dequant_fold(gp, 0, zz, ss0, ss1, ra);
                     } else {
-                        dequant(gp, 0, z, ra);
+                        load_half(gp, 0, h0a, h0b);
+                        load_half(gp, 1, h1a, h1b);
+                        if (gg == ng - 1) {               // last shared-memory read of the stage
+                            release(s);
+                            released = true;
+                        }
+                        convert(h0a, h0b, z, ra);
                     }
                     if (gg == 0) {
                         // the release by unit f - 3: this parity's ((f - 3) / 6)-th on the barrier
@@ -783,11 +794,15 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                         tc_fence_after();
                     }
                     tmem_st_32x32b_x32(col + 64 * gg, ra);
-                    if constexpr (kFold)
+                    if constexpr (kFold) {
                         dequant_fold(gp, 1, zz, ss0, ss1, rb);
-                    else
-                        dequant(gp, 1, z, rb);
-                    if (gg == ng - 1) release(s);     // last shared-memory read of the stage
+                        if (gg == ng - 1) {               // last shared-memory read of the stage
+                            release(s);
+                            released = true;
+                        }
+                    } else {
+                        convert(h1a, h1b, z, rb);
+                    }
                     tmem_st_32x32b_x32(col + 64 * gg + 32, rb);
                     // the group is in tensor memory: the slot's issuer may start on
                     // it while the next group is being dequantized
@@ -799,7 +814,7 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                     if (lane == 0) mbar_arrive(afull(slot, gg));
                 }
                 if (aborted) {
-                    release(s);
+                    if (!released) release(s);
                     break;
                 }
                 // a unit with one group still completes its group-1 barrier
