@@ -931,8 +931,8 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
             const int ng = wd.ng();
             const uint32_t dset = tmem + lane_base + kDcol0 + set * L::kDUnit;
             // accumulators [group][block][16]; group 1 only if the unit has it
-            uint32_t d[kUnitGroups * NBLK][16];
             if constexpr (NBLK == 1) {
+                uint32_t d[kUnitGroups][16];
                 uint32_t d2[32];
                 tmem_ld_32x32b_x32(dset, d2);
                 tc_wait_ld_keep<32>(d2);
@@ -941,46 +941,64 @@ w4a16_decode_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
                     d[0][j] = d2[j];
                     d[1][j] = d2[16 + j];
                 }
-            } else {
-                uint32_t d2[32], d3[32];
-                tmem_ld_32x32b_x32(dset, d2);
-                tmem_ld_32x32b_x32(dset + 32, d3);
-                tc_wait_ld_keep<32>(d2);
-                tc_wait_ld_keep<32>(d3);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    d[0][j] = d2[j];
-                    d[1][j] = d2[16 + j];
-                    d[2][j] = d3[j];
-                    d[3][j] = d3[16 + j];
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dempty(set, (f + DS) % kIssuers));
+                // groups in ascending order, each scaled in fp32 (group size 32:
+                // the weights carry their scales, the sums are added as they are)
+                float s0 = 1.f, s1 = 1.f;
+                if (!kFold) {
+                    const int b = du % kSclSlots;
+                    // once per stage (on an abort the values are never stored)
+                    if (dj == 0) warp_wait(sfull(b), uint32_t(du / kSclSlots) & 1u, ab);
+                    const uint32_t row0 = sst + uint32_t(b * kSclSlotBytes) + srow;
+                    const uint32_t pitch = uint32_t(pr_sbox_w(wd.pi) * 2);
+                    s0 = __half2float(__ushort_as_half(lds_u16(row0 + uint32_t(2 * dj) * pitch)));
+                    if (ng > 1) s1 = __half2float(__ushort_as_half(lds_u16(row0 + uint32_t(2 * dj + 1) * pitch)));
                 }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(dempty(set, (f + DS) % kIssuers));
-            // groups in ascending order, each scaled in fp32 (group size 32:
-            // the weights carry their scales, the sums are added as they are)
-            float s0 = 1.f, s1 = 1.f;
-            if (!kFold) {
-                const int b = du % kSclSlots;
-                // once per stage (on an abort the values are never stored)
-                if (dj == 0) warp_wait(sfull(b), uint32_t(du / kSclSlots) & 1u, ab);
-                const uint32_t row0 = sst + uint32_t(b * kSclSlotBytes) + srow;
-                const uint32_t pitch = uint32_t(pr_sbox_w(wd.pi) * 2);
-                s0 = __half2float(__ushort_as_half(lds_u16(row0 + uint32_t(2 * dj) * pitch)));
-                if (ng > 1) s1 = __half2float(__ushort_as_half(lds_u16(row0 + uint32_t(2 * dj + 1) * pitch)));
-            }
-            // two lanes of fp32 per instruction (each lane rounds like fmaf)
+                // two lanes of fp32 per instruction (each lane rounds like fmaf)
 #pragma unroll
-            for (int b = 0; b < NBLK; ++b)
+                for (int j = 0; j < 16; j += 2) fma_f32x2(acc[0][j], acc[0][j + 1], s0, d[0][j], d[0][j + 1]);
+                if (ng > 1) {
 #pragma unroll
-                for (int j = 0; j < 16; j += 2) fma_f32x2(acc[b][j], acc[b][j + 1], s0, d[b][j], d[b][j + 1]);
-            if (ng > 1) {
+                    for (int j = 0; j < 16; j += 2) fma_f32x2(acc[0][j], acc[0][j + 1], s1, d[1][j], d[1][j + 1]);
+                }
+            } else {
+                // 17..32 rows: one group (both 16-row blocks, 32 words) in
+                // registers at a time beside the 32 sums; the second group is
+                // read after the first is added in (same order per sum)
+                float s0 = 1.f, s1 = 1.f;
+                uint32_t dg[32];
+                tmem_ld_32x32b_x32(dset, dg);
+                if (!kFold) {
+                    const int b = du % kSclSlots;
+                    // once per stage (on an abort the values are never stored)
+                    if (dj == 0) warp_wait(sfull(b), uint32_t(du / kSclSlots) & 1u, ab);
+                    const uint32_t row0 = sst + uint32_t(b * kSclSlotBytes) + srow;
+                    const uint32_t pitch = uint32_t(pr_sbox_w(wd.pi) * 2);
+                    s0 = __half2float(__ushort_as_half(lds_u16(row0 + uint32_t(2 * dj) * pitch)));
+                    if (ng > 1) s1 = __half2float(__ushort_as_half(lds_u16(row0 + uint32_t(2 * dj + 1) * pitch)));
+                }
+                tc_wait_ld_keep<32>(dg);
 #pragma unroll
                 for (int b = 0; b < NBLK; ++b)
 #pragma unroll
                     for (int j = 0; j < 16; j += 2)
-                        fma_f32x2(acc[b][j], acc[b][j + 1], s1, d[NBLK + b][j], d[NBLK + b][j + 1]);
+                        fma_f32x2(acc[b][j], acc[b][j + 1], s0, dg[16 * b + j], dg[16 * b + j + 1]);
+                if (ng > 1) {
+                    tmem_ld_32x32b_x32(dset + 32, dg);
+                    tc_wait_ld_keep<32>(dg);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dempty(set, (f + DS) % kIssuers));
+                if (ng > 1) {
+#pragma unroll
+                    for (int b = 0; b < NBLK; ++b)
+#pragma unroll
+                        for (int j = 0; j < 16; j += 2)
+                            fma_f32x2(acc[b][j], acc[b][j + 1], s1, dg[16 * b + j], dg[16 * b + j + 1]);
+                }
             }
             if (++dj == dw.size()) {             // the stage's last unit: its scales are read
                 if (!kFold) {

@@ -55,7 +55,7 @@ def test_cfg0_lmhead(w4v_mod, gpu, oracle_mod):
 
 @pytest.mark.parametrize("M,K,V", [(1, 256, 1024), (3, 128, 136), (16, 384, 1000), (21, 256, 2048),
                                    (32, 512, 1032), (48, 1280, 296), (64, 256, 520), (100, 128, 4096),
-                                   (128, 640, 3000)])
+                                   (128, 640, 3000), (128, 256, 38408)])
 def test_shapes(w4v_mod, gpu, oracle_mod, M, K, V):
     X = inputs.activations(M, M, K, "x")
     W, s = inputs.lmhead_weights(V, V, K)
