@@ -23,18 +23,26 @@
 //     two CTAs per SM with N = 128 tiles reached ~50%.
 //   * Per 128-k group: one 8 KB bulk copy of packed int4 and one 64 KB 3-D
 //     TMA of the activation slice (128-byte swizzle), three stages.
-//   * Four dequant warps turn a group into fp16 s * (q - z) and write it into
+//   * Two sets of four dequant warps, taking alternate groups (set s always
+//     fills A slot s), turn a group into fp16 s * (q - z) and write it into
 //     tensor memory (64-column tcgen05.st); one thread issues eight
 //     tcgen05.mma.kind::f16 per group with A = weights from TMEM (M = 128),
 //     B = activations from shared memory (N = 256), D in TMEM.
 //   * Four epilogue warps read the finished tile (32-column tcgen05.ld),
 //     round to fp16 and store C.
-//   * When the last wave of tiles would leave most SMs idle and K is long
-//     enough to pay for it (down at 2048 and 8192 rows), each tile's k range
-//     is split in two halves done by two CTAs at the same time: each writes
-//     its fp32 partial tile to the workspace, and the second to arrive
-//     (acquire-release counter, no waiting) adds half 0 and half 1 in that
-//     order and writes C, so the result does not depend on timing.
+//   * When the last wave of tiles would leave most SMs idle, the tiles of
+//     that wave are cut by activation rows into 2 or 4 slices of 128 or 64
+//     rows, each an output tile of its own over the whole k range (N = 128
+//     or 64 MMAs, the activation box as narrow as the slice): a slice costs
+//     about half a tile or less, since the weights' dequantization, not the
+//     MMAs, then paces it, and nothing is added across CTAs.  (o and down at
+//     2048 rows: 160 tiles for 152 SMs, the last 8 as 32 slices.)
+//   * Alternatively each tile's k range is split in two halves done by two
+//     CTAs at the same time: each writes its fp32 partial tile to the
+//     workspace, and the second to arrive (acquire-release counter, no
+//     waiting) adds half 0 and half 1 in that order and writes C, so the
+//     result does not depend on timing.  The host takes whichever of whole
+//     tiles, slices and halves its cost model finds shortest.
 #include "runtime.h"
 #include "sm103_ptx.cuh"
 
@@ -55,9 +63,9 @@ constexpr uint32_t kAcol0 = 0;
 constexpr uint32_t kDcol0 = kASlots * 64;
 constexpr int kWarpProd = 0;
 constexpr int kWarpMma = 1;                       // also owns TMEM
-constexpr int kWarpDq0 = 2;                       // 2..5
-constexpr int kWarpEp0 = 6;                       // 6..9
-constexpr int kWarps = 10;
+constexpr int kWarpDq0 = 2;                       // 2..9: two sets of four, alternate groups
+constexpr int kWarpEp0 = 10;                      // 10..13
+constexpr int kWarps = 14;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kBar = kStages * kStage;
 constexpr int kNumBars = 2 * kStages + 2 * kASlots + 2 + 2;
@@ -70,6 +78,7 @@ constexpr int kBytes = kMisc + 64 + 1024;
 static_assert(kStage % 1024 == 0, "stage alignment");
 static_assert(kBytes <= 227 * 1024, "shared memory plan");
 static_assert(kDcol0 + kTileM <= kTmemCols, "tensor memory plan");
+static_assert(kASlots == 2, "dequant set s fills A slot s (groups alternate between the two)");
 
 struct Args {
     const uint8_t *wq;
@@ -82,16 +91,36 @@ struct Args {
     int M, N, K;
     int n_tiles_n, n_tiles_m, n_groups;
     int halves;              // 1, or 2: each tile's k range done by two CTAs
+    int n_whole;             // halves == 1: items before this are whole tiles,
+    int slices;              // the rest `slices` slices of each later tile
+    int items;
 };
 
-// Work item i: tile i / halves, k groups [g0, g1) of half i % halves.
+// Work item i.  With halves == 2: tile i / 2, k groups of half i % 2.
+// Otherwise the first n_whole items are whole tiles and each later tile is
+// `slices` items of kTileM / slices activation rows, each over the whole k.
 struct Item {
-    int tile, half, g0, g1;
-    __device__ Item(int i, int halves, int G) {
-        tile = halves == 2 ? i >> 1 : i;
-        half = halves == 2 ? i & 1 : 0;
-        g0 = half ? G / 2 : 0;
-        g1 = (halves == 2 && !half) ? G / 2 : G;
+    int tile, half, g0, g1, col0, width;
+    __device__ Item(int i, const Args &p) {
+        const int G = p.n_groups;
+        half = 0;
+        g0 = 0;
+        g1 = G;
+        col0 = 0;
+        width = kTileM;
+        if (p.halves == 2) {
+            tile = i >> 1;
+            half = i & 1;
+            g0 = half ? G / 2 : 0;
+            g1 = half ? G : G / 2;
+        } else if (i < p.n_whole) {
+            tile = i;
+        } else {
+            const int k = i - p.n_whole;
+            width = kTileM / p.slices;
+            tile = p.n_whole + k / p.slices;
+            col0 = (k % p.slices) * width;
+        }
     }
 };
 
@@ -99,7 +128,8 @@ struct Item {
 // scale and zero point (four per block instead of one).
 template <bool kG32>
 __global__ void __launch_bounds__(kThreads, 1)
-w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
+w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap xmap128,
+                     const __grid_constant__ CUtensorMap xmap64, const Args p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -117,17 +147,16 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int items = p.n_tiles_n * p.n_tiles_m * p.halves;
-    const int G = p.n_groups;
+    const int items = p.items;
     AbortState ab{reinterpret_cast<volatile uint32_t *>(&misc[1]), p.status};
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), 4 + 1);          // dequant warps + MMA commit
+            mbar_init(empty(s), 4 + 1);          // the group's dequant set + MMA commit
         }
         for (int a = 0; a < kASlots; ++a) {
-            mbar_init(afull(a), 4);
+            mbar_init(afull(a), 4);              // dequant set a
             mbar_init(aempty(a), 1);
         }
         mbar_init(dfull, 1);
@@ -154,12 +183,16 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
     if (warp == kWarpProd) {
         if (lane == 0) {
             prefetch_tensormap(&xmap);
+            if (p.slices > 1) prefetch_tensormap(p.slices == 2 ? &xmap128 : &xmap64);
             const uint64_t pol_w = l2_policy_evict_last();
             const uint64_t pol_x = l2_policy_evict_last();
             int it = 0;
             for (int i = blockIdx.x; i < items; i += gridDim.x) {
-                const Item w(i, p.halves, G);
+                const Item w(i, p);
                 const int tn = w.tile % p.n_tiles_n, tm = w.tile / p.n_tiles_n;
+                // the activation box is the item's rows only (blocks of width x 128 bytes)
+                const CUtensorMap *xm = w.width == kTileM ? &xmap : (w.width == 128 ? &xmap128 : &xmap64);
+                const uint32_t xbytes = 2u * uint32_t(w.width) * 128u;
                 bool ok = true;
                 for (int g = w.g0; g < w.g1; ++g, ++it) {
                     const int s = it % kStages;
@@ -168,8 +201,8 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                         break;
                     }
                     const uint32_t sa = base_s + s * kStage;
-                    mbar_arrive_expect_tx(full(s), kAct + kBlockBytes);
-                    tma_load_3d(sa, &xmap, 0, tm * kTileM, 2 * g, full(s), pol_x);
+                    mbar_arrive_expect_tx(full(s), xbytes + kBlockBytes);
+                    tma_load_3d(sa, xm, 0, tm * kTileM + w.col0, 2 * g, full(s), pol_x);
                     bulk_load(sa + kAct, p.wq + (size_t(tn) * p.n_groups + g) * kBlockBytes, kBlockBytes, full(s),
                               pol_w);
                 }
@@ -183,11 +216,12 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         // The whole warp runs the loop and lane 0 alone issues, so the
         // operands stay warp-uniform.
         {
-            constexpr uint32_t idesc = idesc_f16_f32(128, kTileM);
             int it = 0, nt = 0;
             bool ok = true;
             for (int i = blockIdx.x; i < items && ok; i += gridDim.x, ++nt) {
-                const Item w(i, p.halves, G);
+                const Item w(i, p);
+                const uint32_t idesc = idesc_f16_f32(128, w.width);
+                const uint32_t xblk = uint32_t(w.width) * 128u;     // one 64-k block of the item's rows
                 if (nt > 0 && !warp_wait(dempty, (nt - 1) & 1, ab)) break;
                 for (int g = w.g0; g < w.g1; ++g, ++it) {
                     const int s = it % kStages;
@@ -201,7 +235,7 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                     const uint32_t act = base_s + s * kStage;
 #pragma unroll
                     for (int j = 0; j < kGroup / 16; ++j) {
-                        const uint32_t baddr = act + (j >> 2) * kActBox + (j & 3) * 32;
+                        const uint32_t baddr = act + (j >> 2) * xblk + (j & 3) * 32;
                         mma_f16_ts_lane0(tmem + kDcol0, tmem + kAcol0 + slot * 64 + 8 * j, sdesc_sw128(baddr), idesc,
                                    (g > w.g0 || j > 0) ? 1u : 0u);
                     }
@@ -214,34 +248,42 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
             mbar_wait_bounded(done_bar, 0);
             __syncwarp();
         }
-    } else if (warp >= kWarpDq0 && warp < kWarpDq0 + 4) {
+    } else if (warp >= kWarpDq0 && warp < kWarpDq0 + 8) {
         const int q = warp & 3;
+        const int set = (warp - kWarpDq0) >> 2;           // groups it with it % 2 == set
         const int r = 32 * q + lane;
         const uint32_t lane_base = uint32_t(32 * q) << 16;
         const __half2 sixteenth = __float2half2_rn(0.0625f);
         int it = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < items && ok; i += gridDim.x) {
-            const Item w(i, p.halves, G);
+            const Item w(i, p);
             const int tn = w.tile % p.n_tiles_n;
             const int n = tn * kTileN + r;
             const bool valid = n < p.N;
             // scale rows per 128-k block: 1, or 4 with group size 32
             constexpr int kSub = kG32 ? 4 : 1;
-            float s_next[kSub];
-#pragma unroll
-            for (int c = 0; c < kSub; ++c)
-                s_next[c] = valid ? __half2float(__ldg(p.scales + size_t(kSub * w.g0 + c) * p.N + n)) : 0.f;
+            // The item's scale (and zero-point) rows are fetched into L2 up
+            // front, one row of the tile's 128 columns per lane of set 0, so
+            // the per-group loads below hit L2.
+            if (set == 0 && tn * kTileN + kTileN <= p.N) {
+                for (int row = 32 * q + lane; row < kSub * (w.g1 - w.g0); row += 128) {
+                    const size_t off = size_t(kSub * w.g0 + row) * p.N + size_t(tn) * kTileN;
+                    const __half *sp = p.scales + off;
+                    if ((reinterpret_cast<uintptr_t>(sp) & 15u) == 0u) prefetch_l2(sp, kTileN * 2);
+                    if (p.zeros != nullptr && (reinterpret_cast<uintptr_t>(p.zeros + off) & 15u) == 0u)
+                        prefetch_l2(p.zeros + off, kTileN);
+                }
+            }
             for (int g = w.g0; g < w.g1; ++g, ++it) {
+                if ((it & 1) != set) continue;
                 const int s = it % kStages;
                 const int slot = it % kASlots;
                 float sc[kSub];
                 uint32_t z[kSub];
 #pragma unroll
                 for (int c = 0; c < kSub; ++c) {
-                    sc[c] = s_next[c];
-                    if (g + 1 < w.g1)
-                        s_next[c] = valid ? __half2float(__ldg(p.scales + size_t(kSub * (g + 1) + c) * p.N + n)) : 0.f;
+                    sc[c] = valid ? __half2float(__ldg(p.scales + size_t(kSub * g + c) * p.N + n)) : 0.f;
                     z[c] = 8;
                     if (p.zeros != nullptr && valid) z[c] = __ldg(p.zeros + size_t(kSub * g + c) * p.N + n);
                 }
@@ -301,18 +343,18 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
         };
         int nt = 0;
         for (int i = blockIdx.x; i < items; i += gridDim.x, ++nt) {
-            const Item w(i, p.halves, G);
+            const Item w(i, p);
             const int tn = w.tile % p.n_tiles_n, tm = w.tile / p.n_tiles_n;
             const int n = tn * kTileN + r;
             float *part = p.partial + (size_t(w.tile) * 2 + w.half) * kPart;
             if (!warp_wait(dfull, nt & 1, ab)) break;
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < kTileM; c += 32) {
+            for (int c = 0; c < w.width; c += 32) {
                 uint32_t d[32];
                 tmem_ld_32x32b_x32(tmem + lane_base + kDcol0 + c, d);
                 tc_wait_ld_keep<32>(d);
-                if (c + 32 == kTileM) {
+                if (c + 32 == w.width) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(dempty);
@@ -321,7 +363,7 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
                     if (n < p.N) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            const int m = tm * kTileM + c + j;
+                            const int m = tm * kTileM + w.col0 + c + j;
                             if (m < p.M) p.C[size_t(m) * p.N + n] = __float2half_rn(__uint_as_float(d[j]));
                         }
                     }
@@ -376,7 +418,8 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const Args p) {
 }
 
 template <bool kG32>
-w4v_status launch(const CUtensorMap &xmap, const Args &a, int grid, cudaStream_t stream) {
+w4v_status launch(const CUtensorMap &xmap, const CUtensorMap &xmap128, const CUtensorMap &xmap64, const Args &a,
+                  int grid, cudaStream_t stream) {
     static int configured_for = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -388,7 +431,8 @@ w4v_status launch(const CUtensorMap &xmap, const Args &a, int grid, cudaStream_t
         }
         configured_for = dev;
     }
-    if (launch_pdl(w4a16_prefill_kernel<kG32>, dim3(grid), dim3(kThreads), kBytes, stream, xmap, a) != cudaSuccess) {
+    if (launch_pdl(w4a16_prefill_kernel<kG32>, dim3(grid), dim3(kThreads), kBytes, stream, xmap, xmap128, xmap64,
+                   a) != cudaSuccess) {
         cudaGetLastError();
         return W4V_ERR_CUDA;
     }
@@ -421,9 +465,16 @@ w4v_status launch_w4a16_prefill(const uint16_t *A, const void *Bq, const uint16_
     a.n_tiles_n = (N + kTileN - 1) / kTileN;
     a.n_tiles_m = (M + kTileM - 1) / kTileM;
     a.n_groups = K / kGroup;
-    CUtensorMap xmap;
+    // activation boxes of a whole tile's rows and of 128- and 64-row slices
+    CUtensorMap xmap, xmap128, xmap64;
     st = encode_tmap_kblocks(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, uint64_t(K), uint64_t(M), 64, kTileM, 2,
                              CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == W4V_OK)
+        st = encode_tmap_kblocks(&xmap128, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, uint64_t(K), uint64_t(M), 64, 128, 2,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == W4V_OK)
+        st = encode_tmap_kblocks(&xmap64, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, uint64_t(K), uint64_t(M), 64, 64, 2,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != W4V_OK) return st;
     const long long tiles = (long long)a.n_tiles_n * a.n_tiles_m;
     // Split each tile's k range in two when that shortens the launch: a
@@ -431,15 +482,37 @@ w4v_status launch_w4a16_prefill(const uint16_t *A, const void *Bq, const uint16_
     // G/2 plus about 4 (its fp32 partial out, and for the second half the
     // sum of both in).  E.g. down (G = 76) at 2048 rows: 160 tiles on 152
     // SMs are two waves of whole tiles, or three of halves.
+    //
+    // Or keep the full waves of whole tiles and cut each tile of a short last
+    // wave into f slices (f * remaining tiles <= SMs, so they are one wave):
+    // a slice of 64 rows costs about 0.45 of a whole tile's time (measured on
+    // down and o at 2048 rows: 0.44-0.59, the dequantization pacing it), one
+    // of 128 rows is taken as 0.6.
     const long long sms = info->sm_count;
     const long long G = a.n_groups;
     const long long waves1 = (tiles + sms - 1) / sms, waves2 = (2 * tiles + sms - 1) / sms;
-    a.halves = (G >= 2 && tiles <= kSplitMaxTiles && waves2 * (G / 2 + 4) < waves1 * (G + 2)) ? 2 : 1;
+    const long long rem = tiles % sms, whole = tiles - rem;
+    const int f = rem == 0 ? 1 : (rem * 4 <= sms ? 4 : (rem * 2 <= sms ? 2 : 1));
+    const double cost_whole = double(waves1) * double(G + 2);
+    const double cost_halves = (G >= 2 && tiles <= kSplitMaxTiles) ? double(waves2) * double(G / 2 + 4) : 1e30;
+    const double cost_slices =
+        f > 1 ? double(whole / sms) * double(G + 2) + double(G) * (f == 4 ? 0.45 : 0.6) + 2.0 : 1e30;
+    a.halves = 1;
+    a.n_whole = static_cast<int>(tiles);
+    a.slices = 1;
+    if (cost_halves < cost_whole && cost_halves <= cost_slices) {
+        a.halves = 2;
+    } else if (cost_slices < cost_whole) {
+        a.n_whole = static_cast<int>(whole);
+        a.slices = f;
+    }
+    a.items = static_cast<int>(a.halves == 2 ? 2 * tiles : a.n_whole + (tiles - a.n_whole) * a.slices);
     const size_t part_bytes = tiles <= kSplitMaxTiles ? size_t(tiles) * 2 * kPart * sizeof(float) : 0;
     a.partial = static_cast<float *>(ws);
     a.tile_cnt = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + part_bytes);
-    const int grid = static_cast<int>(std::min<long long>(sms, tiles * a.halves));
-    return group == 32 ? launch<true>(xmap, a, grid, stream) : launch<false>(xmap, a, grid, stream);
+    const int grid = static_cast<int>(std::min<long long>(sms, a.items));
+    return group == 32 ? launch<true>(xmap, xmap128, xmap64, a, grid, stream)
+                       : launch<false>(xmap, xmap128, xmap64, a, grid, stream);
 }
 
 }  // namespace w4v
