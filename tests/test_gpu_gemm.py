@@ -141,7 +141,7 @@ def test_layer_projection_sampled(w4v_mod, gpu, oracle_mod, proj, M, zeros):
 
 # ---------------------------------------------------------------- prefill (M > 32)
 @pytest.mark.parametrize("M,N,K", [(33, 512, 256), (64, 128, 128), (128, 2560, 2560), (200, 520, 640),
-                                   (256, 1024, 1280), (300, 384, 9728)])
+                                   (256, 1024, 1280), (300, 384, 9728), (768, 2560, 512)])
 def test_prefill_shapes(w4v_mod, gpu, oracle_mod, M, N, K):
     A = inputs.activations(M, M, K, "prefill")
     q = inputs.w4_codes(M, N, K, "prefill")
@@ -178,11 +178,14 @@ def test_prefill_layer_projection_sampled(w4v_mod, gpu, oracle_mod, proj, M):
     assert gemm_rel_err(C[rows, cols], R) <= GEMM_TOL
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 2560, 2560), (2048, 2560, 9728), (2048, 2560, 2560)])
+@pytest.mark.parametrize("M,N,K", [(300, 2560, 2560), (2048, 2560, 9728), (2048, 2560, 2560),
+                                   (700, 2560, 1024)])
 def test_prefill_split_tiles_deterministic_and_clean(w4v_mod, gpu, oracle_mod, M, N, K):
-    """Shapes whose last wave is mostly empty split the k range of tiles
-    between CTAs (fp32 partials added by the last contributor in CTA order;
-    o and down at 2048 rows among them): repeated calls on one workspace are
+    """Shapes whose last wave is mostly empty: the first splits the k range
+    of tiles between CTAs (fp32 partials added by the last contributor in
+    CTA order), o and down at 2048 rows cut the last wave's 8 tiles into 32
+    slices of 64 rows, and 60 tiles with a ragged last row of tiles (700
+    rows) become 120 slices of 128: repeated calls on one workspace are
     bit-identical, the arrival counters are left at zero, and sampled
     outputs match the oracle."""
     A = inputs.activations(M, M, K, "split")
