@@ -528,7 +528,8 @@ def run_e2e_capi(args, step, w4v, torch, total_bytes, gemm_bytes, world):
     pinned host memory, the grouped W4A16 launch and the fused lm_head argmax +
     acceptance (libw4v's C entry points), one cudaMemcpyAsync of the accepted
     length and tokens back, all captured once as a CUDA graph per weight copy;
-    the host launches the graph, synchronizes and reads the accepted length."""
+    the host launches the graph, polls the stream until the step completes and
+    reads the accepted length."""
     import ctypes
     cu = _cudart()
     lib = w4v.load()
@@ -542,6 +543,7 @@ def run_e2e_capi(args, step, w4v, torch, total_bytes, gemm_bytes, world):
     cu.cudaGraphInstantiate.argtypes = [ctypes.POINTER(P), P, ctypes.c_ulonglong]
     cu.cudaGraphLaunch.argtypes = [P, P]
     cu.cudaStreamSynchronize.argtypes = [P]
+    cu.cudaStreamQuery.argtypes = [P]
     cu.cudaGraphExecDestroy.argtypes = [P]
     cu.cudaGraphDestroy.argtypes = [P]
     cu.cudaStreamDestroy.argtypes = [P]
@@ -585,12 +587,19 @@ def run_e2e_capi(args, step, w4v, torch, total_bytes, gemm_bytes, world):
         ok(cu.cudaStreamSynchronize(stream), "cudaStreamSynchronize")
     if world > 1:
         torch.distributed.barrier()
-    launch, sync = cu.cudaGraphLaunch, cu.cudaStreamSynchronize
+    # The host waits for each step by polling the stream (a serving loop's
+    # low-latency wait: no thread wake-up on completion), then reads the result.
+    launch, query = cu.cudaGraphLaunch, cu.cudaStreamQuery
     t0 = time.perf_counter()
     acc = 0
     for i in range(args.steps):
         launch(execs[i % COPIES], stream)
-        sync(stream)
+        while True:
+            q = query(stream)
+            if q == 0:
+                break
+            if q != 600:                     # cudaErrorNotReady: still running
+                raise RuntimeError("cudaStreamQuery failed with CUDA error %d" % q)
         acc += n_acc[0]                      # the host reads the accepted length every step
     ms = reduce_step_time((time.perf_counter() - t0) / args.steps * 1e3, world, step.draft.device)
     for ex, g in zip(execs, graphs):
@@ -605,7 +614,8 @@ def run_e2e_capi(args, step, w4v, torch, total_bytes, gemm_bytes, world):
             "how": "C ABI through ctypes and the CUDA runtime, no torch in the loop: per step one CUDA graph "
                    "(cudaMemcpyAsync of the inputs from pinned host memory, w4a16_gemm_grouped, "
                    "w8_lmhead_argmax_accept, cudaMemcpyAsync of the accepted tokens back), then "
-                   "cudaStreamSynchronize and a host read of the accepted length (wall clock); value = the "
+                   "cudaStreamQuery polled until the step completes and a host read of the accepted length "
+                   "(wall clock); value = the "
                    "W4A16 GEMM bytes of the step over the step's end-to-end time"}
 
 
