@@ -29,7 +29,11 @@
 //     tcgen05.mma.kind::f16 per group with A = weights from TMEM (M = 128),
 //     B = activations from shared memory (N = 256), D in TMEM.
 //   * Four epilogue warps read the finished tile (32-column tcgen05.ld),
-//     round to fp16 and store C.
+//     round to fp16 and store C.  The accumulator is two column halves,
+//     each issued by its own MMA thread into one of three 128-column
+//     regions of tensor memory in rotation, so a tile's epilogue overlaps
+//     the next tile's MMAs (with one 256-column accumulator the epilogue
+//     stalled them: ~10 % of the layer set's time).
 //   * When the last wave of tiles would leave most SMs idle, the tiles of
 //     that wave are cut by activation rows into 2 or 4 slices of 128 or 64
 //     rows, each an output tile of its own over the whole k range (N = 128
@@ -65,10 +69,17 @@ constexpr int kWarpProd = 0;
 constexpr int kWarpMma = 1;                       // also owns TMEM
 constexpr int kWarpDq0 = 2;                       // 2..9: two sets of four, alternate groups
 constexpr int kWarpEp0 = 10;                      // 10..13
-constexpr int kWarps = 14;
+constexpr int kWarpMma2 = 14;                     // second issuer: the upper column half of every tile
+constexpr int kWarps = 15;
 constexpr int kThreads = 32 * kWarps;
+// Accumulators: three 128-column regions after the A slots.  Tile nt's lower
+// and upper column halves go to regions (2 nt) % 3 and (2 nt + 1) % 3, so the
+// next tile's lower half always finds a free region and its upper half waits
+// only for the epilogue to have read this tile's lower half.
+constexpr int kRegions = 3;
+constexpr uint32_t kRegionCols = 128;
 constexpr int kBar = kStages * kStage;
-constexpr int kNumBars = 2 * kStages + 2 * kASlots + 2 + 2;
+constexpr int kNumBars = 2 * kStages + 2 * kASlots + 2 * kRegions + 2;
 constexpr int kPart = kTileM * kTileN;             // floats of one output tile
 // Tiles are split in two k halves only for launches of at most this many
 // tiles (the workspace holds both halves' fp32 partials of every tile).
@@ -77,7 +88,7 @@ constexpr int kMisc = kBar + 8 * kNumBars;
 constexpr int kBytes = kMisc + 64 + 1024;
 static_assert(kStage % 1024 == 0, "stage alignment");
 static_assert(kBytes <= 227 * 1024, "shared memory plan");
-static_assert(kDcol0 + kTileM <= kTmemCols, "tensor memory plan");
+static_assert(kDcol0 + kRegions * kRegionCols <= kTmemCols && 2 * kRegionCols >= kTileM, "tensor memory plan");
 static_assert(kASlots == 2, "dequant set s fills A slot s (groups alternate between the two)");
 
 struct Args {
@@ -139,9 +150,9 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_cons
     auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
     auto afull = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
     auto aempty = [&](int a) { return bar0 + 8u * (2 * kStages + kASlots + a); };
-    const uint32_t dfull = bar0 + 8u * (2 * kStages + 2 * kASlots);
-    const uint32_t dempty = dfull + 8u;
-    const uint32_t done_bar = dempty + 8u;
+    auto rfull = [&](int R) { return bar0 + 8u * (2 * kStages + 2 * kASlots + R); };
+    auto rempty = [&](int R) { return bar0 + 8u * (2 * kStages + 2 * kASlots + kRegions + R); };
+    const uint32_t done_bar = bar0 + 8u * (2 * kStages + 2 * kASlots + 2 * kRegions);
     const uint32_t ep_bar = done_bar + 8u;                            // epilogue warps' sync
     uint32_t *misc = reinterpret_cast<uint32_t *>(base + kMisc);     // [0] tmem, [1] abort, [2] last
 
@@ -153,15 +164,17 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_cons
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full(s), 1);
-            mbar_init(empty(s), 4 + 1);          // the group's dequant set + MMA commit
+            mbar_init(empty(s), 4 + 2);          // the group's dequant set + both issuers' commits
         }
         for (int a = 0; a < kASlots; ++a) {
             mbar_init(afull(a), 4);              // dequant set a
-            mbar_init(aempty(a), 1);
+            mbar_init(aempty(a), 2);
         }
-        mbar_init(dfull, 1);
-        mbar_init(dempty, 4);
-        mbar_init(done_bar, 1);
+        for (int R = 0; R < kRegions; ++R) {
+            mbar_init(rfull(R), 1);              // the issuer of the half using it
+            mbar_init(rempty(R), 4);             // epilogue warps
+        }
+        mbar_init(done_bar, 2);
         mbar_init(ep_bar, 4);
         misc[1] = 0;
         misc[2] = 0;
@@ -212,17 +225,27 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_cons
                 for (int i = max(0, it - kStages); i < it; ++i) mbar_wait_bounded(full(i % kStages), (i / kStages) & 1);
             }
         }
-    } else if (warp == kWarpMma) {
-        // The whole warp runs the loop and lane 0 alone issues, so the
-        // operands stay warp-uniform.
+    } else if (warp == kWarpMma || warp == kWarpMma2) {
+        // Issuer h owns column half h of every whole-width tile (N = 128; each
+        // column's k order is the same as with one N = 256 MMA).  A slice
+        // (64 or 128 rows) is issued whole by issuer 0 -- it has no epilogue
+        // stall to hide, and N = 32 halves ran slower -- while issuer 1 keeps
+        // the same waits and commits with no MMAs.  The whole warp runs the
+        // loop and lane 0 alone issues, so the operands stay warp-uniform.
         {
+            const int h = warp == kWarpMma ? 0 : 1;
             int it = 0, nt = 0;
             bool ok = true;
             for (int i = blockIdx.x; i < items && ok; i += gridDim.x, ++nt) {
                 const Item w(i, p);
-                const uint32_t idesc = idesc_f16_f32(128, w.width);
+                const bool split = w.width == kTileM;
+                const int hw = split ? w.width / 2 : w.width;
+                const bool issue = split || h == 0;
+                const uint32_t idesc = idesc_f16_f32(128, hw);
                 const uint32_t xblk = uint32_t(w.width) * 128u;     // one 64-k block of the item's rows
-                if (nt > 0 && !warp_wait(dempty, (nt - 1) & 1, ab)) break;
+                const int x = 2 * nt + h, R = x % kRegions, u = x / kRegions;   // region R's use u
+                if (u > 0 && !warp_wait(rempty(R), (u - 1) & 1, ab)) break;
+                const uint32_t dcol = tmem + kDcol0 + uint32_t(R) * kRegionCols;
                 for (int g = w.g0; g < w.g1; ++g, ++it) {
                     const int s = it % kStages;
                     const int slot = it % kASlots;
@@ -233,16 +256,18 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_cons
                     }
                     tc_fence_after();
                     const uint32_t act = base_s + s * kStage;
+                    if (issue) {
 #pragma unroll
-                    for (int j = 0; j < kGroup / 16; ++j) {
-                        const uint32_t baddr = act + (j >> 2) * xblk + (j & 3) * 32;
-                        mma_f16_ts_lane0(tmem + kDcol0, tmem + kAcol0 + slot * 64 + 8 * j, sdesc_sw128(baddr), idesc,
-                                   (g > w.g0 || j > 0) ? 1u : 0u);
+                        for (int j = 0; j < kGroup / 16; ++j) {
+                            const uint32_t baddr = act + (j >> 2) * xblk + uint32_t(h * hw) * 128u + (j & 3) * 32;
+                            mma_f16_ts_lane0(dcol, tmem + kAcol0 + slot * 64 + 8 * j, sdesc_sw128(baddr), idesc,
+                                       (g > w.g0 || j > 0) ? 1u : 0u);
+                        }
                     }
                     mma_commit_lane0(empty(s));
                     mma_commit_lane0(aempty(slot));
                 }
-                if (ok) mma_commit_lane0(dfull);
+                if (ok) mma_commit_lane0(rfull(R));
             }
             mma_commit_lane0(done_bar);
             mbar_wait_bounded(done_bar, 0);
@@ -347,31 +372,50 @@ w4a16_prefill_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_cons
             const int tn = w.tile % p.n_tiles_n, tm = w.tile / p.n_tiles_n;
             const int n = tn * kTileN + r;
             float *part = p.partial + (size_t(w.tile) * 2 + w.half) * kPart;
-            if (!warp_wait(dfull, nt & 1, ab)) break;
-            tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < w.width; c += 32) {
-                uint32_t d[32];
-                tmem_ld_32x32b_x32(tmem + lane_base + kDcol0 + c, d);
-                tc_wait_ld_keep<32>(d);
-                if (c + 32 == w.width) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(dempty);
+            // the tile's two column halves (a slice: all of it in the first),
+            // each region released once read
+            const bool split = w.width == kTileM;
+            const int hw = split ? w.width / 2 : w.width;
+            bool got = true;
+            for (int h = 0; h < 2 && got; ++h) {
+                const int x = 2 * nt + h, R = x % kRegions, u = x / kRegions;
+                if (!warp_wait(rfull(R), u & 1, ab)) {
+                    got = false;
+                    break;
                 }
-                if (p.halves == 1) {
-                    if (n < p.N) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int m = tm * kTileM + w.col0 + c + j;
-                            if (m < p.M) p.C[size_t(m) * p.N + n] = __float2half_rn(__uint_as_float(d[j]));
-                        }
+                tc_fence_after();
+                if (!split && h == 1) {                  // nothing was issued into it
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(rempty(R));
+                    continue;
+                }
+                const uint32_t dcol = tmem + lane_base + kDcol0 + uint32_t(R) * kRegionCols;
+#pragma unroll 1
+                for (int c = 0; c < hw; c += 32) {
+                    uint32_t d[32];
+                    tmem_ld_32x32b_x32(dcol + c, d);
+                    tc_wait_ld_keep<32>(d);
+                    if (c + 32 == hw) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(rempty(R));
                     }
-                } else {
+                    const int cc = h * hw + c;           // the item's column
+                    if (p.halves == 1) {
+                        if (n < p.N) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) __stcg(part + (c + j) * kTileN + r, __uint_as_float(d[j]));
+                            for (int j = 0; j < 32; ++j) {
+                                const int m = tm * kTileM + w.col0 + cc + j;
+                                if (m < p.M) p.C[size_t(m) * p.N + n] = __float2half_rn(__uint_as_float(d[j]));
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) __stcg(part + (cc + j) * kTileN + r, __uint_as_float(d[j]));
+                    }
                 }
             }
+            if (!got) break;
             if (p.halves == 1) continue;
             // Split tile: the second half to arrive adds the two fp32 partials,
             // half 0 first (a fixed order, so the result is deterministic).
