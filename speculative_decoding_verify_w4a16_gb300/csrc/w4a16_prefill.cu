@@ -17,23 +17,21 @@
 //
 // Design:
 //   * One CTA per SM computes 128 weight rows x 256 activation rows over the
-//     whole K, tile after tile.  An M128 N256 K16 MMA takes ~136 cycles to
-//     issue against ~96 for N = 128 (twice the work in 1.4x the issue
-//     time), so one issuing thread keeps the tensor pipe ~64% busy, where
-//     two CTAs per SM with N = 128 tiles reached ~50%.
+//     whole K, tile after tile (two CTAs per SM with 128 x 128 tiles kept
+//     the tensor pipe ~50% busy, this ~70%).
 //   * Per 128-k group: one 8 KB bulk copy of packed int4 and one 64 KB 3-D
 //     TMA of the activation slice (128-byte swizzle), three stages.
 //   * Two sets of four dequant warps, taking alternate groups (set s always
 //     fills A slot s), turn a group into fp16 s * (q - z) and write it into
-//     tensor memory (64-column tcgen05.st); one thread issues eight
-//     tcgen05.mma.kind::f16 per group with A = weights from TMEM (M = 128),
-//     B = activations from shared memory (N = 256), D in TMEM.
+//     tensor memory (64-column tcgen05.st).  Two issuing threads each issue
+//     eight tcgen05.mma.kind::f16 per group for one 128-column half of the
+//     tile: A = weights from TMEM (M = 128), B = half the activation rows
+//     from shared memory (N = 128), D in TMEM.
 //   * Four epilogue warps read the finished tile (32-column tcgen05.ld),
-//     round to fp16 and store C.  The accumulator is two column halves,
-//     each issued by its own MMA thread into one of three 128-column
-//     regions of tensor memory in rotation, so a tile's epilogue overlaps
-//     the next tile's MMAs (with one 256-column accumulator the epilogue
-//     stalled them: ~10 % of the layer set's time).
+//     round to fp16 and store C.  The two accumulator halves rotate over
+//     three 128-column regions of tensor memory, so a tile's epilogue
+//     overlaps the next tile's MMAs (with one 256-column accumulator the
+//     epilogue stalled them: ~10 % of the layer set's time).
 //   * When the last wave of tiles would leave most SMs idle, the tiles of
 //     that wave are cut by activation rows into 2 or 4 slices of 128 or 64
 //     rows, each an output tile of its own over the whole k range (N = 128
