@@ -150,8 +150,10 @@ def test_prefill_shapes(w4v_mod, gpu, oracle_mod, M, N, K):
     assert gemm_rel_err(C, oracle_mod.w4a16_gemm(A, q, s)) <= GEMM_TOL
 
 
-def test_prefill_zero_points(w4v_mod, gpu, oracle_mod):
-    M, N, K = 96, 256, 512
+@pytest.mark.parametrize("M,N,K", [(96, 256, 512), (2048, 2560, 512)])
+def test_prefill_zero_points(w4v_mod, gpu, oracle_mod, M, N, K):
+    """Zero tables on the prefill kernel: a few row slices, and 152 whole
+    tiles (each accumulator half from its own issuer) plus 32 slices."""
     A = inputs.activations(8, M, K)
     q = inputs.w4_codes(8, N, K)
     s = inputs.w4_scales(8, N, K)

@@ -78,7 +78,7 @@ def test_zero_points_stream_k(w4v_mod, gpu, oracle_mod, M):
 
 
 @pytest.mark.parametrize("M,N,K", [(33, 512, 256), (128, 2560, 2560), (200, 520, 640), (300, 384, 9728),
-                                   (700, 2560, 512)])
+                                   (700, 2560, 512), (2048, 2560, 512)])
 def test_prefill_sizes(w4v_mod, gpu, oracle_mod, M, N, K):
     A, q, s, _ = _case(M, M, N, K, False, "g32p")
     C = _gemm(w4v_mod, gpu, A, q, s)
